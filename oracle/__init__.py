@@ -1,0 +1,31 @@
+"""Plain float64 CPU oracle for SepLLM's attention hot path.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product package imports, links or
+executes anything here; only the tests, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may use it.
+
+The oracle is written from the SepLLM pages ("SepLLM: Accelerate Large
+Language Models by Compressing One Segment into One Separator", arXiv
+2412.12094), not from the CUDA path, and shares no code, table or constant
+with it.  Its functions take every input as an argument (arrays produced by
+the seeded generators); it holds no random state of its own.
+
+Modules
+-------
+``sepllm``     separator detection, the SepLLM mask, keep-token compaction,
+               per-query-tile block lists, masked softmax attention forward
+               and its textbook backward.
+``streaming``  the four-block streaming KV cache (initial, separator, past
+               window, local window) with eviction into the separator cache,
+               position shifting inside the cache, RoPE and decode attention.
+
+Parity status: every function here is pinned by the ``-m "not gpu"`` tests
+(brute force, reductions to textbook cases, library routines, closed forms
+and the pages' worked example), except the choices the pages leave open and
+that the build declares itself (RoPE theta and variant, the split of the
+streaming window into past and local parts, the moment compression fires,
+the block-list record format).  Those are marked "parity unpinned" where
+they are defined.
+"""
+
+from . import sepllm, streaming  # noqa: F401
