@@ -1,0 +1,195 @@
+// C ABI of the library (declared in include/sepattn.h): host-side argument
+// checks, buffer layouts and kernel launches.  No call here allocates device
+// memory.
+#include <math.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "layout.h"
+
+#define SEP_API extern "C" __attribute__((visibility("default")))
+
+namespace sep {
+
+// The device status word (one per device context); kernels record the first
+// error they meet here.
+__device__ int g_device_status;
+
+size_t attn_fwd_tc_workspace(int B, int Hkv, int L, int d);
+int launch_attn_fwd_tc(IndexPtrs idx, const void* q, const void* k, const void* v, void* o,
+                       float* lse, int B, int Hq, int Hkv, int L, int d, float scale, void* ws,
+                       int* status, void* stream);
+size_t attn_bwd_tc_workspace(int B, int Hq, int Hkv, int L, int d);
+int launch_attn_bwd_tc(IndexPtrs idx, const void* q, const void* k, const void* v, const void* o,
+                       const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                       int Hq, int Hkv, int L, int d, float scale, void* ws, int* status,
+                       void* stream);
+
+namespace {
+
+int* device_status_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  static int* cache[64] = {nullptr};
+  if (dev < 0 || dev >= 64) return nullptr;
+  if (!cache[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+    cache[dev] = static_cast<int*>(p);
+  }
+  return cache[dev];
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+sep_status from_cuda(int e) { return e == 0 ? SEP_OK : SEP_ERR_CUDA; }
+
+bool fill_sep_ids(const int32_t* sep_ids, int n_sep_ids, SepIdList* out) {
+  if (n_sep_ids < 0 || n_sep_ids > SEP_MAX_SEP_IDS) return false;
+  if (n_sep_ids > 0 && !sep_ids) return false;
+  memset(out, 0, sizeof(*out));
+  out->n = n_sep_ids;
+  for (int i = 0; i < n_sep_ids; ++i) out->ids[i] = sep_ids[i];
+  return true;
+}
+
+bool attn_shape_ok(int B, int Hq, int Hkv, int L, int d) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || L < 1) return false;
+  if (Hq % Hkv != 0) return false;
+  if (d != 64 && d != 128) return false;
+  // every offset a kernel forms stays below 2^31 elements per plane index
+  if ((double)B * Hq * L * d >= 9.0e15) return false;
+  return true;
+}
+
+}  // namespace
+}  // namespace sep
+
+using namespace sep;
+
+SEP_API size_t sep_index_bytes(int B, int L, int block_m) {
+  if (B < 1 || L < 1 || block_m < 1) return 0;
+  return index_layout(B, L, block_m).total;
+}
+
+SEP_API sep_status sep_build_index(const int32_t* ids, int B, int L, const int32_t* sep_ids,
+                                   int n_sep_ids, int a, int n, int block_m, void* index_buf,
+                                   size_t index_bytes, void* stream) {
+  if (B < 1 || L < 1 || a < 0 || n < 1 || !ids || !index_buf) return SEP_ERR_INVALID_ARG;
+  if (!aligned(ids, 4) || !aligned(index_buf, 256)) return SEP_ERR_INVALID_ARG;
+  if (block_m != SEP_BLOCK_M) return SEP_ERR_UNSUPPORTED;
+  SepIdList sids;
+  if (!fill_sep_ids(sep_ids, n_sep_ids, &sids)) return SEP_ERR_INVALID_ARG;
+  const IndexLayout lay = index_layout(B, L, block_m);
+  if (index_bytes < lay.total) return SEP_ERR_WORKSPACE;
+  int* st = device_status_ptr();
+  if (!st) return SEP_ERR_CUDA;
+  return from_cuda(launch_build_index(ids, B, L, sids, a, n, block_m,
+                                      index_ptrs(index_buf, lay), st, stream));
+}
+
+SEP_API sep_status sep_index_views(void* index_buf, int B, int L, int block_m,
+                                   int32_t** keep_prefix, int32_t** keep_pos,
+                                   int32_t** keep_count, int32_t** blocks, uint32_t** keep_bits) {
+  if (!index_buf || B < 1 || L < 1 || block_m < 1) return SEP_ERR_INVALID_ARG;
+  const IndexPtrs p = index_ptrs(index_buf, index_layout(B, L, block_m));
+  if (keep_prefix) *keep_prefix = p.keep_prefix;
+  if (keep_pos) *keep_pos = p.keep_pos;
+  if (keep_count) *keep_count = p.keep_count;
+  if (blocks) *blocks = p.blocks;
+  if (keep_bits) *keep_bits = p.keep_bits;
+  return SEP_OK;
+}
+
+SEP_API size_t sep_attn_workspace_bytes(int B, int Hq, int Hkv, int L, int d, sep_dtype dtype,
+                                        int backward) {
+  if (!attn_shape_ok(B, Hq, Hkv, L, d)) return 0;
+  if (dtype == SEP_F32) return backward ? 0 : 256;
+  if (backward) return attn_bwd_tc_workspace(B, Hq, Hkv, L, d);
+  return attn_fwd_tc_workspace(B, Hkv, L, d);
+}
+
+SEP_API sep_status sep_attn_fwd(const void* index_buf, const void* q, const void* k,
+                                const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                                int L, int d, sep_dtype dtype, float scale, void* ws,
+                                size_t ws_bytes, void* stream) {
+  if (!index_buf || !q || !k || !v || !o || !lse) return SEP_ERR_INVALID_ARG;
+  if (!attn_shape_ok(B, Hq, Hkv, L, d)) {
+    if (B >= 1 && Hq >= 1 && Hkv >= 1 && L >= 1 && Hq % Hkv == 0) return SEP_ERR_UNSUPPORTED;
+    return SEP_ERR_INVALID_ARG;
+  }
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(lse, 4) || !aligned(index_buf, 256))
+    return SEP_ERR_INVALID_ARG;
+  if (!(scale > 0.f)) scale = 1.0f / sqrtf(static_cast<float>(d));
+  if (dtype != SEP_F32 && dtype != SEP_BF16) return SEP_ERR_UNSUPPORTED;
+  if (dtype == SEP_BF16) {
+    const size_t need = attn_fwd_tc_workspace(B, Hkv, L, d);
+    if (!ws || ws_bytes < need) return SEP_ERR_WORKSPACE;
+    if (!aligned(ws, 256)) return SEP_ERR_INVALID_ARG;
+  }
+  int* st = device_status_ptr();
+  if (!st) return SEP_ERR_CUDA;
+  const IndexPtrs idx = index_ptrs(const_cast<void*>(index_buf), index_layout(B, L, SEP_BLOCK_M));
+  if (dtype == SEP_F32) {
+    return from_cuda(launch_attn_fwd_simt(idx, static_cast<const float*>(q),
+                                          static_cast<const float*>(k),
+                                          static_cast<const float*>(v), static_cast<float*>(o),
+                                          lse, B, Hq, Hkv, L, d, scale, st, stream));
+  }
+  return from_cuda(launch_attn_fwd_tc(idx, q, k, v, o, lse, B, Hq, Hkv, L, d, scale, ws, st,
+                                      stream));
+}
+
+SEP_API sep_status sep_attn_bwd(const void* index_buf, const void* q, const void* k,
+                                const void* v, const void* o, const float* lse,
+                                const void* dout, void* dq, void* dk, void* dv, int B, int Hq,
+                                int Hkv, int L, int d, sep_dtype dtype, float scale, void* ws,
+                                size_t ws_bytes, void* stream) {
+  if (!index_buf || !q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv)
+    return SEP_ERR_INVALID_ARG;
+  if (!attn_shape_ok(B, Hq, Hkv, L, d)) {
+    if (B >= 1 && Hq >= 1 && Hkv >= 1 && L >= 1 && Hq % Hkv == 0) return SEP_ERR_UNSUPPORTED;
+    return SEP_ERR_INVALID_ARG;
+  }
+  if (dtype != SEP_BF16) return SEP_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
+      !aligned(lse, 4) || !aligned(index_buf, 256))
+    return SEP_ERR_INVALID_ARG;
+  const size_t need = attn_bwd_tc_workspace(B, Hq, Hkv, L, d);
+  if (!ws || ws_bytes < need) return SEP_ERR_WORKSPACE;
+  if (!aligned(ws, 256)) return SEP_ERR_INVALID_ARG;
+  if (!(scale > 0.f)) scale = 1.0f / sqrtf(static_cast<float>(d));
+  int* st = device_status_ptr();
+  if (!st) return SEP_ERR_CUDA;
+  const IndexPtrs idx = index_ptrs(const_cast<void*>(index_buf), index_layout(B, L, SEP_BLOCK_M));
+  return from_cuda(launch_attn_bwd_tc(idx, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, L, d,
+                                      scale, ws, st, stream));
+}
+
+SEP_API sep_status sep_get_device_status(void) {
+  int* st = device_status_ptr();
+  if (!st) return SEP_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return SEP_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, st, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return SEP_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpy(st, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+    return SEP_ERR_CUDA;
+  return static_cast<sep_status>(v);
+}
+
+SEP_API const char* sep_status_string(sep_status s) {
+  switch (s) {
+    case SEP_OK: return "ok";
+    case SEP_ERR_INVALID_ARG: return "invalid argument";
+    case SEP_ERR_UNSUPPORTED: return "unsupported configuration";
+    case SEP_ERR_CAPACITY: return "cache capacities violate a + s + w < c";
+    case SEP_ERR_CUDA: return "CUDA runtime error";
+    case SEP_ERR_TIMEOUT: return "device wait timed out";
+    case SEP_ERR_DEVICE_BOUNDS: return "device index or count out of range";
+    case SEP_ERR_WORKSPACE: return "buffer smaller than the size query";
+  }
+  return "unknown status";
+}
