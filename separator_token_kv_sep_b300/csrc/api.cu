@@ -25,8 +25,6 @@ int launch_attn_bwd_tc(IndexPtrs idx, const void* q, const void* k, const void* 
                        int Hq, int Hkv, int L, int d, float scale, void* ws, int* status,
                        void* stream);
 
-namespace {
-
 int* device_status_ptr() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
@@ -39,6 +37,8 @@ int* device_status_ptr() {
   }
   return cache[dev];
 }
+
+namespace {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 

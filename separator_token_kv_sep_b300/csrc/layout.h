@@ -74,6 +74,10 @@ inline IndexPtrs index_ptrs(void* buf, const IndexLayout& l) {
   return r;
 }
 
+// Device address of the library's status word on the current device (null if
+// the CUDA runtime is unavailable).  Defined in api.cu.
+int* device_status_ptr();
+
 // ---------------------------------------------------------------------------
 // Host launchers (each defined in the kernel file named beside it).
 // Every launcher enqueues on `stream` and returns the launch's cudaError_t.

@@ -82,3 +82,24 @@ def test_index_views_offsets_on_host():
         for (o1, s1), o2 in zip(zip(offs, sizes), offs[1:]):
             assert o1 + s1 <= o2
         assert offs[-1] + sizes[-1] <= L_.sep_index_bytes(B, L, 128)
+
+
+def test_cache_host_checks():
+    from separator_token_kv_sep_b300 import api
+    L_ = api.library()
+    good = api.cache_params(64, 8, 128, 4, 32, 256, 324)
+    assert L_.sep_cache_bytes(ctypes.byref(good)) > 0
+    assert L_.sep_cache_export_bytes(ctypes.byref(good)) > 0
+    full = api.cache_params(64, 8, 128, 4, 32, 288, 324)   # a + s + w == c: no room to compress
+    assert L_.sep_cache_bytes(ctypes.byref(full)) == 0
+    assert L_.sep_cache_init(ctypes.byref(full), ctypes.c_void_p(256), 1 << 30, None) == 3
+    wide = api.cache_params(4, 16, 128, 4, 32, 256, 324)   # more kv heads than a cluster holds
+    assert L_.sep_cache_init(ctypes.byref(wide), ctypes.c_void_p(256), 1 << 30, None) == 2
+    assert L_.sep_cache_init(ctypes.byref(good), ctypes.c_void_p(256), 100, None) == 7
+    P = ctypes.c_void_p(4096)
+    arr = (ctypes.c_int32 * 1)(1)
+    # q given without out, and Hq not a multiple of Hkv
+    assert L_.sep_cache_step(ctypes.byref(good), P, P, P, P, P, arr, 1, None, 32,
+                             ctypes.c_float(0), None) == 1
+    assert L_.sep_cache_step(ctypes.byref(good), P, P, P, P, P, arr, 1, P, 30,
+                             ctypes.c_float(0), None) == 1
