@@ -1,0 +1,540 @@
+#!/usr/bin/env python
+"""Benchmark of the SepLLM attention hot path on B300.
+
+One timed step = sep_build_index + sep_attn_fwd + sep_attn_bwd on the
+Pythia-160M-shaped training workload (B8 H12 L2048 d64, a=4, n=128,
+separator probability 0.10), replayed from a CUDA graph with L2 flushed
+(256 MiB write) between steps and device time taken from CUDA events.
+Also measured, in sub-objects of the same JSON line: streaming decode on the
+Llama-3-8B-shaped workload (64 sequences, c = 324, 2048 prompt tokens then
+4096 decode steps; tokens/s against HBM bandwidth) and forward-only prefill
+at L = 8192 and L = 65536.
+
+FLOPs are counted over visited (unmasked) pairs only: 4 d per pair for the
+forward, 10 d per pair for the backward, per q head.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+For N > 1 the script runs under torch.distributed.run, one rank per GPU;
+every rank processes its own batch (weak scaling, no collective on the data
+path) and rank 0 prints the line with the max time over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from separator_token_kv_sep_b300 import synth  # noqa: E402
+
+METRIC = "Sep-Attention fwd+bwd TFLOP/s (visited pairs) & decode tok/s; % roofline"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+            "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# Work accounting (bookkeeping only; the computation itself runs in the
+# library's kernels)
+# ---------------------------------------------------------------------------
+
+def visited_pairs_per_head(ids: np.ndarray, a: int, n: int) -> int:
+    """Sum over the batch of the unmasked pairs of one head: row i sees the
+    keep tokens before its window start W(i) plus the whole window [W(i), i]."""
+    keep = np.isin(ids, synth.SEP_IDS) | (np.arange(ids.shape[1]) < a)[None, :]
+    kp = np.concatenate([np.zeros((ids.shape[0], 1), np.int64), np.cumsum(keep, axis=1)], axis=1)
+    i = np.arange(ids.shape[1])
+    W = np.maximum(0, i - n + 1)
+    return int((kp[:, W] + (i - W + 1)[None, :]).sum())
+
+
+def decode_cache_lengths(sep: np.ndarray, a: int, s: int, w: int, c: int) -> np.ndarray:
+    """Entries each sequence's cache holds after each step (new token
+    included), from counts alone: tokens [a, cp) have been through
+    compression, the separator block keeps the last <= s separators among
+    them, and [max(a, cp), t] is the past + local window."""
+    T, S = sep.shape
+    csum = np.concatenate([np.zeros((1, S), np.int64), np.cumsum(sep, axis=0)], axis=0)
+    cp = np.full(S, a, np.int64)
+    out = np.zeros((T, S), np.int64)
+    cols = np.arange(S)
+    for t in range(T):
+        if t >= a:
+            n_sep = np.minimum(s, csum[cp, cols] - csum[a, cols])
+            total = a + n_sep + (t - cp)
+            cp = np.where(total == c, np.maximum(cp, t - w), cp)
+            n_sep = np.minimum(s, csum[cp, cols] - csum[a, cols])
+            out[t] = a + n_sep + (t + 1 - np.maximum(a, cp))
+        else:
+            out[t] = t + 1
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the timed regions
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        rows = []
+        if self.path and os.path.exists(self.path):
+            with open(self.path) as f:
+                for line in f:
+                    parts = [x.strip() for x in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4)
+                          if r[5 + k].lower().startswith("active")})
+        loaded = sorted(sm)[len(sm) // 2:] if sm else []
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, rank, world, device):
+    import torch
+    from separator_token_kv_sep_b300 import api
+
+    torch.cuda.set_device(device)
+    peaks = load_peaks()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream()
+
+    # ---------------------------------------------------------- train step
+    cfg = synth.PYTHIA_TRAIN_N128
+    q_np, k_np, v_np, do_np, ids_np = synth.prefill_inputs(cfg, seed=cfg.seed + rank)
+    bf = torch.bfloat16
+    q = torch.from_numpy(q_np).to(device, bf)
+    k = torch.from_numpy(k_np).to(device, bf)
+    v = torch.from_numpy(v_np).to(device, bf)
+    dout = torch.from_numpy(do_np).to(device, bf)
+    ids = torch.from_numpy(ids_np).to(device)
+    B, Hq, L, d = q.shape
+    Hkv = k.shape[1]
+    pairs = visited_pairs_per_head(ids_np, cfg.a, cfg.n)
+    fwd_flops = 4.0 * d * pairs * Hq
+    bwd_flops = 10.0 * d * pairs * Hq
+    idx_buf = torch.empty(api.sep_index_bytes(B, L), dtype=torch.uint8, device=device)
+    ws_f = torch.empty(api.sep_attn_workspace_bytes(B, Hq, Hkv, L, d, api.SEP_BF16, False),
+                       dtype=torch.uint8, device=device)
+    ws_b = torch.empty(api.sep_attn_workspace_bytes(B, Hq, Hkv, L, d, api.SEP_BF16, True),
+                       dtype=torch.uint8, device=device)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, L), dtype=torch.float32, device=device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+
+    def train_step(mark=False):
+        if mark:
+            ev[0].record()
+        api.sep_build_index(ids, synth.SEP_IDS, cfg.a, cfg.n, index_buf=idx_buf)
+        if mark:
+            ev[1].record()
+        api.sep_attn_fwd(idx_buf, q, k, v, o=o, lse=lse, ws=ws_f)
+        if mark:
+            ev[2].record()
+        api.sep_attn_bwd(idx_buf, q, k, v, o, lse, dout, dq=dq, dk=dk, dv=dv, ws=ws_b)
+        if mark:
+            ev[3].record()
+
+    for _ in range(2):
+        train_step()
+    torch.cuda.synchronize()
+    assert api.sep_get_device_status() == 0
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        train_step(mark=True)
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        graph.replay()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(device.index if device.index is not None else 0)
+    t_idx, t_fwd, t_bwd, t_step = [], [], [], []
+    with sampler:
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        for _ in range(args.steps):
+            flush.zero_()
+            graph.replay()
+            torch.cuda.synchronize()
+            t_idx.append(ev[0].elapsed_time(ev[1]))
+            t_fwd.append(ev[1].elapsed_time(ev[2]))
+            t_bwd.append(ev[2].elapsed_time(ev[3]))
+            t_step.append(ev[0].elapsed_time(ev[3]))
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        total_ms = sum(t_step)
+        total_ms = max_over_ranks(total_ms, world)
+        decode = run_decode(args, rank, device, flush, peaks)
+        prefill = run_prefill(args, rank, device, flush, peaks)
+    assert api.sep_get_device_status() == 0
+    clocks = sampler.summary()
+
+    ms_per_step = total_ms / args.steps
+    value = (fwd_flops + bwd_flops) * world * args.steps / (total_ms * 1e-3) / 1e12
+    mean = lambda xs: sum(xs) / len(xs)
+    fwd_ms, bwd_ms, idx_ms = mean(t_fwd), mean(t_bwd), mean(t_idx)
+    fwd_tf = fwd_flops / (fwd_ms * 1e-3) / 1e12
+    bwd_tf = bwd_flops / (bwd_ms * 1e-3) / 1e12
+
+    # ------------------------------------------------------------ e2e
+    e2e = run_e2e(api, cfg, q_np, k_np, v_np, do_np, ids_np, device, args, fwd_flops + bwd_flops,
+                  world)
+
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; separator ids 1..9 stand in for . , ? ! ; : space tab newline)",
+        "config": {"workload": "pythia160m_train_step " + cfg.describe() +
+                   " = sep_build_index + sep_attn_fwd + sep_attn_bwd (CUDA graph replay)",
+                   "visited_pairs_per_head": pairs, "visited_over_causal":
+                       round(pairs / (B * L * (L + 1) / 2), 4),
+                   "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas x{world}"},
+        "phases_ms": {"index": round(idx_ms, 5), "fwd": round(fwd_ms, 5), "bwd": round(bwd_ms, 5),
+                      "fwd_tflops": round(fwd_tf, 2), "bwd_tflops": round(bwd_tf, 2)},
+        "roofline": {
+            "bound": "tensor", "kernel": "sep_attn_bwd call (5 kernels; the dominant phase)",
+            "achieved": round(bwd_tf, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": round(bwd_tf / peaks["bf16_tflops"], 4),
+            "frac_of_sustained": round(bwd_tf / peaks["bf16_tflops_sustained"], 4)
+            if peaks.get("bf16_tflops_sustained") else None,
+            "peak_source": peaks["source"] + " (burst bf16)", "traffic": None},
+        "e2e": e2e,
+        "clocks": clocks,
+        "gpu_launches": 8 * args.steps,
+        "decode": decode,
+        "prefill": prefill,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_train(cfg, q_np, k_np, v_np, do_np, ids_np)
+    return line
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_e2e(api, cfg, q_np, k_np, v_np, do_np, ids_np, device, args, flops, world):
+    """The same step through the public API from pinned host buffers: H2D of
+    the inputs, index + forward + backward, D2H of the gradients."""
+    import torch
+    bf = torch.bfloat16
+    hq = torch.from_numpy(q_np).to(bf).pin_memory()
+    hk = torch.from_numpy(k_np).to(bf).pin_memory()
+    hv = torch.from_numpy(v_np).to(bf).pin_memory()
+    hdo = torch.from_numpy(do_np).to(bf).pin_memory()
+    hids = torch.from_numpy(ids_np).pin_memory()
+    q, k, v, dout = (torch.empty_like(x, device=device) for x in (hq, hk, hv, hdo))
+    ids = torch.empty_like(hids, device=device)
+    dq_h = torch.empty_like(hq).pin_memory()
+    dk_h = torch.empty_like(hk).pin_memory()
+    dv_h = torch.empty_like(hv).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdo, hids))
+    d2h = sum(x.numel() * x.element_size() for x in (dq_h, dk_h, dv_h))
+
+    def step():
+        for dst, src in ((q, hq), (k, hk), (v, hv), (dout, hdo), (ids, hids)):
+            dst.copy_(src, non_blocking=True)
+        buf = api.sep_build_index(ids, synth.SEP_IDS, cfg.a, cfg.n)
+        o, lse = api.sep_attn_fwd(buf, q, k, v)
+        dq, dk, dv = api.sep_attn_bwd(buf, q, k, v, o, lse, dout)
+        dq_h.copy_(dq, non_blocking=True)
+        dk_h.copy_(dk, non_blocking=True)
+        dv_h.copy_(dv, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    n = max(5, args.steps)
+    t0 = time.perf_counter()
+    for _ in range(n):
+        step()
+    torch.cuda.synchronize()
+    dt = max_over_ranks(time.perf_counter() - t0, world)
+    return {"value": round(flops * world * n / dt / 1e12, 3), "unit": "TFLOP/s",
+            "ms_per_step": round(dt / n * 1e3, 4), "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+            "note": "public API, eager launches, pinned host buffers, wall clock"}
+
+
+def run_decode(args, rank, device, flush, peaks):
+    """Streaming decode: prompt tokens enter through update-only steps
+    (untimed), then every decode step (cache update + attention over the
+    cache) is timed by CUDA events with L2 flushed before it."""
+    import torch
+    from separator_token_kv_sep_b300 import api
+    cfg = synth.STREAM_DECODE
+    qp, kp, vp, ids_np = synth.stream_inputs(cfg, seed=cfg.seed + rank)
+    P = qp.shape[0]
+    bf = torch.bfloat16
+    dq = torch.from_numpy(qp).to(device, bf)
+    dk = torch.from_numpy(kp).to(device, bf)
+    dv = torch.from_numpy(vp).to(device, bf)
+    dids = torch.from_numpy(ids_np).to(device)
+    out = torch.empty((cfg.S, cfg.Hq, cfg.d), dtype=bf, device=device)
+    p = api.cache_params(cfg.S, cfg.Hkv, cfg.d, cfg.a, cfg.s, cfg.w, cfg.c, cfg.theta)
+    buf = api.sep_cache_init(p, device=device)
+    T = cfg.prompt + cfg.steps
+    for t in range(cfg.prompt):
+        api.sep_cache_step(p, buf, None, dk[t % P], dv[t % P], dids[t], synth.SEP_IDS, Hq=cfg.Hq)
+    torch.cuda.synchronize()
+    n_dec = cfg.steps
+    ev_a = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n_dec)]
+    ev_b = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n_dec)]
+    graph = torch.cuda.CUDAGraph()
+    # capture the whole decode phase: flush, event, step, event per token
+    with torch.cuda.graph(graph):
+        for j in range(n_dec):
+            t = cfg.prompt + j
+            flush.zero_()
+            ev_a[j].record()
+            api.sep_cache_step(p, buf, dq[t % P], dk[t % P], dv[t % P], dids[t], synth.SEP_IDS,
+                               out=out)
+            ev_b[j].record()
+    # the capture did not run anything: the cache is still at the end of the prompt
+    graph.replay()
+    torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(b) for a, b in zip(ev_a, ev_b)]
+    total_ms = sum(step_ms)
+    assert api.sep_get_device_status() == 0
+    sep = np.isin(ids_np, synth.SEP_IDS)
+    lens = decode_cache_lengths(sep, cfg.a, cfg.s, cfg.w, cfg.c)[cfg.prompt:T]
+    G = cfg.Hq // cfg.Hkv
+    # K and V rows read once per kv head; q, out, new k/v and ids
+    kv_bytes = lens.sum() * cfg.Hkv * cfg.d * 2 * 2
+    io_bytes = n_dec * cfg.S * (2 * cfg.Hq * cfg.d * 2 + 2 * cfg.Hkv * cfg.d * 2 + 4)
+    alg_bytes = float(kv_bytes + io_bytes)
+    gbs = alg_bytes / (total_ms * 1e-3) / 1e9
+    tok_s = cfg.S * n_dec / (total_ms * 1e-3)
+    return {"workload": "llama3_8b_stream_decode " + cfg.describe(),
+            "value": round(tok_s, 1), "unit": "tok/s", "ms_per_step": round(total_ms / n_dec, 5),
+            "mean_cache_entries": round(float(lens.mean()), 2), "gqa_group": G,
+            "l2": "flushed before every decode step (256 MiB write)",
+            "roofline": {"bound": "hbm", "kernel": "cache_step_kernel (one launch per step)",
+                         "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(gbs / peaks["hbm_gbs"], 4),
+                         "traffic": None, "algorithmic_bytes_per_step": round(alg_bytes / n_dec)},
+            "gpu_launches": n_dec}
+
+
+def run_prefill(args, rank, device, flush, peaks):
+    """Forward-only prefill at L = 8192 and L = 65536 (index + forward)."""
+    import torch
+    from separator_token_kv_sep_b300 import api
+    res = {}
+    for cfg, reps in ((synth.LLAMA_PREFILL, 10), (synth.LONG_PREFILL, 3)):
+        rng = np.random.Generator(np.random.PCG64(cfg.seed + rank))
+        ids_np = synth.token_ids(rng, (cfg.B, cfg.L), cfg.p)
+        gen = torch.Generator(device=device)
+        gen.manual_seed(cfg.seed + rank)
+        bf = torch.bfloat16
+        q = torch.randn((cfg.B, cfg.Hq, cfg.L, cfg.d), generator=gen, device=device).to(bf)
+        k = torch.randn((cfg.B, cfg.Hkv, cfg.L, cfg.d), generator=gen, device=device).to(bf)
+        v = torch.randn((cfg.B, cfg.Hkv, cfg.L, cfg.d), generator=gen, device=device).to(bf)
+        ids = torch.from_numpy(ids_np).to(device)
+        idx_buf = api.sep_build_index(ids, synth.SEP_IDS, cfg.a, cfg.n)
+        o, lse = api.sep_attn_fwd(idx_buf, q, k, v)
+        ws = torch.empty(api.sep_attn_workspace_bytes(cfg.B, cfg.Hq, cfg.Hkv, cfg.L, cfg.d,
+                                                      api.SEP_BF16, False),
+                         dtype=torch.uint8, device=device)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        times = []
+        for it in range(reps + 2):
+            flush.zero_()
+            e0.record()
+            api.sep_attn_fwd(idx_buf, q, k, v, o=o, lse=lse, ws=ws)
+            e1.record()
+            torch.cuda.synchronize()
+            if it >= 2:
+                times.append(e0.elapsed_time(e1))
+        pairs = visited_pairs_per_head(ids_np, cfg.a, cfg.n)
+        flops = 4.0 * cfg.d * pairs * cfg.Hq
+        ms = sum(times) / len(times)
+        tf = flops / (ms * 1e-3) / 1e12
+        res[cfg.name] = {"workload": cfg.describe(), "ms": round(ms, 4),
+                         "value": round(tf, 2), "unit": "TFLOP/s",
+                         "visited_over_causal": round(pairs / (cfg.B * cfg.L * (cfg.L + 1) / 2), 4),
+                         "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
+                         "note": "sep_attn_fwd call (gather + attention kernel), events on the "
+                                 "launching stream, L2 flushed before each call; inputs drawn "
+                                 "on the device with torch's seeded generator"}
+    return res
+
+
+# ---------------------------------------------------------------------------
+# CPU baselines (the float64 oracle, as it stands)
+# ---------------------------------------------------------------------------
+
+def _cores() -> int:
+    return len(os.sched_getaffinity(0))
+
+
+def cpu_baseline_train(cfg, q_np, k_np, v_np, do_np, ids_np, batches=(0,)):
+    from oracle import sepllm as O
+    bs = list(batches)
+    t0 = time.perf_counter()
+    O.attention_forward(q_np[bs], k_np[bs], v_np[bs], ids_np[bs], synth.SEP_IDS, cfg.a, cfg.n)
+    O.attention_backward(q_np[bs], k_np[bs], v_np[bs], do_np[bs], ids_np[bs], synth.SEP_IDS,
+                         cfg.a, cfg.n)
+    dt = time.perf_counter() - t0
+    pairs = visited_pairs_per_head(ids_np[bs], cfg.a, cfg.n)
+    flops = 14.0 * cfg.d * pairs * cfg.Hq
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": _cores(),
+            "kind": "oracle", "seconds": round(dt, 3),
+            "sample": f"batch rows {bs} of the training workload ({len(bs)}/{cfg.B} of it), "
+                      "float64 NumPy forward + backward with explicit masks"}
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: each step is one batch row of the
+    training workload (forward + backward, float64 NumPy)."""
+    if rank != 0:
+        return None
+    cfg = synth.PYTHIA_TRAIN_N128
+    q_np, k_np, v_np, do_np, ids_np = synth.prefill_inputs(cfg)
+    from oracle import sepllm as O
+    heads = [0, 1]
+
+    def step(b):
+        sl = slice(b, b + 1)
+        qq, kk, vv, dd = (x[sl][:, heads] for x in (q_np, k_np, v_np, do_np))
+        O.attention_forward(qq, kk, vv, ids_np[sl], synth.SEP_IDS, cfg.a, cfg.n)
+        O.attention_backward(qq, kk, vv, dd, ids_np[sl], synth.SEP_IDS, cfg.a, cfg.n)
+
+    for w in range(args.warmup):
+        step(w % cfg.B)
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        step(s % cfg.B)
+    dt = time.perf_counter() - t0
+    pairs = sum(visited_pairs_per_head(ids_np[s % cfg.B:s % cfg.B + 1], cfg.a, cfg.n)
+                for s in range(args.steps))
+    flops = 14.0 * cfg.d * pairs * len(heads)
+    value = flops / dt / 1e12
+    sample = (f"each step: one batch row, q heads {heads} of the training workload "
+              f"(forward + backward, float64 NumPy)")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "pythia160m_train_step " + cfg.describe()},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": _cores(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", str(args.gpus if args.gpus == 1 else 1)))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return 0
+    import torch
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(device)
+        dist.init_process_group("nccl", device_id=device)
+    line = run_ours(args, rank, world, device)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
