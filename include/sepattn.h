@@ -48,7 +48,8 @@ typedef enum {
   SEP_ERR_CUDA = 4,          /* a CUDA runtime call failed */
   SEP_ERR_TIMEOUT = 5,       /* device: a bounded wait expired */
   SEP_ERR_DEVICE_BOUNDS = 6, /* device: an index or count was out of range */
-  SEP_ERR_WORKSPACE = 7      /* workspace / buffer smaller than the size query */
+  SEP_ERR_WORKSPACE = 7,     /* workspace / buffer smaller than the size query */
+  SEP_ERR_TOO_LARGE = 8      /* request exceeds the fixed scratch of sep_attn_fwd_static */
 } sep_status;
 
 typedef enum { SEP_F32 = 0, SEP_BF16 = 1 } sep_dtype;
@@ -166,6 +167,44 @@ sep_status sep_attn_bwd(const void* index_buf, const void* q, const void* k,
                         const void* dout, void* dq, void* dk, void* dv,
                         int B, int Hq, int Hkv, int L, int d, sep_dtype dtype,
                         float scale, void* ws, size_t ws_bytes, void* stream);
+
+/* Size of the fixed device scratch array behind sep_attn_fwd_static. */
+#define SEP_STATIC_SCRATCH_BYTES (64u << 20)
+
+/* sep_attn_fwd_static -- sep_attn_fwd for callers that cannot allocate.
+ *
+ * The paper has no counterpart to this call; it exists for library users.
+ * Some callers cannot call cudaMalloc or any allocating routine: code inside
+ * an allocator callback or out-of-memory handler, a plug-in whose host
+ * framework owns all device memory, a real-time loop that allocates nothing
+ * after start-up.  sep_attn_fwd needs a caller-provided workspace; this call
+ * needs none.  It computes exactly what sep_attn_fwd computes for
+ * dtype = SEP_BF16, with the gathered keep-token K/V rows held in a fixed
+ * device array of SEP_STATIC_SCRATCH_BYTES (64 MiB) inside the library.
+ * It calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * Arguments, layouts and the index are those of sep_attn_fwd (bf16 only;
+ * d 64 or 128).  The caller still allocates q, k, v, o, lse and the index.
+ * Limit: the forward workspace, sep_attn_workspace_bytes(B, Hq, Hkv, L, d,
+ * SEP_BF16, 0) (about 4 * B * Hkv * L * d bytes), must not exceed
+ * SEP_STATIC_SCRATCH_BYTES; larger shapes return SEP_ERR_TOO_LARGE before
+ * any device work.
+ *
+ * The scratch array:
+ *  - is held by every GPU that loads the library, until the process exits;
+ *  - is found on each device by the first call made with that device
+ *    current (cudaGetSymbolAddress); make that first call before any stream
+ *    capture;
+ *  - is shared by every call and keeps the last call's contents.  Calls do
+ *    not depend on them: every scratch row a call reads, it first writes.
+ *    Calls that overlap on the GPU (other streams, unordered host threads)
+ *    race on it, so the caller must order them.
+ * Errors: SEP_ERR_INVALID_ARG, SEP_ERR_UNSUPPORTED, SEP_ERR_TOO_LARGE,
+ * SEP_ERR_CUDA; device errors as sep_attn_fwd. */
+sep_status sep_attn_fwd_static(const void* index_buf, const void* q, const void* k,
+                               const void* v, void* o, float* lse,
+                               int B, int Hq, int Hkv, int L, int d, float scale,
+                               void* stream);
 
 /* ======================================================================
  * Streaming four-block KV cache and decode attention

@@ -24,13 +24,14 @@ SEP_MAX_SEP_IDS = 64
 
 STATUS = {0: "SEP_OK", 1: "SEP_ERR_INVALID_ARG", 2: "SEP_ERR_UNSUPPORTED",
           3: "SEP_ERR_CAPACITY", 4: "SEP_ERR_CUDA", 5: "SEP_ERR_TIMEOUT",
-          6: "SEP_ERR_DEVICE_BOUNDS", 7: "SEP_ERR_WORKSPACE"}
+          6: "SEP_ERR_DEVICE_BOUNDS", 7: "SEP_ERR_WORKSPACE", 8: "SEP_ERR_TOO_LARGE"}
+SEP_STATIC_SCRATCH_BYTES = 64 << 20
 
 EXPORTED = ["sep_index_bytes", "sep_build_index", "sep_index_views",
             "sep_attn_workspace_bytes", "sep_attn_fwd", "sep_attn_bwd",
             "sep_cache_bytes", "sep_cache_init", "sep_cache_step",
             "sep_cache_export_bytes", "sep_cache_export", "sep_cache_import",
-            "sep_get_device_status", "sep_status_string"]
+            "sep_get_device_status", "sep_status_string", "sep_attn_fwd_static"]
 
 
 class SepError(RuntimeError):
@@ -68,6 +69,7 @@ def _load() -> ctypes.CDLL:
         "sep_cache_import": (I, [CP, P, P, Z, P]),
         "sep_get_device_status": (I, []),
         "sep_status_string": (ctypes.c_char_p, [I]),
+        "sep_attn_fwd_static": (I, [P, P, P, P, P, P, I, I, I, I, I, F, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -187,6 +189,25 @@ def sep_attn_fwd(index_buf, q, k, v, scale: float = 0.0, o=None, lse=None, ws=No
     _check(_lib.sep_attn_fwd(_ptr(index_buf), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
                              B, Hq, Hkv, L, d, dt, float(scale), _ptr(ws), ws.numel(),
                              _stream(stream)), "sep_attn_fwd")
+    return o, lse
+
+
+def sep_attn_fwd_static(index_buf, q, k, v, scale: float = 0.0, o=None, lse=None,
+                        stream=None):
+    """sep_attn_fwd for callers that cannot allocate device memory: the
+    library keeps the forward's scratch in a fixed 64 MiB device array, so
+    no workspace is passed.  bf16 only.  The binding allocates o and lse
+    only when they are not given; pass them to allocate nothing.
+    Returns (o, lse)."""
+    B, Hq, L, d = q.shape
+    Hkv = k.shape[1]
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, L), dtype=torch.float32, device=q.device)
+    _check(_lib.sep_attn_fwd_static(_ptr(index_buf), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                    _ptr(lse), B, Hq, Hkv, L, d, float(scale),
+                                    _stream(stream)), "sep_attn_fwd_static")
     return o, lse
 
 

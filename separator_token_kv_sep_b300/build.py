@@ -15,7 +15,8 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libsepattn.so")
 INCLUDE = os.path.join(ROOT, "include")
 
-SOURCES = ["index.cu", "attn_simt.cu", "attn_fwd_tc.cu", "attn_bwd_tc.cu", "cache.cu", "api.cu"]
+SOURCES = ["index.cu", "attn_simt.cu", "attn_fwd_tc.cu", "attn_bwd_tc.cu", "cache.cu", "api.cu",
+           "attn_fwd_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
                 "-I", INCLUDE, "-I", CSRC]

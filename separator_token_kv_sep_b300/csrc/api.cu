@@ -190,6 +190,7 @@ SEP_API const char* sep_status_string(sep_status s) {
     case SEP_ERR_TIMEOUT: return "device wait timed out";
     case SEP_ERR_DEVICE_BOUNDS: return "device index or count out of range";
     case SEP_ERR_WORKSPACE: return "buffer smaller than the size query";
+    case SEP_ERR_TOO_LARGE: return "shape exceeds the fixed scratch of sep_attn_fwd_static";
   }
   return "unknown status";
 }
