@@ -68,6 +68,19 @@ def visited_pairs_per_head(ids: np.ndarray, a: int, n: int) -> int:
     return int((kp[:, W] + (i - W + 1)[None, :]).sum())
 
 
+def gathered_band_pairs_per_head(ids: np.ndarray, a: int, n: int, bm: int):
+    """Split of the visited pairs of one head (summed over the batch) between
+    the two key sources of a 128-row query tile: keep tokens gathered from
+    before the tile's first window start, and the dense band after it."""
+    keep = np.isin(ids, synth.SEP_IDS) | (np.arange(ids.shape[1]) < a)[None, :]
+    kp = np.concatenate([np.zeros((ids.shape[0], 1), np.int64), np.cumsum(keep, axis=1)], axis=1)
+    L = ids.shape[1]
+    i = np.arange(L)
+    W0 = np.maximum(0, (i // bm) * bm - n + 1)
+    gathered = int(kp[:, W0].sum())
+    return gathered, visited_pairs_per_head(ids, a, n) - gathered
+
+
 def decode_cache_lengths(sep: np.ndarray, a: int, s: int, w: int, c: int) -> np.ndarray:
     """Entries each sequence's cache holds after each step (new token
     included), from counts alone: tokens [a, cp) have been through
@@ -168,7 +181,7 @@ def run_ours(args, rank, world, device):
 
     # ---------------------------------------------------------- train step
     cfg = synth.PYTHIA_TRAIN_N128
-    q_np, k_np, v_np, do_np, ids_np = synth.prefill_inputs(cfg, seed=cfg.seed + rank)
+    q_np, k_np, v_np, do_np, ids_np = synth.prefill_inputs(cfg, seed=shard_seed(cfg.seed, rank))
     bf = torch.bfloat16
     q = torch.from_numpy(q_np).to(device, bf)
     k = torch.from_numpy(k_np).to(device, bf)
@@ -188,20 +201,30 @@ def run_ours(args, rank, world, device):
     o = torch.empty_like(q)
     lse = torch.empty((B, Hq, L), dtype=torch.float32, device=device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+    # step boundaries, and the per-kernel marks the library records through
+    # sep_profile_events (fwd: gather | attention; bwd: gather | prep | keep
+    # dK/dV | dense dK/dV | dQ)
+    Ev = lambda: torch.cuda.Event(enable_timing=True, external=True)  # noqa: E731
+    step_ev = [Ev(), Ev()]
+    fwd_ev = [Ev() for _ in range(3)]
+    bwd_ev = [Ev() for _ in range(6)]
+    for e in step_ev + fwd_ev + bwd_ev:  # create the CUDA events outside the capture
+        e.record()
+    torch.cuda.synchronize()
 
     def train_step(mark=False):
         if mark:
-            ev[0].record()
+            step_ev[0].record()
         api.sep_build_index(ids, synth.SEP_IDS, cfg.a, cfg.n, index_buf=idx_buf)
         if mark:
-            ev[1].record()
+            api.sep_profile_events(fwd_ev)
         api.sep_attn_fwd(idx_buf, q, k, v, o=o, lse=lse, ws=ws_f)
         if mark:
-            ev[2].record()
+            api.sep_profile_events(bwd_ev)
         api.sep_attn_bwd(idx_buf, q, k, v, o, lse, dout, dq=dq, dk=dk, dv=dv, ws=ws_b)
         if mark:
-            ev[3].record()
+            api.sep_profile_events([])
+            step_ev[1].record()
 
     for _ in range(2):
         train_step()
@@ -215,8 +238,16 @@ def run_ours(args, rank, world, device):
         graph.replay()
     torch.cuda.synchronize()
 
+    kern_names = ["index", "fwd_gather", "fwd_attn", "bwd_gather", "bwd_prep", "bwd_kv_keep",
+                  "bwd_kv_dense", "bwd_dq"]
+    marks = [step_ev[0], fwd_ev[0], fwd_ev[1], fwd_ev[2], bwd_ev[0], bwd_ev[1], bwd_ev[2],
+             bwd_ev[3], bwd_ev[4], bwd_ev[5]]
+    # index: step start -> fwd gather; fwd attn end -> bwd gather is launch glue
+    spans = {"index": (0, 1), "fwd_gather": (1, 2), "fwd_attn": (2, 3), "bwd_gather": (4, 5),
+             "bwd_prep": (5, 6), "bwd_kv_keep": (6, 7), "bwd_kv_dense": (7, 8), "bwd_dq": (8, 9)}
     sampler = ClockSampler(device.index if device.index is not None else 0)
-    t_idx, t_fwd, t_bwd, t_step = [], [], [], []
+    t_step = []
+    t_kern = {n: [] for n in kern_names}
     with sampler:
         if world > 1:
             torch.distributed.barrier()
@@ -225,30 +256,45 @@ def run_ours(args, rank, world, device):
             flush.zero_()
             graph.replay()
             torch.cuda.synchronize()
-            t_idx.append(ev[0].elapsed_time(ev[1]))
-            t_fwd.append(ev[1].elapsed_time(ev[2]))
-            t_bwd.append(ev[2].elapsed_time(ev[3]))
-            t_step.append(ev[0].elapsed_time(ev[3]))
+            t_step.append(step_ev[0].elapsed_time(step_ev[1]))
+            for n in kern_names:
+                a_, b_ = spans[n]
+                t_kern[n].append(marks[a_].elapsed_time(marks[b_]))
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
         total_ms = sum(t_step)
         total_ms = max_over_ranks(total_ms, world)
-        decode = run_decode(args, rank, device, flush, peaks)
-        prefill = run_prefill(args, rank, device, flush, peaks)
+        decode = run_decode(args, rank, device, flush, peaks) if args.only == "all" else None
+        prefill = run_prefill(args, rank, device, flush, peaks) if args.only == "all" else None
     assert api.sep_get_device_status() == 0
     clocks = sampler.summary()
 
     ms_per_step = total_ms / args.steps
-    value = (fwd_flops + bwd_flops) * world * args.steps / (total_ms * 1e-3) / 1e12
-    mean = lambda xs: sum(xs) / len(xs)
-    fwd_ms, bwd_ms, idx_ms = mean(t_fwd), mean(t_bwd), mean(t_idx)
+    value = aggregate_value(fwd_flops + bwd_flops, world, args.steps, total_ms)
+    mean = lambda xs: sum(xs) / len(xs)  # noqa: E731
+    kern_ms = {n: mean(t_kern[n]) for n in kern_names}
+    fwd_ms = kern_ms["fwd_gather"] + kern_ms["fwd_attn"]
+    bwd_ms = sum(kern_ms[n] for n in ("bwd_gather", "bwd_prep", "bwd_kv_keep", "bwd_kv_dense",
+                                      "bwd_dq"))
     fwd_tf = fwd_flops / (fwd_ms * 1e-3) / 1e12
     bwd_tf = bwd_flops / (bwd_ms * 1e-3) / 1e12
+    # Algorithmic FLOPs of each tensor-core kernel over the visited pairs it
+    # owns: attention forward 4d per pair; key-major dK/dV 8d per pair
+    # (S and dP recomputed, dV, dK); query-major dQ 6d per pair (S, dP, dQ).
+    g_pairs, band_pairs = gathered_band_pairs_per_head(ids_np, cfg.a, cfg.n, 128)
+    kern_flops = {"fwd_attn": 4.0 * d * pairs * Hq, "bwd_kv_keep": 8.0 * d * g_pairs * Hq,
+                  "bwd_kv_dense": 8.0 * d * band_pairs * Hq, "bwd_dq": 6.0 * d * pairs * Hq}
+    dom = max(kern_flops, key=lambda n: kern_ms[n])
+    dom_tf = kern_flops[dom] / (kern_ms[dom] * 1e-3) / 1e12
+    kernels = {n: {"ms": round(kern_ms[n], 5)} for n in kern_names}
+    for n, fl in kern_flops.items():
+        kernels[n]["tflops"] = round(fl / (kern_ms[n] * 1e-3) / 1e12, 2)
+        kernels[n]["gflop"] = round(fl / 1e9, 3)
 
     # ------------------------------------------------------------ e2e
     e2e = run_e2e(api, cfg, q_np, k_np, v_np, do_np, ids_np, device, args, fwd_flops + bwd_flops,
-                  world)
+                  world) if args.only == "all" else None
 
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
@@ -260,24 +306,40 @@ def run_ours(args, rank, world, device):
                    "visited_pairs_per_head": pairs, "visited_over_causal":
                        round(pairs / (B * L * (L + 1) / 2), 4),
                    "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas x{world}"},
-        "phases_ms": {"index": round(idx_ms, 5), "fwd": round(fwd_ms, 5), "bwd": round(bwd_ms, 5),
+        "phases_ms": {"fwd": round(fwd_ms, 5), "bwd": round(bwd_ms, 5),
                       "fwd_tflops": round(fwd_tf, 2), "bwd_tflops": round(bwd_tf, 2)},
+        "kernels": kernels,
         "roofline": {
-            "bound": "tensor", "kernel": "sep_attn_bwd call (5 kernels; the dominant phase)",
-            "achieved": round(bwd_tf, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-            "frac": round(bwd_tf / peaks["bf16_tflops"], 4),
-            "frac_of_sustained": round(bwd_tf / peaks["bf16_tflops_sustained"], 4)
+            "bound": "tensor", "kernel": dom,
+            "achieved": round(dom_tf, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": round(dom_tf / peaks["bf16_tflops"], 4),
+            "frac_of_sustained": round(dom_tf / peaks["bf16_tflops_sustained"], 4)
             if peaks.get("bf16_tflops_sustained") else None,
-            "peak_source": peaks["source"] + " (burst bf16)", "traffic": None},
+            "peak_source": peaks["source"] + " (burst bf16; of measured)",
+            "timing": "CUDA events recorded around the kernel inside the timed graph",
+            "traffic": None},
         "e2e": e2e,
         "clocks": clocks,
         "gpu_launches": 8 * args.steps,
         "decode": decode,
         "prefill": prefill,
     }
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and args.only == "all":
         line["cpu_baseline"] = cpu_baseline_train(cfg, q_np, k_np, v_np, do_np, ids_np)
     return line
+
+
+def shard_seed(base_seed: int, rank: int) -> int:
+    """Each rank draws its own shard of the workload (independent problems:
+    the data path needs no collective)."""
+    return base_seed + rank
+
+
+def aggregate_value(work_per_rank: float, world: int, steps: int, max_ms: float,
+                    unit_scale: float = 1e12) -> float:
+    """Whole-job throughput: the work every rank did over the slowest rank's
+    time."""
+    return work_per_rank * world * steps / (max_ms * 1e-3) / unit_scale
 
 
 def max_over_ranks(x: float, world: int) -> float:
@@ -341,7 +403,7 @@ def run_decode(args, rank, device, flush, peaks):
     import torch
     from separator_token_kv_sep_b300 import api
     cfg = synth.STREAM_DECODE
-    qp, kp, vp, ids_np = synth.stream_inputs(cfg, seed=cfg.seed + rank)
+    qp, kp, vp, ids_np = synth.stream_inputs(cfg, seed=shard_seed(cfg.seed, rank))
     P = qp.shape[0]
     bf = torch.bfloat16
     dq = torch.from_numpy(qp).to(device, bf)
@@ -400,10 +462,10 @@ def run_prefill(args, rank, device, flush, peaks):
     from separator_token_kv_sep_b300 import api
     res = {}
     for cfg, reps in ((synth.LLAMA_PREFILL, 10), (synth.LONG_PREFILL, 3)):
-        rng = np.random.Generator(np.random.PCG64(cfg.seed + rank))
+        rng = np.random.Generator(np.random.PCG64(shard_seed(cfg.seed, rank)))
         ids_np = synth.token_ids(rng, (cfg.B, cfg.L), cfg.p)
         gen = torch.Generator(device=device)
-        gen.manual_seed(cfg.seed + rank)
+        gen.manual_seed(shard_seed(cfg.seed, rank))
         bf = torch.bfloat16
         q = torch.randn((cfg.B, cfg.Hq, cfg.L, cfg.d), generator=gen, device=device).to(bf)
         k = torch.randn((cfg.B, cfg.Hkv, cfg.L, cfg.d), generator=gen, device=device).to(bf)
@@ -510,6 +572,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["all", "train", "decode"], default="all",
+                    help="train: the training step alone (no e2e, decode or prefill legs); "
+                         "decode: the streaming-decode leg alone")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
     rank = int(os.environ.get("RANK", "0"))
@@ -526,7 +591,12 @@ def main(argv=None):
         import torch.distributed as dist
         torch.cuda.set_device(device)
         dist.init_process_group("nccl", device_id=device)
-    line = run_ours(args, rank, world, device)
+    if args.only == "decode":
+        torch.cuda.set_device(device)
+        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+        line = run_decode(args, rank, device, flush, load_peaks())
+    else:
+        line = run_ours(args, rank, world, device)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -213,12 +213,12 @@ sep_status sep_attn_fwd_static(const void* index_buf, const void* q, const void*
 /* Shape of a batch of S streaming caches. */
 typedef struct {
   int S;            /* sequences */
-  int Hkv;          /* kv heads, 1..8 */
+  int Hkv;          /* kv heads, 1..64 */
   int d;            /* head dim, 128 (64 also accepted) */
   int a;            /* initial (sink) block capacity */
   int s;            /* separator block capacity */
   int w;            /* local window capacity */
-  int c;            /* total capacity; requires a + s + w < c */
+  int c;            /* total capacity, <= 1024; requires a + s + w < c */
   float rope_theta; /* RoPE base; <= 0 selects 500000 */
 } sep_cache_params;
 
@@ -230,7 +230,7 @@ size_t sep_cache_bytes(const sep_cache_params* p);
  *   p          HOST params; cache_buf device buffer of `bytes` >=
  *              sep_cache_bytes(p), 256-byte aligned.
  * Errors: SEP_ERR_INVALID_ARG, SEP_ERR_CAPACITY (a + s + w >= c),
- * SEP_ERR_UNSUPPORTED (Hkv > 8, d not 64/128), SEP_ERR_WORKSPACE,
+ * SEP_ERR_UNSUPPORTED (Hkv > 64, c > 1024, d not 64/128), SEP_ERR_WORKSPACE,
  * SEP_ERR_CUDA.  Synchronous on `stream` for the table upload. */
 sep_status sep_cache_init(const sep_cache_params* p, void* cache_buf,
                           size_t bytes, void* stream);
@@ -254,7 +254,7 @@ sep_status sep_cache_init(const sep_cache_params* p, void* cache_buf,
  *   ids_new  int32 [S] token ids of the new tokens.
  *   sep_ids  HOST int32 [n_sep_ids] separator ids (<= SEP_MAX_SEP_IDS).
  *   out      [S, Hq, d] bf16 (NULL: update only).
- *   Hq       q heads, a multiple of Hkv.
+ *   Hq       q heads: Hq / Hkv must be 1, 2, 4 or 8.
  *   scale    <= 0 selects 1/sqrt(d).
  * Errors: SEP_ERR_INVALID_ARG, SEP_ERR_UNSUPPORTED, SEP_ERR_CUDA; device:
  * SEP_ERR_DEVICE_BOUNDS if the stored counters are inconsistent. */
@@ -295,6 +295,35 @@ sep_status sep_cache_import(const sep_cache_params* p, void* cache_buf,
 /* Read and clear the device status word of the current device (SEP_OK if no
  * kernel reported an error since the last call).  Synchronises the device. */
 sep_status sep_get_device_status(void);
+
+/* sep_profile_events -- timing hook for benchmarks (no counterpart in the
+ * paper).  Registers up to SEP_MAX_PROFILE_EVENTS cudaEvent_t handles for
+ * the calling host thread; while registered, sep_attn_fwd and sep_attn_bwd
+ * record them on their stream around the kernels they launch, so a caller
+ * can time each kernel with cudaEventElapsedTime (also inside a CUDA-graph
+ * capture, where the records become graph nodes).  n_events = 0 clears.
+ *   sep_attn_fwd (bf16): [0] before the keep gather, [1] before the
+ *                        attention kernel, [2] after it.
+ *   sep_attn_bwd:        [0] before the keep gather, [1] before the Delta
+ *                        prep, [2] before the keep-tile dK/dV kernel, [3]
+ *                        before the dense dK/dV kernel, [4] before the dQ
+ *                        kernel, [5] after it.
+ * Indices past n_events are skipped.  The handles stay owned by the caller
+ * and must outlive their registration.
+ * Errors: SEP_ERR_INVALID_ARG (n_events out of range, or events NULL with
+ * n_events > 0). */
+#define SEP_MAX_PROFILE_EVENTS 8
+sep_status sep_profile_events(void* const* events, int n_events);
+
+/* sep_selftest_wait_timeout -- exercises the failure path every kernel's
+ * bounded waits share (no counterpart in the paper).  Launches one thread
+ * that waits on a shared-memory mbarrier whose arrival never comes; after
+ * limit_us microseconds (1 .. 1000000) the wait gives up, the kernel writes
+ * SEP_ERR_TIMEOUT to the device status word and returns.  Nothing traps and
+ * the context stays usable: sep_get_device_status() then returns
+ * SEP_ERR_TIMEOUT (and clears it).  Asynchronous on `stream`.
+ * Errors: SEP_ERR_INVALID_ARG, SEP_ERR_CUDA. */
+sep_status sep_selftest_wait_timeout(int limit_us, void* stream);
 
 /* Static English text for a status code. */
 const char* sep_status_string(sep_status s);

@@ -31,7 +31,8 @@ EXPORTED = ["sep_index_bytes", "sep_build_index", "sep_index_views",
             "sep_attn_workspace_bytes", "sep_attn_fwd", "sep_attn_bwd",
             "sep_cache_bytes", "sep_cache_init", "sep_cache_step",
             "sep_cache_export_bytes", "sep_cache_export", "sep_cache_import",
-            "sep_get_device_status", "sep_status_string", "sep_attn_fwd_static"]
+            "sep_get_device_status", "sep_status_string", "sep_attn_fwd_static",
+            "sep_profile_events", "sep_selftest_wait_timeout"]
 
 
 class SepError(RuntimeError):
@@ -70,6 +71,8 @@ def _load() -> ctypes.CDLL:
         "sep_get_device_status": (I, []),
         "sep_status_string": (ctypes.c_char_p, [I]),
         "sep_attn_fwd_static": (I, [P, P, P, P, P, P, I, I, I, I, I, F, P]),
+        "sep_profile_events": (I, [ctypes.POINTER(ctypes.c_void_p), I]),
+        "sep_selftest_wait_timeout": (I, [I, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -291,6 +294,26 @@ def sep_cache_import(p: CacheParams, cache_buf, image: bytes, stream=None) -> No
 # ---------------------------------------------------------------------------
 # Status
 # ---------------------------------------------------------------------------
+
+def sep_profile_events(events) -> None:
+    """Register torch.cuda.Event objects (created with enable_timing=True)
+    for the calling thread; the attention calls record them around their
+    kernels.  An empty list clears the registration."""
+    handles = []
+    for ev in events:
+        if ev.cuda_event == 0:  # torch creates the CUDA event on first record
+            ev.record()
+        handles.append(ev.cuda_event)
+    arr = (ctypes.c_void_p * max(1, len(handles)))(*handles)
+    _check(_lib.sep_profile_events(arr, len(handles)), "sep_profile_events")
+
+
+def sep_selftest_wait_timeout(limit_us: int, stream=None) -> None:
+    """Launch the bounded-wait self-test: a wait that never completes gives
+    up after limit_us and records SEP_ERR_TIMEOUT in the device status."""
+    _check(_lib.sep_selftest_wait_timeout(int(limit_us), _stream(stream)),
+           "sep_selftest_wait_timeout")
+
 
 def sep_get_device_status() -> int:
     return int(_lib.sep_get_device_status())

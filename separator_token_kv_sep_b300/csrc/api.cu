@@ -25,6 +25,19 @@ int launch_attn_bwd_tc(IndexPtrs idx, const void* q, const void* k, const void* 
                        int Hq, int Hkv, int L, int d, float scale, void* ws, int* status,
                        void* stream);
 
+namespace {
+thread_local void* t_prof_events[SEP_MAX_PROFILE_EVENTS] = {nullptr};
+thread_local int t_prof_n = 0;
+}  // namespace
+
+void profile_mark(int i, void* stream) {
+  if (i < 0 || i >= t_prof_n || !t_prof_events[i]) return;
+  // External records become event nodes when the stream is being captured
+  // into a CUDA graph; outside a capture they are ordinary records.
+  cudaEventRecordWithFlags(static_cast<cudaEvent_t>(t_prof_events[i]),
+                           static_cast<cudaStream_t>(stream), cudaEventRecordExternal);
+}
+
 int* device_status_ptr() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
@@ -166,6 +179,36 @@ SEP_API sep_status sep_attn_bwd(const void* index_buf, const void* q, const void
   const IndexPtrs idx = index_ptrs(const_cast<void*>(index_buf), index_layout(B, L, SEP_BLOCK_M));
   return from_cuda(launch_attn_bwd_tc(idx, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, L, d,
                                       scale, ws, st, stream));
+}
+
+SEP_API sep_status sep_profile_events(void* const* events, int n_events) {
+  if (n_events < 0 || n_events > SEP_MAX_PROFILE_EVENTS || (n_events > 0 && !events))
+    return SEP_ERR_INVALID_ARG;
+  for (int i = 0; i < SEP_MAX_PROFILE_EVENTS; ++i)
+    t_prof_events[i] = i < n_events ? events[i] : nullptr;
+  t_prof_n = n_events;
+  return SEP_OK;
+}
+
+namespace sep {
+namespace {
+// One thread waits on an mbarrier that expects an arrival nobody makes.
+__global__ void wait_selftest_kernel(uint64_t limit_ns, int* status) {
+  __shared__ __align__(8) uint64_t bar;
+  mbar_init(&bar, 1);
+  fence_mbar_init();
+  mbar_wait(&bar, 0, status, limit_ns);
+}
+}  // namespace
+}  // namespace sep
+
+SEP_API sep_status sep_selftest_wait_timeout(int limit_us, void* stream) {
+  if (limit_us < 1 || limit_us > 1000000) return SEP_ERR_INVALID_ARG;
+  int* st = device_status_ptr();
+  if (!st) return SEP_ERR_CUDA;
+  wait_selftest_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<uint64_t>(limit_us) * 1000ull, st);
+  return from_cuda(static_cast<int>(cudaGetLastError()));
 }
 
 SEP_API sep_status sep_get_device_status(void) {

@@ -40,6 +40,7 @@ namespace {
 constexpr int kChunk = 128 * 128;  // bytes of a [128 rows x 64 cols] bf16 block
 constexpr int kThreads = 192;      // warp 0 TMA, warp 1 MMA, warps 2-5 elementwise
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kKeepChunk = 4;      // query tiles per CTA of the keep-tile dK/dV kernel
 
 __device__ __forceinline__ uint32_t range_bits(int lo, int hi, int w) {
   // bits c of word w (columns 32w .. 32w+31) with lo <= c < hi
@@ -61,42 +62,76 @@ __device__ __forceinline__ void ew_sync() { asm volatile("bar.sync 1, 128;" ::: 
 
 // ---------------------------------------------------------------------------
 // Prep: Delta = rowsum(dO o O) in fp32, and zeroed keep-token accumulators.
+// The first kPrepDeltaBlocks(..) CTAs compute Delta: U = D/8 lanes share a
+// row (16 bytes each, so a warp reads 32/U whole rows per instruction) and
+// each warp covers kPrepRows rows.  The remaining CTAs zero, per (batch, kv
+// head), the contiguous accumulator rows [0, ceil128(keep_count)).
 // ---------------------------------------------------------------------------
+constexpr int kPrepThreads = 256;
+constexpr int kPrepRows = 16;  // rows per warp in the Delta part
+
 template <int D>
-__global__ void __launch_bounds__(256)
+__host__ __device__ constexpr int prep_rows_per_block() {
+  return (kPrepThreads / 32) * kPrepRows;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kPrepThreads)
     bwd_prep_kernel(IndexPtrs idx, const uint4* __restrict__ o, const uint4* __restrict__ dout,
                     float* __restrict__ delta, float4* __restrict__ dk_keep,
-                    float4* __restrict__ dv_keep, int Hq, int Hkv, int L) {
-  constexpr int U = D / 8;
-  const int h = blockIdx.y, b = blockIdx.z;
-  const int row = blockIdx.x * 256 + threadIdx.x;
-  if (row < L) {
-    const size_t base = (((size_t)b * Hq + h) * L + row) * U;
-    float acc = 0.f;
-#pragma unroll 4
-    for (int u = 0; u < U; ++u) {
-      const uint4 x = o[base + u], y = dout[base + u];
-      const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+                    float4* __restrict__ dv_keep, int B, int Hq, int Hkv, int L,
+                    int delta_blocks) {
+  constexpr int U = D / 8;         // 16-byte units per row
+  constexpr int RPI = 32 / U;      // rows per warp instruction
+  constexpr int IT = kPrepRows / RPI;
+  const IndexHeader hdr = *idx.header;
+  if (hdr.magic != kIndexMagic || hdr.B != B || hdr.L != L) return;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (static_cast<int>(blockIdx.x) < delta_blocks) {
+    const size_t R = (size_t)B * Hq * L;
+    const size_t row0 = ((size_t)blockIdx.x * (kPrepThreads / 32) + warp) * kPrepRows;
+    const int sub = lane / U, u = lane % U;
+    uint4 xo[IT], xd[IT];
+#pragma unroll
+    for (int it = 0; it < IT; ++it) {
+      const size_t row = row0 + it * RPI + sub;
+      xo[it] = row < R ? o[row * U + u] : make_uint4(0, 0, 0, 0);
+      xd[it] = row < R ? dout[row * U + u] : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int it = 0; it < IT; ++it) {
+      const uint32_t xs[4] = {xo[it].x, xo[it].y, xo[it].z, xo[it].w};
+      const uint32_t ys[4] = {xd[it].x, xd[it].y, xd[it].z, xd[it].w};
+      float acc = 0.f;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         acc = fmaf(__uint_as_float(xs[e] << 16), __uint_as_float(ys[e] << 16), acc);
         acc = fmaf(__uint_as_float(xs[e] & 0xffff0000u), __uint_as_float(ys[e] & 0xffff0000u),
                    acc);
       }
+#pragma unroll
+      for (int off = U / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      const size_t row = row0 + it * RPI + sub;
+      if (u == 0 && row < R) delta[row] = acc;
     }
-    delta[((size_t)b * Hq + h) * L + row] = acc;
+    return;
   }
-  // the CTAs of q head h < Hkv also zero the keep accumulators of kv head h
-  if (h < Hkv) {
-    const int count = idx.keep_count[b];
-    const int end = min(L, (count + 127) / 128 * 128);
-    if (row < end) {
-      const size_t kb = (((size_t)b * Hkv + h) * L + row) * (D / 4);
-      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int u = 0; u < D / 4; ++u) {
-        dk_keep[kb + u] = z;
-        dv_keep[kb + u] = z;
-      }
+  // zero the keep accumulators: per_plane consecutive blocks cover one plane
+  const int zb = static_cast<int>(blockIdx.x) - delta_blocks;
+  const int per_plane = (L * (D / 4) + kPrepThreads * 4 - 1) / (kPrepThreads * 4);
+  const int plane = zb / per_plane, part = zb % per_plane;
+  if (plane >= B * Hkv) return;
+  const int b = plane / Hkv;
+  const int count = min(max(idx.keep_count[b], 0), L);
+  const int end = min(L, (count + 127) / 128 * 128) * (D / 4);  // float4s in use
+  const size_t base = (size_t)plane * L * (D / 4);
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int e = (part * 4 + r) * kPrepThreads + threadIdx.x;
+    if (e < end) {
+      dk_keep[base + e] = z;
+      dv_keep[base + e] = z;
     }
   }
 }
@@ -109,7 +144,12 @@ __global__ void __launch_bounds__(256)
   constexpr int U = D / 8;
   constexpr int ROWS = 64;
   const int g = blockIdx.y, b = blockIdx.z;
+  // the header sits at offset 0 of any index buffer: check it before using
+  // the fields whose offsets depend on B and L
+  const IndexHeader hdr = *idx.header;
+  if (hdr.magic != kIndexMagic || hdr.B != static_cast<int>(gridDim.z) || hdr.L != L) return;
   const int count = idx.keep_count[b];
+  if (count < 0 || count > L) return;
   const int end = min(L, (count + 127) / 128 * 128);
   const int r0 = blockIdx.x * ROWS;
   if (r0 >= end) return;
@@ -170,7 +210,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = (L + 127) >> 7;
   const int G = Hq / Hkv;
-  const int tile = T - 1 - static_cast<int>(blockIdx.x);  // key tile (or keep tile)
+  // DENSE: one key tile per CTA (longest first).  KEEP: one keep tile and one
+  // chunk of kKeepChunk query tiles per CTA, so a keep tile's many query
+  // tiles spread over several CTAs (their partial sums meet in the fp32 keep
+  // accumulators).
+  const int n_qc = (T + kKeepChunk - 1) / kKeepChunk;
+  const int tile = KEEP ? static_cast<int>(blockIdx.x) / n_qc
+                        : T - 1 - static_cast<int>(blockIdx.x);
+  const int qc = KEEP ? static_cast<int>(blockIdx.x) % n_qc : 0;
   const int b = blockIdx.z;
   // KEEP: blockIdx.y is the q head; DENSE: the kv head
   const int g = KEEP ? static_cast<int>(blockIdx.y) / G : static_cast<int>(blockIdx.y);
@@ -198,8 +245,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int mid = (lo_t + hi_t) >> 1;
       if (blocks[4 * mid] > j0) hi_t = mid; else lo_t = mid + 1;
     }
-    t_begin = lo_t;
-    n_t = T - lo_t;
+    t_begin = max(lo_t, qc * kKeepChunk);
+    n_t = min(T, (qc + 1) * kKeepChunk) - t_begin;
     if (n_t <= 0) return;
   } else {
     // query tiles t >= tile whose dense band starts before this key tile ends
@@ -806,12 +853,21 @@ int launch_bwd_impl(IndexPtrs idx, const void* q, const void* k, const void* v, 
                     cudaStream_t s) {
   const BwdWs w = bwd_ws(ws, B, Hq, Hkv, L, D);
   const int T = (L + 127) / 128;
+  profile_mark(0, s);
   bwd_gather_kernel<D><<<dim3((L + 63) / 64, Hkv, B), 256, 0, s>>>(
       idx, static_cast<const uint4*>(k), static_cast<const uint4*>(v),
       reinterpret_cast<uint4*>(w.kk), reinterpret_cast<uint4*>(w.vk), Hkv, L);
-  bwd_prep_kernel<D><<<dim3((L + 255) / 256, Hq, B), 256, 0, s>>>(
-      idx, static_cast<const uint4*>(o), static_cast<const uint4*>(dout), w.delta,
-      reinterpret_cast<float4*>(w.dk_keep), reinterpret_cast<float4*>(w.dv_keep), Hq, Hkv, L);
+  profile_mark(1, s);
+  {
+    const size_t rows = (size_t)B * Hq * L;
+    const int delta_blocks =
+        static_cast<int>((rows + prep_rows_per_block<D>() - 1) / prep_rows_per_block<D>());
+    const int per_plane = (L * (D / 4) + kPrepThreads * 4 - 1) / (kPrepThreads * 4);
+    bwd_prep_kernel<D><<<delta_blocks + B * Hkv * per_plane, kPrepThreads, 0, s>>>(
+        idx, static_cast<const uint4*>(o), static_cast<const uint4*>(dout), w.delta,
+        reinterpret_cast<float4*>(w.dk_keep), reinterpret_cast<float4*>(w.dv_keep), B, Hq, Hkv,
+        L, delta_blocks);
+  }
   CUtensorMap mq, mdo, mk, mv, mkk, mvk;
   if (!make_bf16_map(&mq, q, (uint64_t)B * Hq, L, D, 128) ||
       !make_bf16_map(&mdo, dout, (uint64_t)B * Hq, L, D, 128) ||
@@ -833,16 +889,21 @@ int launch_bwd_impl(IndexPtrs idx, const void* q, const void* k, const void* v, 
     return static_cast<int>(e);
   __nv_bfloat16* dkb = static_cast<__nv_bfloat16*>(dk);
   __nv_bfloat16* dvb = static_cast<__nv_bfloat16*>(dv);
-  keep_k<<<dim3(T, Hq, B), kThreads, KC::SMEM, s>>>(mkk, mvk, mq, mdo, idx, lse, w.delta,
+  profile_mark(2, s);
+  keep_k<<<dim3(T * ((T + kKeepChunk - 1) / kKeepChunk), Hq, B), kThreads, KC::SMEM, s>>>(mkk, mvk, mq, mdo, idx, lse, w.delta,
                                                       w.dk_keep, w.dv_keep, dkb, dvb, B, Hq, Hkv,
                                                       L, scale, scale_log2, status);
+  profile_mark(3, s);
   dense_k<<<dim3(T, Hkv, B), kThreads, KC::SMEM, s>>>(mk, mv, mq, mdo, idx, lse, w.delta,
                                                         w.dk_keep, w.dv_keep, dkb, dvb, B, Hq,
                                                         Hkv, L, scale, scale_log2, status);
+  profile_mark(4, s);
   dq_k<<<dim3(T, Hq, B), kThreads, QC::SMEM, s>>>(mq, mdo, mk, mv, mkk, mvk, idx, lse, w.delta,
                                                     static_cast<__nv_bfloat16*>(dq), B, Hq, Hkv,
                                                     L, scale, scale_log2, status);
-  return static_cast<int>(cudaGetLastError());
+  const cudaError_t err = cudaGetLastError();
+  profile_mark(5, s);
+  return static_cast<int>(err);
 }
 
 }  // namespace

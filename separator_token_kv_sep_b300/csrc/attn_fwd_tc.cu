@@ -58,7 +58,12 @@ __global__ void __launch_bounds__(256)
   constexpr int U = D / 8;  // 16-byte units per row
   constexpr int ROWS = 64;
   const int g = blockIdx.y, b = blockIdx.z;
+  // the header sits at offset 0 of any index buffer: check it before using
+  // the fields whose offsets depend on B and L
+  const IndexHeader hdr = *idx.header;
+  if (hdr.magic != kIndexMagic || hdr.B != static_cast<int>(gridDim.z) || hdr.L != L) return;
   const int count = idx.keep_count[b];
+  if (count < 0 || count > L) return;
   const int end = min(L, (count + 127) / 128 * 128);
   const int r0 = blockIdx.x * ROWS;
   if (r0 >= end) return;
@@ -383,6 +388,7 @@ int launch_fwd_impl(IndexPtrs idx, const void* q, const void* k, const void* v, 
   uint8_t* kk = static_cast<uint8_t*>(ws);
   uint8_t* vk = kk + align_up((size_t)B * Hkv * plane_elems * 2, 256);
   dim3 ggrid((L + 63) / 64, Hkv, B);
+  profile_mark(0, s);
   gather_keep_kernel<D><<<ggrid, 256, 0, s>>>(idx, static_cast<const uint4*>(k),
                                                static_cast<const uint4*>(v),
                                                reinterpret_cast<uint4*>(kk),
@@ -399,10 +405,13 @@ int launch_fwd_impl(IndexPtrs idx, const void* q, const void* k, const void* v, 
   if (e != cudaSuccess) return static_cast<int>(e);
   const float scale_log2 = scale * 1.4426950408889634f;
   dim3 grid((L + 127) / 128, Hq, B);
+  profile_mark(1, s);
   kern<<<grid, kThreads, C::SMEM, s>>>(mq, mk, mv, mkk, mvk, idx,
                                        static_cast<__nv_bfloat16*>(o), lse, B, Hq, Hkv, L,
                                        scale_log2, status);
-  return static_cast<int>(cudaGetLastError());
+  const cudaError_t err = cudaGetLastError();
+  profile_mark(2, s);
+  return static_cast<int>(err);
 }
 
 }  // namespace

@@ -17,18 +17,23 @@
 //
 // Storage: keys are kept un-rotated in bf16, so a position shift never
 // rewrites them and the cache contents stay bit-exact; RoPE is applied on
-// load from a cos/sin table of positions 0..c-1.  Each sequence owns
-// a + s + (c - a) slots: the initial block, a ring of s separator slots and a
-// ring of c - a slots holding the past and local windows (which are one
-// contiguous stretch of text).  Logical entry k maps to its slot through the
-// ring heads, and attention always reduces in logical order, so the outputs
-// do not depend on where the rings happen to start.
+// load.  Each sequence owns a + s + (c - a) slots per kv head: the initial
+// block, a ring of s separator slots and a ring of c - a slots holding the
+// past and local windows (one contiguous stretch of text).  Logical entry k
+// maps to its slot through the ring heads, and attention reduces in logical
+// order, so the outputs do not depend on where the rings happen to start.
 //
-// One thread-block cluster per sequence, one CTA per kv head: every CTA reads
-// the shared counters and separator flags, arrives on the cluster barrier,
-// moves and appends its own head's K/V rows, attends for the q heads of its
-// group, and CTA 0 alone writes the shared counters and flags after the
-// barrier, so no CTA can see half-updated metadata.
+// One step is one launch: a cluster of `split` CTAs per (sequence, kv head).
+// Every CTA reads the (sequence, head)'s counters and derives the layout the
+// cache will have after this step's update; it then attends over its share
+// of the entries in that layout, reading each entry from where it sits
+// *before* the update (a separator that moves this step is read from its
+// window slot, the new token from the caller's k_new / v_new).  The rows
+// arrive by TMA bulk copies into shared memory.  The partial softmax states
+// merge over distributed shared memory, and only after the whole cluster has
+// finished reading does CTA 0 write the update (moves, new row, flags,
+// counters).  Counters and flags are kept per (sequence, kv head), so no
+// cluster ever waits for another.
 #include <math.h>
 #include <string.h>
 
@@ -44,16 +49,21 @@ namespace sep {
 namespace {
 
 constexpr int kCacheMagic = 0x43504553;  // 'SEPC'
-constexpr int kThreads = 256;
+constexpr int kThreads = 128;            // 4 warps per CTA
 constexpr int kWarps = kThreads / 32;
-constexpr int kMaxPast = 1024;  // c - a slots of the window ring are scanned in smem
+constexpr int kMaxC = 1024;              // survivor list is kept in shared memory
+constexpr int kMaxHkv = 64;
+constexpr int kMaxSplit = 8;             // portable cluster size
+constexpr int kTargetCtas = 2048;        // CTAs per step the split aims at
 
 struct CacheLayout {
-  int S, Hkv, d, a, s, w, c, NSL;
+  int S, Hkv, d, a, s, w, c, NSL, rope_rows;
   size_t meta, rope, pos, issep, k, v, total;
 };
 
-// Counters of one sequence (int32 x 8 in device memory).
+// Counters of one (sequence, kv head) (int32 x 8 in device memory).  Every
+// kv head of a sequence holds the same values; each cluster updates its own
+// copy.
 struct Meta {
   int n_init, n_sep, sep_head, n_pw, pw_head, t, pad0, pad1;
 };
@@ -67,15 +77,16 @@ CacheLayout cache_layout(const sep_cache_params* p) {
   CacheLayout l;
   l.S = p->S; l.Hkv = p->Hkv; l.d = p->d; l.a = p->a; l.s = p->s; l.w = p->w; l.c = p->c;
   l.NSL = p->a + p->s + (p->c - p->a);
+  l.rope_rows = p->c > 64 ? p->c : 64;  // rows 16 and 32 hold the recurrence steps
   size_t off = 0;
   l.meta = off;
-  off = align_up(off + sizeof(Meta) * (size_t)l.S, 256);
+  off = align_up(off + sizeof(Meta) * (size_t)l.S * l.Hkv, 256);
   l.rope = off;
-  off = align_up(off + sizeof(float2) * (size_t)l.c * (l.d / 2), 256);
+  off = align_up(off + sizeof(float2) * (size_t)l.rope_rows * (l.d / 2), 256);
   l.pos = off;
   off = align_up(off + sizeof(int32_t) * (size_t)l.S * l.NSL, 256);
   l.issep = off;
-  off = align_up(off + (size_t)l.S * l.NSL, 256);
+  off = align_up(off + (size_t)l.S * l.Hkv * l.NSL, 256);
   l.k = off;
   off = align_up(off + 2 * (size_t)l.S * l.Hkv * l.NSL * l.d, 256);
   l.v = off;
@@ -106,29 +117,39 @@ CachePtrs cache_ptrs(void* buf, const CacheLayout& l) {
 }
 
 struct StepArgs {
-  int S, Hkv, Hq, a, s, w, c, NSL;
+  int S, Hkv, Hq, a, s, w, c, NSL, split, emax;
   float scale_log2;
   SepIdList sids;
 };
 
-__device__ __forceinline__ int slot_of(int k, const Meta& m, int a, int s, int ring) {
-  if (k < m.n_init) return k;
-  k -= m.n_init;
-  if (k < m.n_sep) return a + (m.sep_head + k) % s;
-  k -= m.n_sep;
-  return a + s + (m.pw_head + k) % ring;
-}
-
+// ---------------------------------------------------------------------------
+// Device helpers
+// ---------------------------------------------------------------------------
 __device__ __forceinline__ void cluster_arrive() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-__device__ __forceinline__ uint32_t cluster_rank() {
+__device__ __forceinline__ uint32_t dsmem_addr(const void* p, uint32_t rank) {
   uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
   return r;
+}
+__device__ __forceinline__ float dsmem_ld(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+// Global -> shared bulk copy (TMA, untiled); completion as transaction
+// bytes on `bar`.  Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
 }
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float* f) {
@@ -140,59 +161,116 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float* f) {
   }
 }
 
-// Dynamic shared memory of the step kernel.
-template <int D, int G>
-struct StepSmem {
-  static size_t bytes(int c) {
-    return sizeof(float) * ((size_t)G * D + (size_t)G * (c + 32) + (size_t)kWarps * G * D);
-  }
+// The layout after this step's update, expressed through where each entry
+// sits before it:
+//   [0, I0)                 initial slots 0 .. I0-1
+//   [I0, I0+SK)             kept separator-ring entries from ring offset sk0
+//   [.., +SV)               separators moving out of the past window now
+//                           (window-ring slots in surv_src)
+//   [.., +W0)               window-ring entries from ring position pw0
+//   N-1                     the new token (caller's k_new / v_new)
+struct StepPlan {
+  int I0, SK, SV, W0, N;
+  int sk0, pw0;
 };
 
+// Slot of logical entry k < N-1, or -1 for the new token.
+__device__ __forceinline__ int plan_slot(int k, const StepPlan& pl, const int* surv_src, int a,
+                                         int s, int ring) {
+  if (k < pl.I0) return k;
+  k -= pl.I0;
+  if (k < pl.SK) return a + (pl.sk0 + k) % s;
+  k -= pl.SK;
+  if (k < pl.SV) return surv_src[k];
+  k -= pl.SV;
+  if (k < pl.W0) return a + s + (pl.pw0 + k) % ring;
+  return -1;
+}
+
+// Dynamic shared memory of the step kernel (byte offsets; every region is
+// 16-byte aligned).
+struct StepSmem {
+  int k, v, q, p, acc, red, src, total;
+};
+
+__host__ __device__ inline StepSmem step_smem(int D, int G, int emax) {
+  auto al = [](int x) { return (x + 15) / 16 * 16; };
+  StepSmem m;
+  int off = 0;
+  m.k = off;
+  const int kbytes = emax * D * 2, redbytes = kWarps * G * D * 4;
+  off += al(kbytes > redbytes ? kbytes : redbytes);  // the PV reduction reuses the K rows
+  m.v = off;
+  off += al(emax * D * 2);
+  m.q = off;
+  off += al(G * D * 4);
+  m.p = off;
+  off += al(G * emax * 4);
+  m.acc = off;
+  off += al(G * D * 4 + 2 * G * 4);  // acc[G][D], then m[G], l[G]
+  m.red = m.k;
+  m.src = off;
+  off += al(emax * 4);
+  m.total = off;
+  return m;
+}
+
+// ---------------------------------------------------------------------------
+// The step kernel
+// ---------------------------------------------------------------------------
 template <int D, int G>
 __global__ void __launch_bounds__(kThreads)
     cache_step_kernel(CachePtrs cp, StepArgs args, const uint16_t* __restrict__ q,
                       const uint16_t* __restrict__ k_new, const uint16_t* __restrict__ v_new,
                       const int32_t* __restrict__ ids_new, uint16_t* __restrict__ out,
                       int* status) {
-  constexpr int LPE = D / 8;     // lanes per cache entry (16 bytes each)
-  constexpr int EPW = 32 / LPE;  // entries per warp pass
   constexpr int HALF = D / 2;
-  extern __shared__ float dsm[];
-  __shared__ int sep_src[kMaxPast];  // window-ring slots of surviving separators
-  __shared__ int sep_dst[kMaxPast];  // their separator-ring slots
-  __shared__ int src_pos[kMaxPast];
+  constexpr int CPR = D / 8;       // 16-byte chunks per row
+  constexpr int LPE = CPR / 2;     // lanes per entry in the score phase (low chunk + partner)
+  constexpr int EPW = 32 / LPE;    // entries per warp per score iteration
+  constexpr int STRIDE = kWarps * EPW;  // entries per CTA per score iteration (16 or 32)
+  constexpr int NSLICE = kThreads / CPR;  // entry slices in the PV phase
+  extern __shared__ __align__(128) uint8_t dsm[];
+  __shared__ int surv_src[kMaxC];
+  __shared__ int surv_pos[kMaxC];
   __shared__ int warp_cnt[kWarps];
-  __shared__ int bad;
+  __shared__ __align__(8) uint64_t bar_k, bar_v;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int g = blockIdx.x, sq = blockIdx.y;
+  const int rank = blockIdx.x, g = blockIdx.y, sq = blockIdx.z;
+  const int split = args.split;
   const int a = args.a, s = args.s, w = args.w, c = args.c, NSL = args.NSL;
   const int ring = c - a;
-  const bool rank0 = cluster_rank() == 0;
-  float* qs = dsm;                        // [G][D]
-  float* scores = qs + G * D;             // [G][c + 32]
-  float* partial = scores + G * (c + 32); // [kWarps][G][D]
-  const int SP = c + 32;
+  const bool attend = q != nullptr && out != nullptr;
+  const StepSmem L = step_smem(D, G, args.emax);
+  uint16_t* sK = reinterpret_cast<uint16_t*>(dsm + L.k);
+  uint16_t* sV = reinterpret_cast<uint16_t*>(dsm + L.v);
+  float* sQ = reinterpret_cast<float*>(dsm + L.q);
+  float* sP = reinterpret_cast<float*>(dsm + L.p);
+  float* sAcc = reinterpret_cast<float*>(dsm + L.acc);
+  float* sM = sAcc + G * D;
+  float* sL = sM + G;
+  float* sRed = reinterpret_cast<float*>(dsm + L.red);
+  int* sSrc = reinterpret_cast<int*>(dsm + L.src);
 
-  const Meta m = cp.meta[sq];
-  const int32_t* posr = cp.pos + (size_t)sq * NSL;
-  const uint8_t* sepr = cp.issep + (size_t)sq * NSL;
-  if (tid == 0)
-    bad = (m.n_init < 0 || m.n_init > a || m.n_sep < 0 || m.n_sep > s || m.n_pw < 0 ||
-           m.n_pw > ring || m.sep_head < 0 || (s > 0 && m.sep_head >= s) || m.pw_head < 0 ||
-           m.pw_head >= ring || m.n_init + m.n_sep + m.n_pw > c ||
-           (m.n_init < a && (m.n_sep | m.n_pw) != 0));
-  __syncthreads();
-  const bool ok = !bad;
+  const size_t mh = (size_t)sq * args.Hkv + g;  // (sequence, kv head)
+  const Meta m = cp.meta[mh];
+  const uint8_t* sepr = cp.issep + mh * NSL;
+  const bool ok = !(m.n_init < 0 || m.n_init > a || m.n_sep < 0 || m.n_sep > s || m.n_pw < 0 ||
+                    m.n_pw > ring || m.sep_head < 0 || (s > 0 && m.sep_head >= s) ||
+                    m.pw_head < 0 || m.pw_head >= ring || m.n_init + m.n_sep + m.n_pw > c ||
+                    (m.n_init < a && (m.n_sep | m.n_pw) != 0));
 
-  // ---- new counters (identical in every CTA of the cluster)
+  // ---- plan this step's update (identical in every CTA of the cluster)
   Meta nm = m;
+  StepPlan pl;
+  pl.I0 = m.n_init; pl.SK = m.n_sep; pl.SV = 0; pl.W0 = m.n_pw;
+  pl.sk0 = m.sep_head; pl.pw0 = m.pw_head;
   const bool compress = ok && (m.n_init + m.n_sep + m.n_pw == c);
-  int n_surv = 0;
   if (compress) {
     const int n_win = min(w, m.n_pw);
     const int n_past = m.n_pw - n_win;
-    // pass 1: number of separators in the past window
+    // pass 1: separators in the past window
     int ms = 0;
     for (int k0 = 0; k0 < n_past; k0 += kThreads) {
       const int k = k0 + tid;
@@ -220,19 +298,24 @@ __global__ void __launch_bounds__(kThreads)
       }
       const int r = before + __popc(bal & ((1u << lane) - 1u));
       if (is_s && r >= first) {
-        sep_src[r - first] = slot;
-        sep_dst[r - first] = a + (m.sep_head + m.n_sep + r) % s;
-        src_pos[r - first] = posr[slot];
+        surv_src[r - first] = slot;
+        // text positions are kept once per sequence, by kv head 0's cluster
+        surv_pos[r - first] = g == 0 ? cp.pos[(size_t)sq * NSL + slot] : 0;
       }
       base += tot;
       __syncthreads();
     }
-    n_surv = ms - first;
+    const int n_surv = ms - first;
     const int drop = max(0, m.n_sep + ms - s);
     nm.sep_head = s > 0 ? (m.sep_head + drop) % s : 0;
     nm.n_sep = m.n_sep + ms - drop;
     nm.pw_head = (m.pw_head + n_past) % ring;
     nm.n_pw = n_win;
+    pl.SV = n_surv;
+    pl.SK = nm.n_sep - n_surv;
+    pl.sk0 = nm.sep_head;  // the kept old entries start where the ring now starts
+    pl.W0 = n_win;
+    pl.pw0 = nm.pw_head;
   }
   int new_slot = 0;
   if (ok) {
@@ -245,186 +328,284 @@ __global__ void __launch_bounds__(kThreads)
     }
     nm.t = m.t + 1;
   }
-  const int32_t new_id = ids_new[sq];
-  bool new_is_sep = false;
-  for (int x = 0; x < args.sids.n; ++x) new_is_sep |= (new_id == args.sids.ids[x]);
+  pl.N = pl.I0 + pl.SK + pl.SV + pl.W0 + 1;
 
-  cluster_arrive();  // every CTA has read the shared counters and flags
-
-  // ---- move this head's surviving separator rows, then append the new token
-  const size_t head_off = ((size_t)sq * args.Hkv + g) * (size_t)NSL * D;
-  uint16_t* kh = cp.k + head_off;
-  uint16_t* vh = cp.v + head_off;
-  for (int e = tid; e < n_surv * (D / 8); e += kThreads) {
-    const int r = e / (D / 8), u = e % (D / 8);
-    const size_t so = (size_t)sep_src[r] * D + 8 * u, dst = (size_t)sep_dst[r] * D + 8 * u;
-    *reinterpret_cast<uint4*>(kh + dst) = *reinterpret_cast<const uint4*>(kh + so);
-    *reinterpret_cast<uint4*>(vh + dst) = *reinterpret_cast<const uint4*>(vh + so);
-  }
-  __syncthreads();  // the new token may land on a slot a survivor was copied from
-  if (ok) {
-    const size_t src = ((size_t)sq * args.Hkv + g) * D;
-    for (int u = tid; u < D / 8; u += kThreads) {
-      *reinterpret_cast<uint4*>(kh + (size_t)new_slot * D + 8 * u) =
-          *reinterpret_cast<const uint4*>(k_new + src + 8 * u);
-      *reinterpret_cast<uint4*>(vh + (size_t)new_slot * D + 8 * u) =
-          *reinterpret_cast<const uint4*>(v_new + src + 8 * u);
-    }
-  }
-  __syncthreads();
-
-  // ---- decode attention for the G q heads of kv head g
-  if (ok && q != nullptr && out != nullptr) {
-    const int N = nm.n_init + nm.n_sep + nm.n_pw;
-    const int qpos = N - 1;
-    for (int e = tid; e < G * D; e += kThreads) {
-      const int hh = e / D, x = e % D;
-      const uint16_t* qr = q + (((size_t)sq * args.Hq) + g * G + hh) * D;
-      const int i = x % HALF;
-      const float2 cs = cp.rope[(size_t)qpos * HALF + i];
-      const float x1 = __uint_as_float((uint32_t)qr[i] << 16);
-      const float x2 = __uint_as_float((uint32_t)qr[i + HALF] << 16);
-      qs[hh * D + x] = x < HALF ? (x1 * cs.x - x2 * cs.y) : (x2 * cs.x + x1 * cs.y);
+  // ---- attention over this CTA's share [k0, k1) of the new layout
+  bool att_ok = ok && attend;
+  if (attend) {
+    const int N = pl.N;
+    const int k0 = (int)(((long long)N * rank) / split);
+    const int k1 = (int)(((long long)N * (rank + 1)) / split);
+    const int ne = ok ? k1 - k0 : 0;
+    const size_t head_off = mh * (size_t)NSL * D;
+    const uint16_t* kh = cp.k + head_off;
+    const uint16_t* vh = cp.v + head_off;
+    const size_t new_off = mh * D;  // [S][Hkv][D] inputs
+    for (int e = tid; e < ne; e += kThreads)
+      sSrc[e] = plan_slot(k0 + e, pl, surv_src, a, s, ring);
+    if (tid == 0) {
+      mbar_init(&bar_k, 1);
+      mbar_init(&bar_v, 1);
+      fence_mbar_init();
     }
     __syncthreads();
-    const int sub = lane / LPE, l8 = lane % LPE;  // entry within the pass, lane within entry
-    const int e0 = 8 * l8;                        // first of this lane's 8 columns
-    const bool lo_half = e0 < HALF;
-    // scores, rotating each key by its rank in the cache
-    for (int k0 = warp * EPW; k0 < N; k0 += kWarps * EPW) {
-      const int k = k0 + sub;
-      const bool valid = k < N;
-      const int slot = valid ? slot_of(k, nm, a, s, ring) : 0;
-      float x[8];
-      bf16x8_to_f32(*reinterpret_cast<const uint4*>(kh + (size_t)slot * D + e0), x);
-      float y[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) y[j] = __shfl_xor_sync(0xffffffffu, x[j], LPE / 2);
-      const float4* cs4 =
-          reinterpret_cast<const float4*>(cp.rope + (size_t)(valid ? k : 0) * HALF + (e0 % HALF));
-      float rk[8];
-#pragma unroll
-      for (int j2 = 0; j2 < 4; ++j2) {
-        const float4 t = cs4[j2];  // (cos, sin) of columns 2*j2 and 2*j2+1
-        const int j = 2 * j2;
-        rk[j] = lo_half ? (x[j] * t.x - y[j] * t.y) : (x[j] * t.x + y[j] * t.y);
-        rk[j + 1] = lo_half ? (x[j + 1] * t.z - y[j + 1] * t.w) : (x[j + 1] * t.z + y[j + 1] * t.w);
-      }
-#pragma unroll
-      for (int hh = 0; hh < G; ++hh) {
-        float acc = 0.f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc = fmaf(rk[j], qs[hh * D + e0 + j], acc);
-#pragma unroll
-        for (int off = LPE / 2; off > 0; off >>= 1)
-          acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (valid && l8 == 0) scores[hh * SP + k] = acc * args.scale_log2;
+    if (tid == 0) {
+      mbar_arrive_expect_tx(&bar_k, (uint32_t)(ne * D * 2));
+      mbar_arrive_expect_tx(&bar_v, (uint32_t)(ne * D * 2));
+    }
+    __syncthreads();
+    for (int e = tid; e < ne; e += kThreads) {
+      const int slot = sSrc[e];
+      const uint16_t* srck = slot >= 0 ? kh + (size_t)slot * D : k_new + new_off;
+      const uint16_t* srcv = slot >= 0 ? vh + (size_t)slot * D : v_new + new_off;
+      bulk_g2s(sK + (size_t)e * D, srck, D * 2, &bar_k);
+      bulk_g2s(sV + (size_t)e * D, srcv, D * 2, &bar_v);
+    }
+    // rotated queries of the G heads at position N-1
+    if (ok) {
+      const float2* cs_row = cp.rope + (size_t)(N - 1) * HALF;
+      for (int e = tid; e < G * HALF; e += kThreads) {
+        const int hh = e / HALF, i = e % HALF;
+        const uint16_t* qr = q + (((size_t)sq * args.Hq) + g * G + hh) * D;
+        const float2 cs = cs_row[i];
+        const float x1 = __uint_as_float((uint32_t)qr[i] << 16);
+        const float x2 = __uint_as_float((uint32_t)qr[i + HALF] << 16);
+        sQ[hh * D + i] = x1 * cs.x - x2 * cs.y;
+        sQ[hh * D + i + HALF] = x2 * cs.x + x1 * cs.y;
       }
     }
     __syncthreads();
-    // softmax, one warp per head
-    for (int hh = warp; hh < G; hh += kWarps) {
-      float* sc = scores + hh * SP;
-      float mx = -INFINITY;
-      for (int k = lane; k < N; k += 32) mx = fmaxf(mx, sc[k]);
+
+    // ---- scores: LPE lanes per entry, lane l covers dims [8l, 8l+8) and
+    // their rotate-half partners [8l+HALF, 8l+HALF+8)
+    if (!mbar_wait(&bar_k, 0, status)) att_ok = false;
+    att_ok = __syncthreads_and(att_ok);
+    const int sub = lane / LPE, l8 = lane % LPE;
+    const int i0 = 8 * l8;  // first frequency index of this lane
+    if (att_ok && ne > 0) {
+      // (cos, sin) of this lane's 8 frequencies at its first position, and
+      // the rotation by STRIDE positions that advances it
+      const int e_first = warp * EPW + sub;
+      float cz[8], sz[8], cst[8], sst[8];
+      {
+        const float2* r0 = cp.rope + (size_t)min(k0 + e_first, c - 1) * HALF + i0;
+        const float2* rs = cp.rope + (size_t)STRIDE * HALF + i0;
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-      float sum = 0.f;
-      for (int k = lane; k < N; k += 32) {
-        const float p = exp2f(sc[k] - mx);
-        sc[k] = p;
-        sum += p;
+        for (int j = 0; j < 8; ++j) {
+          const float2 t0 = r0[j], ts = rs[j];
+          cz[j] = t0.x; sz[j] = t0.y; cst[j] = ts.x; sst[j] = ts.y;
+        }
       }
+      for (int eb = 0; eb < ne; eb += STRIDE) {
+        const int e = eb + e_first;
+        const bool live = e < ne;
+        float lo[8], hi[8];
+        const uint16_t* row = sK + (size_t)(live ? e : 0) * D;
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(row + i0), lo);
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(row + i0 + HALF), hi);
+        float rl[8], rh[8];
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-      const float inv = 1.f / sum;
-      for (int k = lane; k < N; k += 32) sc[k] *= inv;
-    }
-    __syncthreads();
-    // P V
-    float acc[G][8];
-#pragma unroll
-    for (int hh = 0; hh < G; ++hh)
-#pragma unroll
-      for (int j = 0; j < 8; ++j) acc[hh][j] = 0.f;
-    for (int k0 = warp * EPW; k0 < N; k0 += kWarps * EPW) {
-      const int k = k0 + sub;
-      if (k < N) {
-        const int slot = slot_of(k, nm, a, s, ring);
-        float x[8];
-        bf16x8_to_f32(*reinterpret_cast<const uint4*>(vh + (size_t)slot * D + e0), x);
+        for (int j = 0; j < 8; ++j) {
+          rl[j] = lo[j] * cz[j] - hi[j] * sz[j];
+          rh[j] = hi[j] * cz[j] + lo[j] * sz[j];
+        }
 #pragma unroll
         for (int hh = 0; hh < G; ++hh) {
-          const float p = scores[hh * SP + k];
+          const float4* qa = reinterpret_cast<const float4*>(sQ + hh * D + i0);
+          const float4* qb = reinterpret_cast<const float4*>(sQ + hh * D + i0 + HALF);
+          const float4 a0 = qa[0], a1 = qa[1], b0 = qb[0], b1 = qb[1];
+          float acc = rl[0] * a0.x;
+          acc = fmaf(rl[1], a0.y, acc); acc = fmaf(rl[2], a0.z, acc); acc = fmaf(rl[3], a0.w, acc);
+          acc = fmaf(rl[4], a1.x, acc); acc = fmaf(rl[5], a1.y, acc); acc = fmaf(rl[6], a1.z, acc);
+          acc = fmaf(rl[7], a1.w, acc);
+          acc = fmaf(rh[0], b0.x, acc); acc = fmaf(rh[1], b0.y, acc); acc = fmaf(rh[2], b0.z, acc);
+          acc = fmaf(rh[3], b0.w, acc); acc = fmaf(rh[4], b1.x, acc); acc = fmaf(rh[5], b1.y, acc);
+          acc = fmaf(rh[6], b1.z, acc); acc = fmaf(rh[7], b1.w, acc);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) acc[hh][j] = fmaf(p, x[j], acc[hh][j]);
+          for (int off = LPE / 2; off > 0; off >>= 1)
+            acc += __shfl_xor_sync(0xffffffffu, acc, off);
+          if (live && l8 == 0) sP[hh * args.emax + e] = acc * args.scale_log2;
+        }
+        // advance the angles by STRIDE positions
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float cn = cz[j] * cst[j] - sz[j] * sst[j];
+          const float sn = sz[j] * cst[j] + cz[j] * sst[j];
+          cz[j] = cn;
+          sz[j] = sn;
         }
       }
     }
+    __syncthreads();
+    // ---- local softmax statistics, one warp per head
+    for (int hh = warp; hh < G; hh += kWarps) {
+      float* sc = sP + hh * args.emax;
+      float mx = -INFINITY;
+      if (att_ok)
+        for (int e = lane; e < ne; e += 32) mx = fmaxf(mx, sc[e]);
 #pragma unroll
-    for (int hh = 0; hh < G; ++hh)
+      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      float sum = 0.f;
+      if (att_ok)
+        for (int e = lane; e < ne; e += 32) {
+          const float p = exp2f(sc[e] - mx);
+          sc[e] = p;
+          sum += p;
+        }
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-#pragma unroll
-        for (int off = LPE; off < 32; off <<= 1)
-          acc[hh][j] += __shfl_xor_sync(0xffffffffu, acc[hh][j], off);
+      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+      if (lane == 0) {
+        sM[hh] = mx;
+        sL[hh] = sum;
       }
-    if (sub == 0) {
+    }
+    __syncthreads();
+    // ---- P V: thread = (entry slice, 16-byte chunk of the row)
+    if (!mbar_wait(&bar_v, 0, status)) att_ok = false;
+    att_ok = __syncthreads_and(att_ok);
+    {
+      const int ch = tid % CPR, sl = tid / CPR;
+      float acc[G][8];
 #pragma unroll
       for (int hh = 0; hh < G; ++hh)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) partial[(warp * G + hh) * D + e0 + j] = acc[hh][j];
-    }
-    __syncthreads();
-    for (int e = tid; e < G * D; e += kThreads) {
-      const int hh = e / D, x = e % D;
-      float sacc = 0.f;
+        for (int j = 0; j < 8; ++j) acc[hh][j] = 0.f;
+      if (att_ok) {
+#pragma unroll 4
+        for (int e = sl; e < ne; e += NSLICE) {
+          float x[8];
+          bf16x8_to_f32(*reinterpret_cast<const uint4*>(sV + (size_t)e * D + 8 * ch), x);
 #pragma unroll
-      for (int r = 0; r < kWarps; ++r) sacc += partial[(r * G + hh) * D + x];
-      const __nv_bfloat16 b = __float2bfloat16_rn(sacc);
-      out[(((size_t)sq * args.Hq) + g * G + hh) * D + x] = *reinterpret_cast<const uint16_t*>(&b);
+          for (int hh = 0; hh < G; ++hh) {
+            const float p = sP[hh * args.emax + e];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[hh][j] = fmaf(p, x[j], acc[hh][j]);
+          }
+        }
+      }
+      // slices inside a warp, then across warps through shared memory
+#pragma unroll
+      for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+#pragma unroll
+          for (int off = CPR; off < 32; off <<= 1)
+            acc[hh][j] += __shfl_xor_sync(0xffffffffu, acc[hh][j], off);
+      __syncthreads();  // sK (aliased by sRed) is no longer read
+      if (lane < CPR) {
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) sRed[(warp * G + hh) * D + 8 * ch + j] = acc[hh][j];
+      }
+      __syncthreads();
+      for (int e = tid; e < G * D; e += kThreads) {
+        float t = 0.f;
+#pragma unroll
+        for (int r = 0; r < kWarps; ++r) t += sRed[r * G * D + e];
+        sAcc[e] = t;
+      }
     }
   }
 
-  cluster_wait();  // every CTA of the sequence has read the old metadata
-  if (rank0) {
+  // ---- merge the cluster's partial states (CTA 0), then write the update
+  cluster_arrive();
+  cluster_wait();
+  if (rank == 0) {
+    if (attend && att_ok) {
+      for (int e = tid; e < G * D; e += kThreads) {
+        const int hh = e / D;
+        float mr[kMaxSplit];
+        float M = -INFINITY;
+        for (int r = 0; r < split; ++r) {
+          mr[r] = dsmem_ld(dsmem_addr(sM + hh, r));
+          M = fmaxf(M, mr[r]);
+        }
+        float num = 0.f, den = 0.f;
+        for (int r = 0; r < split; ++r) {
+          if (mr[r] == -INFINITY) continue;
+          const float f = exp2f(mr[r] - M);
+          num = fmaf(f, dsmem_ld(dsmem_addr(sAcc + e, r)), num);
+          den = fmaf(f, dsmem_ld(dsmem_addr(sL + hh, r)), den);
+        }
+        const __nv_bfloat16 b = __float2bfloat16_rn(num / den);
+        out[(((size_t)sq * args.Hq) + g * G + hh) * D + (e % D)] =
+            *reinterpret_cast<const uint16_t*>(&b);
+      }
+    }
     if (!ok) {
       if (tid == 0) report(status, SEP_ERR_DEVICE_BOUNDS);
     } else {
+      // the update: surviving separators into the separator ring, then the
+      // new token (its slot may be one a survivor was read from)
+      const size_t head_off = mh * (size_t)NSL * D;
+      uint16_t* kh = cp.k + head_off;
+      uint16_t* vh = cp.v + head_off;
+      uint8_t* sepw = cp.issep + mh * NSL;
       int32_t* posw = cp.pos + (size_t)sq * NSL;
-      uint8_t* sepw = cp.issep + (size_t)sq * NSL;
+      const int n_surv = pl.SV;
+      for (int e = tid; e < n_surv * CPR; e += kThreads) {
+        const int r = e / CPR, u = e % CPR;
+        const int dst = a + (pl.sk0 + pl.SK + r) % s;
+        const size_t so = (size_t)surv_src[r] * D + 8 * u, dso = (size_t)dst * D + 8 * u;
+        const uint4 kx = *reinterpret_cast<const uint4*>(kh + so);
+        const uint4 vx = *reinterpret_cast<const uint4*>(vh + so);
+        *reinterpret_cast<uint4*>(kh + dso) = kx;
+        *reinterpret_cast<uint4*>(vh + dso) = vx;
+      }
       for (int r = tid; r < n_surv; r += kThreads) {
-        posw[sep_dst[r]] = src_pos[r];
-        sepw[sep_dst[r]] = 1;
+        const int dst = a + (pl.sk0 + pl.SK + r) % s;
+        sepw[dst] = 1;
+        if (g == 0) posw[dst] = surv_pos[r];
       }
       __syncthreads();
+      const int32_t new_id = ids_new[sq];
+      bool new_is_sep = false;
+      for (int x = 0; x < args.sids.n; ++x) new_is_sep |= (new_id == args.sids.ids[x]);
+      for (int u = tid; u < CPR; u += kThreads) {
+        *reinterpret_cast<uint4*>(kh + (size_t)new_slot * D + 8 * u) =
+            *reinterpret_cast<const uint4*>(k_new + mh * D + 8 * u);
+        *reinterpret_cast<uint4*>(vh + (size_t)new_slot * D + 8 * u) =
+            *reinterpret_cast<const uint4*>(v_new + mh * D + 8 * u);
+      }
       if (tid == 0) {
-        posw[new_slot] = m.t;
         sepw[new_slot] = new_is_sep ? 1 : 0;
-        cp.meta[sq] = nm;
+        if (g == 0) posw[new_slot] = m.t;
+        cp.meta[mh] = nm;
       }
     }
   }
+  // CTA 0 has read every partial before any CTA's shared memory goes away
+  cluster_arrive();
+  cluster_wait();
+}
+
+int pick_split(int S, int Hkv, int c) {
+  const int pairs = S * Hkv;
+  int sp = (kTargetCtas + pairs - 1) / pairs;
+  sp = sp < 1 ? 1 : (sp > kMaxSplit ? kMaxSplit : sp);
+  const int by_len = c / 16 > 1 ? c / 16 : 1;  // at least ~16 entries per CTA
+  return sp < by_len ? sp : by_len;
 }
 
 template <int D, int G>
-cudaError_t launch_step_t(const CachePtrs& cp, const StepArgs& args, const void* q,
-                          const void* k_new, const void* v_new, const int32_t* ids_new,
-                          void* out, int* status, cudaStream_t stream) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(args.Hkv, args.S, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  const size_t smem = StepSmem<D, G>::bytes(args.c);
+cudaError_t launch_step_t(const CachePtrs& cp, StepArgs args, const void* q, const void* k_new,
+                          const void* v_new, const int32_t* ids_new, void* out, int* status,
+                          cudaStream_t stream) {
+  const size_t smem = step_smem(D, G, args.emax).total;
   if (smem > 48 * 1024) {
     const cudaError_t e = cudaFuncSetAttribute(
         cache_step_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(args.split, args.Hkv, args.S);
+  cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = args.Hkv;
+  attr[0].val.clusterDim.x = args.split;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
@@ -450,8 +631,8 @@ cudaError_t launch_step(const CachePtrs& cp, const StepArgs& args, int d, int G,
 sep_status shape_check(const sep_cache_params* p) {
   if (!params_ok(p)) return SEP_ERR_INVALID_ARG;
   if (!(p->a + p->s + p->w < p->c)) return SEP_ERR_CAPACITY;
-  if (p->Hkv > 8 || (p->d != 64 && p->d != 128)) return SEP_ERR_UNSUPPORTED;
-  if (p->c > kMaxPast) return SEP_ERR_UNSUPPORTED;
+  if (p->Hkv > kMaxHkv || (p->d != 64 && p->d != 128)) return SEP_ERR_UNSUPPORTED;
+  if (p->c > kMaxC) return SEP_ERR_UNSUPPORTED;
   return SEP_OK;
 }
 
@@ -460,12 +641,13 @@ float theta_of(const sep_cache_params* p) {
 }
 
 // RoPE table in double precision: inv_freq_i = theta^(-2i/d), entry
-// [pos][i] = (cos(pos * inv_freq_i), sin(pos * inv_freq_i)).
-std::vector<float2> rope_table(const sep_cache_params* p) {
+// [pos][i] = (cos(pos * inv_freq_i), sin(pos * inv_freq_i)), for positions
+// 0 .. rope_rows-1.
+std::vector<float2> rope_table(const sep_cache_params* p, int rows) {
   const int half = p->d / 2;
-  std::vector<float2> t((size_t)p->c * half);
+  std::vector<float2> t((size_t)rows * half);
   const double theta = theta_of(p);
-  for (int pos = 0; pos < p->c; ++pos)
+  for (int pos = 0; pos < rows; ++pos)
     for (int i = 0; i < half; ++i) {
       const double f = pow(theta, -2.0 * i / p->d);
       t[(size_t)pos * half + i] = make_float2(static_cast<float>(cos(pos * f)),
@@ -499,7 +681,7 @@ SEP_API sep_status sep_cache_init(const sep_cache_params* p, void* cache_buf, si
   const CacheLayout l = cache_layout(p);
   if (bytes < l.total) return SEP_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const std::vector<float2> tab = rope_table(p);
+  const std::vector<float2> tab = rope_table(p, l.rope_rows);
   if (cudaMemsetAsync(cache_buf, 0, l.total, s) != cudaSuccess) return SEP_ERR_CUDA;
   if (cudaMemcpyAsync(static_cast<char*>(cache_buf) + l.rope, tab.data(),
                       tab.size() * sizeof(float2), cudaMemcpyHostToDevice, s) != cudaSuccess)
@@ -533,6 +715,8 @@ SEP_API sep_status sep_cache_step(const sep_cache_params* p, void* cache_buf, co
   args.w = p->w; args.c = p->c;
   const CacheLayout l = cache_layout(p);
   args.NSL = l.NSL;
+  args.split = q ? pick_split(p->S, p->Hkv, p->c) : 1;
+  args.emax = (p->c + args.split - 1) / args.split + 1;
   if (!(scale > 0.f)) scale = 1.0f / sqrtf(static_cast<float>(p->d));
   args.scale_log2 = scale * 1.4426950408889634f;
   int* status = device_status_ptr();
@@ -616,7 +800,11 @@ SEP_API sep_status sep_cache_export(const sep_cache_params* p, const void* cache
   memcpy(im.header, hdr, sizeof(hdr));
   const int ring = p->c - p->a, NSL = hc.l.NSL, HD = p->Hkv * p->d;
   for (int sq = 0; sq < p->S; ++sq) {
-    const Meta m = hc.meta()[sq];
+    const Meta m = hc.meta()[(size_t)sq * p->Hkv];
+    // every kv head keeps its own copy of the counters; they must agree
+    for (int g = 1; g < p->Hkv; ++g)
+      if (memcmp(&hc.meta()[(size_t)sq * p->Hkv + g], &m, sizeof(Meta)) != 0)
+        return SEP_ERR_DEVICE_BOUNDS;
     const int n_win = m.n_pw < p->w ? m.n_pw : p->w;
     const int total = m.n_init + m.n_sep + m.n_pw;
     if (total > p->c || m.n_init > p->a || m.n_sep > p->s || m.n_pw > ring)
@@ -628,7 +816,7 @@ SEP_API sep_status sep_cache_export(const sep_cache_params* p, const void* cache
     for (int k = 0; k < total; ++k) {
       const int slot = host_slot(k, m, p->a, p->s, ring);
       im.pos[(size_t)sq * p->c + k] = hc.pos()[(size_t)sq * NSL + slot];
-      im.issep[(size_t)sq * p->c + k] = hc.issep()[(size_t)sq * NSL + slot];
+      im.issep[(size_t)sq * p->c + k] = hc.issep()[(size_t)sq * p->Hkv * NSL + slot];
       for (int g = 0; g < p->Hkv; ++g) {
         const size_t src = (((size_t)sq * p->Hkv + g) * NSL + slot) * p->d;
         const size_t dst = ((size_t)sq * p->c + k) * HD + (size_t)g * p->d;
@@ -652,7 +840,7 @@ SEP_API sep_status sep_cache_import(const sep_cache_params* p, void* cache_buf,
   HostCache hc;
   hc.l = cache_layout(p);
   hc.raw.assign(hc.l.total, 0);
-  const std::vector<float2> tab = rope_table(p);
+  const std::vector<float2> tab = rope_table(p, hc.l.rope_rows);
   memcpy(hc.raw.data() + hc.l.rope, tab.data(), tab.size() * sizeof(float2));
   const int ring = p->c - p->a, NSL = hc.l.NSL, HD = p->Hkv * p->d;
   for (int sq = 0; sq < p->S; ++sq) {
@@ -668,12 +856,12 @@ SEP_API sep_status sep_cache_import(const sep_cache_params* p, void* cache_buf,
         cnt[3] < 0 || cnt[3] > p->w || m.n_pw > ring || total != cnt[4] || total > p->c ||
         (cnt[2] > 0 && cnt[3] != p->w) || (m.n_init < p->a && (m.n_sep | m.n_pw) != 0))
       return SEP_ERR_INVALID_ARG;
-    hc.meta()[sq] = m;
+    for (int g = 0; g < p->Hkv; ++g) hc.meta()[(size_t)sq * p->Hkv + g] = m;
     for (int k = 0; k < total; ++k) {
       const int slot = host_slot(k, m, p->a, p->s, ring);
       hc.pos()[(size_t)sq * NSL + slot] = im.pos[(size_t)sq * p->c + k];
-      hc.issep()[(size_t)sq * NSL + slot] = im.issep[(size_t)sq * p->c + k];
       for (int g = 0; g < p->Hkv; ++g) {
+        hc.issep()[((size_t)sq * p->Hkv + g) * NSL + slot] = im.issep[(size_t)sq * p->c + k];
         const size_t dst = (((size_t)sq * p->Hkv + g) * NSL + slot) * p->d;
         const size_t src = ((size_t)sq * p->c + k) * HD + (size_t)g * p->d;
         memcpy(hc.k() + dst, im.k + src, 2 * p->d);

@@ -74,6 +74,10 @@ inline IndexPtrs index_ptrs(void* buf, const IndexLayout& l) {
   return r;
 }
 
+// Records the calling thread's registered profiling event `i` on `stream`
+// (no-op when none is registered at that index).  Defined in api.cu.
+void profile_mark(int i, void* stream);
+
 // Device address of the library's status word on the current device (null if
 // the CUDA runtime is unavailable).  Defined in api.cu.
 int* device_status_ptr();

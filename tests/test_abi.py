@@ -93,8 +93,12 @@ def test_cache_host_checks():
     full = api.cache_params(64, 8, 128, 4, 32, 288, 324)   # a + s + w == c: no room to compress
     assert L_.sep_cache_bytes(ctypes.byref(full)) == 0
     assert L_.sep_cache_init(ctypes.byref(full), ctypes.c_void_p(256), 1 << 30, None) == 3
-    wide = api.cache_params(4, 16, 128, 4, 32, 256, 324)   # more kv heads than a cluster holds
+    odd_d = api.cache_params(4, 8, 96, 4, 32, 256, 324)    # head dim without a kernel
+    assert L_.sep_cache_init(ctypes.byref(odd_d), ctypes.c_void_p(256), 1 << 30, None) == 2
+    wide = api.cache_params(4, 65, 128, 4, 32, 256, 324)   # more kv heads than supported
     assert L_.sep_cache_init(ctypes.byref(wide), ctypes.c_void_p(256), 1 << 30, None) == 2
+    big = api.cache_params(4, 8, 128, 4, 32, 256, 1025)    # capacity above the kernel's limit
+    assert L_.sep_cache_bytes(ctypes.byref(big)) == 0
     assert L_.sep_cache_init(ctypes.byref(good), ctypes.c_void_p(256), 100, None) == 7
     P = ctypes.c_void_p(4096)
     arr = (ctypes.c_int32 * 1)(1)
