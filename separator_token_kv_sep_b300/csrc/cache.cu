@@ -174,23 +174,10 @@ struct StepPlan {
   int sk0, pw0;
 };
 
-// Slot of logical entry k < N-1, or -1 for the new token.
-__device__ __forceinline__ int plan_slot(int k, const StepPlan& pl, const int* surv_src, int a,
-                                         int s, int ring) {
-  if (k < pl.I0) return k;
-  k -= pl.I0;
-  if (k < pl.SK) return a + (pl.sk0 + k) % s;
-  k -= pl.SK;
-  if (k < pl.SV) return surv_src[k];
-  k -= pl.SV;
-  if (k < pl.W0) return a + s + (pl.pw0 + k) % ring;
-  return -1;
-}
-
 // Dynamic shared memory of the step kernel (byte offsets; every region is
 // 16-byte aligned).
 struct StepSmem {
-  int k, v, q, p, acc, red, src, total;
+  int k, v, q, p, acc, red, total;
 };
 
 __host__ __device__ inline StepSmem step_smem(int D, int G, int emax) {
@@ -209,8 +196,6 @@ __host__ __device__ inline StepSmem step_smem(int D, int G, int emax) {
   m.acc = off;
   off += al(G * D * 4 + 2 * G * 4);  // acc[G][D], then m[G], l[G]
   m.red = m.k;
-  m.src = off;
-  off += al(emax * 4);
   m.total = off;
   return m;
 }
@@ -251,7 +236,6 @@ __global__ void __launch_bounds__(kThreads)
   float* sM = sAcc + G * D;
   float* sL = sM + G;
   float* sRed = reinterpret_cast<float*>(dsm + L.red);
-  int* sSrc = reinterpret_cast<int*>(dsm + L.src);
 
   const size_t mh = (size_t)sq * args.Hkv + g;  // (sequence, kv head)
   const Meta m = cp.meta[mh];
@@ -341,25 +325,49 @@ __global__ void __launch_bounds__(kThreads)
     const uint16_t* kh = cp.k + head_off;
     const uint16_t* vh = cp.v + head_off;
     const size_t new_off = mh * D;  // [S][Hkv][D] inputs
-    for (int e = tid; e < ne; e += kThreads)
-      sSrc[e] = plan_slot(k0 + e, pl, surv_src, a, s, ring);
+    // thread 0 arms both barriers before any thread issues a copy
     if (tid == 0) {
       mbar_init(&bar_k, 1);
       mbar_init(&bar_v, 1);
       fence_mbar_init();
-    }
-    __syncthreads();
-    if (tid == 0) {
       mbar_arrive_expect_tx(&bar_k, (uint32_t)(ne * D * 2));
       mbar_arrive_expect_tx(&bar_v, (uint32_t)(ne * D * 2));
     }
     __syncthreads();
-    for (int e = tid; e < ne; e += kThreads) {
-      const int slot = sSrc[e];
-      const uint16_t* srck = slot >= 0 ? kh + (size_t)slot * D : k_new + new_off;
-      const uint16_t* srcv = slot >= 0 ? vh + (size_t)slot * D : v_new + new_off;
-      bulk_g2s(sK + (size_t)e * D, srck, D * 2, &bar_k);
-      bulk_g2s(sV + (size_t)e * D, srcv, D * 2, &bar_v);
+    // Bulk copies of entries [k0, k1) into shared rows [0, ne), as runs of
+    // consecutive slots: the initial block, the kept separator-ring run, the
+    // window-ring run (each ring run in two pieces where it wraps), then the
+    // separators moving this step one row each, and the new token.
+    if (ne > 0) {
+      const int rS = pl.I0, rV = rS + pl.SK, rW = rV + pl.SV, rN = pl.N - 1;
+      auto run = [&](int lo, int hi, int slot0) {  // slots slot0 .. slot0+hi-lo-1
+        if (hi <= lo) return;
+        const uint32_t bytes = (uint32_t)((hi - lo) * D * 2);
+        bulk_g2s(sK + (size_t)(lo - k0) * D, kh + (size_t)slot0 * D, bytes, &bar_k);
+        bulk_g2s(sV + (size_t)(lo - k0) * D, vh + (size_t)slot0 * D, bytes, &bar_v);
+      };
+      auto ring_run = [&](int r_lo, int r_hi, int base_slot, int head, int size) {
+        const int lo = max(r_lo, k0), hi = min(r_hi, k1);
+        if (hi <= lo) return;
+        const int p0 = (head + (lo - r_lo)) % size;
+        const int n1 = min(hi - lo, size - p0);
+        run(lo, lo + n1, base_slot + p0);
+        run(lo + n1, hi, base_slot);
+      };
+      if (tid == 0) {
+        run(max(0, k0), min(rS, k1), max(0, k0));
+        if (s > 0) ring_run(rS, rV, a, pl.sk0, s);
+        ring_run(rW, rN, a + s, pl.pw0, ring);
+        if (k0 <= rN && rN < k1) {
+          bulk_g2s(sK + (size_t)(rN - k0) * D, k_new + new_off, D * 2, &bar_k);
+          bulk_g2s(sV + (size_t)(rN - k0) * D, v_new + new_off, D * 2, &bar_v);
+        }
+      }
+      for (int k = max(rV, k0) + tid; k < min(rW, k1); k += kThreads) {
+        const int slot = surv_src[k - rV];
+        bulk_g2s(sK + (size_t)(k - k0) * D, kh + (size_t)slot * D, D * 2, &bar_k);
+        bulk_g2s(sV + (size_t)(k - k0) * D, vh + (size_t)slot * D, D * 2, &bar_v);
+      }
     }
     // rotated queries of the G heads at position N-1
     if (ok) {
@@ -494,9 +502,11 @@ __global__ void __launch_bounds__(kThreads)
       __syncthreads();  // sK (aliased by sRed) is no longer read
       if (lane < CPR) {
 #pragma unroll
-        for (int hh = 0; hh < G; ++hh)
-#pragma unroll
-          for (int j = 0; j < 8; ++j) sRed[(warp * G + hh) * D + 8 * ch + j] = acc[hh][j];
+        for (int hh = 0; hh < G; ++hh) {
+          float4* dst = reinterpret_cast<float4*>(sRed + (warp * G + hh) * D + 8 * ch);
+          dst[0] = make_float4(acc[hh][0], acc[hh][1], acc[hh][2], acc[hh][3]);
+          dst[1] = make_float4(acc[hh][4], acc[hh][5], acc[hh][6], acc[hh][7]);
+        }
       }
       __syncthreads();
       for (int e = tid; e < G * D; e += kThreads) {
@@ -508,31 +518,43 @@ __global__ void __launch_bounds__(kThreads)
     }
   }
 
-  // ---- merge the cluster's partial states (CTA 0), then write the update
+  // ---- merge the cluster's partial states, then (CTA 0) write the update
   cluster_arrive();
   cluster_wait();
-  if (rank == 0) {
-    if (attend && att_ok) {
-      for (int e = tid; e < G * D; e += kThreads) {
-        const int hh = e / D;
-        float mr[kMaxSplit];
-        float M = -INFINITY;
-        for (int r = 0; r < split; ++r) {
+  // every CTA merges its own slice of the G*D outputs from all partials
+  if (attend && att_ok) {
+    const int per = (G * D + split - 1) / split;
+    const int e_lo = rank * per, e_hi = min(G * D, e_lo + per);
+    for (int e = e_lo + tid; e < e_hi; e += kThreads) {
+      const int hh = e / D;
+      float mr[kMaxSplit], ar[kMaxSplit], lr[kMaxSplit];
+#pragma unroll
+      for (int r = 0; r < kMaxSplit; ++r) {
+        if (r < split) {
           mr[r] = dsmem_ld(dsmem_addr(sM + hh, r));
-          M = fmaxf(M, mr[r]);
+          lr[r] = dsmem_ld(dsmem_addr(sL + hh, r));
+          ar[r] = dsmem_ld(dsmem_addr(sAcc + e, r));
         }
-        float num = 0.f, den = 0.f;
-        for (int r = 0; r < split; ++r) {
-          if (mr[r] == -INFINITY) continue;
-          const float f = exp2f(mr[r] - M);
-          num = fmaf(f, dsmem_ld(dsmem_addr(sAcc + e, r)), num);
-          den = fmaf(f, dsmem_ld(dsmem_addr(sL + hh, r)), den);
-        }
-        const __nv_bfloat16 b = __float2bfloat16_rn(num / den);
-        out[(((size_t)sq * args.Hq) + g * G + hh) * D + (e % D)] =
-            *reinterpret_cast<const uint16_t*>(&b);
       }
+      float M = -INFINITY;
+#pragma unroll
+      for (int r = 0; r < kMaxSplit; ++r)
+        if (r < split) M = fmaxf(M, mr[r]);
+      float num = 0.f, den = 0.f;
+#pragma unroll
+      for (int r = 0; r < kMaxSplit; ++r) {
+        if (r < split && mr[r] != -INFINITY) {
+          const float f = exp2f(mr[r] - M);
+          num = fmaf(f, ar[r], num);
+          den = fmaf(f, lr[r], den);
+        }
+      }
+      const __nv_bfloat16 bv = __float2bfloat16_rn(num / den);
+      out[(((size_t)sq * args.Hq) + g * G + hh) * D + (e % D)] =
+          *reinterpret_cast<const uint16_t*>(&bv);
     }
+  }
+  if (rank == 0) {
     if (!ok) {
       if (tid == 0) report(status, SEP_ERR_DEVICE_BOUNDS);
     } else {
@@ -575,7 +597,7 @@ __global__ void __launch_bounds__(kThreads)
       }
     }
   }
-  // CTA 0 has read every partial before any CTA's shared memory goes away
+  // every CTA has read the partials it needs before any shared memory goes away
   cluster_arrive();
   cluster_wait();
 }
