@@ -49,12 +49,14 @@ namespace sep {
 namespace {
 
 constexpr int kCacheMagic = 0x43504553;  // 'SEPC'
-constexpr int kThreads = 128;            // 4 warps per CTA
+constexpr int kConsumerWarps = 4;        // score / softmax / P.V warps
+constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one TMA producer warp
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxC = 1024;              // survivor list is kept in shared memory
 constexpr int kMaxHkv = 64;
 constexpr int kMaxSplit = 8;             // portable cluster size
-constexpr int kTargetCtas = 2048;        // CTAs per step the split aims at
+constexpr float kLazyRescale = 8.0f;     // log2 growth of the max before a rescale
+constexpr int kTargetCtas = 296;         // CTAs per step the split aims at (2 per SM)
 
 struct CacheLayout {
   int S, Hkv, d, a, s, w, c, NSL, rope_rows;
@@ -117,7 +119,7 @@ CachePtrs cache_ptrs(void* buf, const CacheLayout& l) {
 }
 
 struct StepArgs {
-  int S, Hkv, Hq, a, s, w, c, NSL, split, emax;
+  int S, Hkv, Hq, a, s, w, c, NSL, split;
   float scale_log2;
   SepIdList sids;
 };
@@ -152,6 +154,25 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// Packed fp32 pairs (f32x2): d = a * b + c and d = a * b, two lanes' worth
+// of arithmetic in one instruction.
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b0,
+                                      float b1, float c0, float c1) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void fmul2(float& d0, float& d1, float a0, float a1, float b0,
+                                      float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 __device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float* f) {
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -174,52 +195,67 @@ struct StepPlan {
   int sk0, pw0;
 };
 
-// Dynamic shared memory of the step kernel (byte offsets; every region is
-// 16-byte aligned).
-struct StepSmem {
-  int k, v, q, p, acc, red, total;
+// Streaming shape of the decode attention: a chunk is the entries the four
+// consumer warps score in one pass (LPE lanes per entry), and NST chunks
+// of K and V rows are in flight through the TMA ring.
+template <int D>
+struct StreamShape {
+  static constexpr int HALF = D / 2;
+  static constexpr int CPR = D / 8;          // 16-byte pieces per row
+  static constexpr int LPE = CPR / 2;        // lanes per entry when scoring
+  static constexpr int EPW = 32 / LPE;       // entries per warp per chunk
+  static constexpr int CH = kConsumerWarps * EPW;  // entries per chunk
+  static constexpr int DPL = D / 32;         // output dims per lane
+  static constexpr int NST = 4;              // ring stages
+  static constexpr int STAGE = 2 * CH * D * 2;  // bytes: K rows then V rows
 };
 
-__host__ __device__ inline StepSmem step_smem(int D, int G, int emax) {
+// Dynamic shared memory of the step kernel (byte offsets, 16-byte aligned).
+struct StepSmem {
+  int ring, q, wstate, part, pw, surv, total;
+};
+
+template <int D, int G>
+__host__ __device__ inline StepSmem step_smem(int s_cap) {
+  using SS = StreamShape<D>;
   auto al = [](int x) { return (x + 15) / 16 * 16; };
   StepSmem m;
   int off = 0;
-  m.k = off;
-  const int kbytes = emax * D * 2, redbytes = kWarps * G * D * 4;
-  off += al(kbytes > redbytes ? kbytes : redbytes);  // the PV reduction reuses the K rows
-  m.v = off;
-  off += al(emax * D * 2);
+  m.ring = off;
+  off += SS::NST * SS::STAGE;
   m.q = off;
   off += al(G * D * 4);
-  m.p = off;
-  off += al(G * emax * 4);
-  m.acc = off;
-  off += al(G * D * 4 + 2 * G * 4);  // acc[G][D], then m[G], l[G]
-  m.red = m.k;
+  m.wstate = off;  // per consumer warp: acc[G][D], m[G], l[G]
+  off += al(kConsumerWarps * G * (D + 2) * 4);
+  m.part = off;    // this CTA's merged partial: acc[G][D], m[G], l[G]
+  off += al(G * (D + 2) * 4);
+  m.pw = off;      // per consumer warp: p[EPW][G] and alpha[G] of the current chunk
+  off += al(kConsumerWarps * (SS::EPW * G + G) * 4);
+  m.surv = off;    // surviving separators: window slot, text position
+  off += al(2 * (s_cap > 0 ? s_cap : 1) * 4);
   m.total = off;
   return m;
+}
+
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
 }
 
 // ---------------------------------------------------------------------------
 // The step kernel
 // ---------------------------------------------------------------------------
 template <int D, int G>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 4)
     cache_step_kernel(CachePtrs cp, StepArgs args, const uint16_t* __restrict__ q,
                       const uint16_t* __restrict__ k_new, const uint16_t* __restrict__ v_new,
                       const int32_t* __restrict__ ids_new, uint16_t* __restrict__ out,
                       int* status) {
-  constexpr int HALF = D / 2;
-  constexpr int CPR = D / 8;       // 16-byte chunks per row
-  constexpr int LPE = CPR / 2;     // lanes per entry in the score phase (low chunk + partner)
-  constexpr int EPW = 32 / LPE;    // entries per warp per score iteration
-  constexpr int STRIDE = kWarps * EPW;  // entries per CTA per score iteration (16 or 32)
-  constexpr int NSLICE = kThreads / CPR;  // entry slices in the PV phase
+  using SS = StreamShape<D>;
+  constexpr int HALF = SS::HALF, CPR = SS::CPR, LPE = SS::LPE, EPW = SS::EPW, CH = SS::CH,
+                DPL = SS::DPL, NST = SS::NST;
   extern __shared__ __align__(128) uint8_t dsm[];
-  __shared__ int surv_src[kMaxC];
-  __shared__ int surv_pos[kMaxC];
   __shared__ int warp_cnt[kWarps];
-  __shared__ __align__(8) uint64_t bar_k, bar_v;
+  __shared__ __align__(8) uint64_t full_bar[NST], empty_bar[NST];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int rank = blockIdx.x, g = blockIdx.y, sq = blockIdx.z;
@@ -227,15 +263,15 @@ __global__ void __launch_bounds__(kThreads)
   const int a = args.a, s = args.s, w = args.w, c = args.c, NSL = args.NSL;
   const int ring = c - a;
   const bool attend = q != nullptr && out != nullptr;
-  const StepSmem L = step_smem(D, G, args.emax);
-  uint16_t* sK = reinterpret_cast<uint16_t*>(dsm + L.k);
-  uint16_t* sV = reinterpret_cast<uint16_t*>(dsm + L.v);
+  const StepSmem L = step_smem<D, G>(s);
   float* sQ = reinterpret_cast<float*>(dsm + L.q);
-  float* sP = reinterpret_cast<float*>(dsm + L.p);
-  float* sAcc = reinterpret_cast<float*>(dsm + L.acc);
+  float* sW = reinterpret_cast<float*>(dsm + L.wstate);
+  float* sAcc = reinterpret_cast<float*>(dsm + L.part);
   float* sM = sAcc + G * D;
   float* sL = sM + G;
-  float* sRed = reinterpret_cast<float*>(dsm + L.red);
+  float* sPx = reinterpret_cast<float*>(dsm + L.pw);
+  int* surv_src = reinterpret_cast<int*>(dsm + L.surv);
+  int* surv_pos = surv_src + (s > 0 ? s : 1);
 
   const size_t mh = (size_t)sq * args.Hkv + g;  // (sequence, kv head)
   const Meta m = cp.meta[mh];
@@ -314,214 +350,320 @@ __global__ void __launch_bounds__(kThreads)
   }
   pl.N = pl.I0 + pl.SK + pl.SV + pl.W0 + 1;
 
-  // ---- attention over this CTA's share [k0, k1) of the new layout
+  // ---- attention over this CTA's share [k0, k1) of the new layout, streamed
+  // in chunks of CH entries through an NST-stage ring of TMA bulk copies
   bool att_ok = ok && attend;
+  const size_t head_off = mh * (size_t)NSL * D;
   if (attend) {
     const int N = pl.N;
     const int k0 = (int)(((long long)N * rank) / split);
     const int k1 = (int)(((long long)N * (rank + 1)) / split);
     const int ne = ok ? k1 - k0 : 0;
-    const size_t head_off = mh * (size_t)NSL * D;
-    const uint16_t* kh = cp.k + head_off;
-    const uint16_t* vh = cp.v + head_off;
-    const size_t new_off = mh * D;  // [S][Hkv][D] inputs
-    // thread 0 arms both barriers before any thread issues a copy
+    const int n_chunks = (ne + CH - 1) / CH;
     if (tid == 0) {
-      mbar_init(&bar_k, 1);
-      mbar_init(&bar_v, 1);
+      for (int st = 0; st < NST; ++st) {
+        mbar_init(&full_bar[st], 1);
+        mbar_init(&empty_bar[st], kConsumerWarps);
+      }
       fence_mbar_init();
-      mbar_arrive_expect_tx(&bar_k, (uint32_t)(ne * D * 2));
-      mbar_arrive_expect_tx(&bar_v, (uint32_t)(ne * D * 2));
-    }
-    __syncthreads();
-    // Bulk copies of entries [k0, k1) into shared rows [0, ne), as runs of
-    // consecutive slots: the initial block, the kept separator-ring run, the
-    // window-ring run (each ring run in two pieces where it wraps), then the
-    // separators moving this step one row each, and the new token.
-    if (ne > 0) {
-      const int rS = pl.I0, rV = rS + pl.SK, rW = rV + pl.SV, rN = pl.N - 1;
-      auto run = [&](int lo, int hi, int slot0) {  // slots slot0 .. slot0+hi-lo-1
-        if (hi <= lo) return;
-        const uint32_t bytes = (uint32_t)((hi - lo) * D * 2);
-        bulk_g2s(sK + (size_t)(lo - k0) * D, kh + (size_t)slot0 * D, bytes, &bar_k);
-        bulk_g2s(sV + (size_t)(lo - k0) * D, vh + (size_t)slot0 * D, bytes, &bar_v);
-      };
-      auto ring_run = [&](int r_lo, int r_hi, int base_slot, int head, int size) {
-        const int lo = max(r_lo, k0), hi = min(r_hi, k1);
-        if (hi <= lo) return;
-        const int p0 = (head + (lo - r_lo)) % size;
-        const int n1 = min(hi - lo, size - p0);
-        run(lo, lo + n1, base_slot + p0);
-        run(lo + n1, hi, base_slot);
-      };
-      if (tid == 0) {
-        run(max(0, k0), min(rS, k1), max(0, k0));
-        if (s > 0) ring_run(rS, rV, a, pl.sk0, s);
-        ring_run(rW, rN, a + s, pl.pw0, ring);
-        if (k0 <= rN && rN < k1) {
-          bulk_g2s(sK + (size_t)(rN - k0) * D, k_new + new_off, D * 2, &bar_k);
-          bulk_g2s(sV + (size_t)(rN - k0) * D, v_new + new_off, D * 2, &bar_v);
-        }
-      }
-      for (int k = max(rV, k0) + tid; k < min(rW, k1); k += kThreads) {
-        const int slot = surv_src[k - rV];
-        bulk_g2s(sK + (size_t)(k - k0) * D, kh + (size_t)slot * D, D * 2, &bar_k);
-        bulk_g2s(sV + (size_t)(k - k0) * D, vh + (size_t)slot * D, D * 2, &bar_v);
-      }
-    }
-    // rotated queries of the G heads at position N-1
-    if (ok) {
-      const float2* cs_row = cp.rope + (size_t)(N - 1) * HALF;
-      for (int e = tid; e < G * HALF; e += kThreads) {
-        const int hh = e / HALF, i = e % HALF;
-        const uint16_t* qr = q + (((size_t)sq * args.Hq) + g * G + hh) * D;
-        const float2 cs = cs_row[i];
-        const float x1 = __uint_as_float((uint32_t)qr[i] << 16);
-        const float x2 = __uint_as_float((uint32_t)qr[i + HALF] << 16);
-        sQ[hh * D + i] = x1 * cs.x - x2 * cs.y;
-        sQ[hh * D + i + HALF] = x2 * cs.x + x1 * cs.y;
-      }
     }
     __syncthreads();
 
-    // ---- scores: LPE lanes per entry, lane l covers dims [8l, 8l+8) and
-    // their rotate-half partners [8l+HALF, 8l+HALF+8)
-    if (!mbar_wait(&bar_k, 0, status)) att_ok = false;
-    att_ok = __syncthreads_and(att_ok);
-    const int sub = lane / LPE, l8 = lane % LPE;
-    const int i0 = 8 * l8;  // first frequency index of this lane
-    if (att_ok && ne > 0) {
-      // (cos, sin) of this lane's 8 frequencies at its first position, and
-      // the rotation by STRIDE positions that advances it
-      const int e_first = warp * EPW + sub;
+    if (warp == kConsumerWarps) {
+      // ------------------------------------------------------------ producer
+      if (lane == 0 && ne > 0) {
+        const uint16_t* kh = cp.k + head_off;
+        const uint16_t* vh = cp.v + head_off;
+        const size_t new_off = mh * D;  // [S][Hkv][D] inputs
+        const int rS = pl.I0, rV = rS + pl.SK, rW = rV + pl.SV, rN = pl.N - 1;
+        for (int ch = 0; ch < n_chunks; ++ch) {
+          const int st = ch % NST;
+          if (ch >= NST && !mbar_wait(&empty_bar[st], ((ch / NST) - 1) & 1, status)) break;
+          const int c0 = k0 + ch * CH, c1 = min(k1, c0 + CH);
+          uint16_t* dK = reinterpret_cast<uint16_t*>(dsm + L.ring + st * SS::STAGE);
+          uint16_t* dV = dK + CH * D;
+          mbar_arrive_expect_tx(&full_bar[st], (uint32_t)((c1 - c0) * D * 2 * 2));
+          // runs of consecutive slots: slots slot0 .. slot0 + (hi - lo) - 1
+          auto run = [&](int lo, int hi, int slot0) {
+            if (hi <= lo) return;
+            const uint32_t bytes = (uint32_t)((hi - lo) * D * 2);
+            bulk_g2s(dK + (size_t)(lo - c0) * D, kh + (size_t)slot0 * D, bytes, &full_bar[st]);
+            bulk_g2s(dV + (size_t)(lo - c0) * D, vh + (size_t)slot0 * D, bytes, &full_bar[st]);
+          };
+          auto ring_run = [&](int r_lo, int r_hi, int base_slot, int head, int size) {
+            const int lo = max(r_lo, c0), hi = min(r_hi, c1);
+            if (hi <= lo) return;
+            const int p0 = (head + (lo - r_lo)) % size;
+            const int n1 = min(hi - lo, size - p0);
+            run(lo, lo + n1, base_slot + p0);
+            run(lo + n1, hi, base_slot);
+          };
+          run(c0, min(rS, c1), c0);
+          if (s > 0) ring_run(rS, rV, a, pl.sk0, s);
+          for (int k = max(rV, c0); k < min(rW, c1); ++k) run(k, k + 1, surv_src[k - rV]);
+          ring_run(rW, rN, a + s, pl.pw0, ring);
+          if (c0 <= rN && rN < c1) {
+            bulk_g2s(dK + (size_t)(rN - c0) * D, k_new + new_off, D * 2, &full_bar[st]);
+            bulk_g2s(dV + (size_t)(rN - c0) * D, v_new + new_off, D * 2, &full_bar[st]);
+          }
+        }
+      }
+    } else {
+      // ------------------------------------------------------------ consumers
+      // Rotated queries of the G heads at position N-1, stored so that the
+      // LPE lanes scoring one entry read 16 consecutive bytes each, lane
+      // after lane (no bank conflicts): sQ[h][j][l][4] holds, for lane l,
+      // q[8l + 4j .. +4) (j = 0, 1) and q[HALF + 8l + 4(j-2) .. +4) (j = 2, 3).
+      if (ok) {
+        const float2* cs_row = cp.rope + (size_t)(N - 1) * HALF;
+        for (int e = tid; e < G * HALF; e += kConsumerWarps * 32) {
+          const int hh = e / HALF, i = e % HALF;
+          const uint16_t* qr = q + (((size_t)sq * args.Hq) + g * G + hh) * D;
+          const float2 cs = cs_row[i];
+          const float x1 = __uint_as_float((uint32_t)qr[i] << 16);
+          const float x2 = __uint_as_float((uint32_t)qr[i + HALF] << 16);
+          const int l = i / 8, j = (i % 8) / 4, x = i % 4;
+          float* qh = sQ + hh * D + l * 4 + x;
+          qh[j * (4 * LPE)] = x1 * cs.x - x2 * cs.y;
+          qh[(j + 2) * (4 * LPE)] = x2 * cs.x + x1 * cs.y;
+        }
+      }
+      consumer_sync();
+      constexpr int HPL = G > LPE ? G / LPE : 1;  // heads a lane keeps after the reduce-scatter
+      const int sub = lane / LPE, l8 = lane % LPE;
+      const int i0 = 8 * l8;  // this lane's first frequency index when scoring
+      const int e_w = warp * EPW + sub;  // entry of this lane within a chunk
+      float* sPw = sPx + warp * (EPW * G + G);  // this warp's p[EPW][G], then alpha[G]
+      // heads this lane holds after the reduce-scatter, and whether it is
+      // the lowest lane of its entry holding them (it publishes p)
+      int hbase = 0;
+      {
+        int cur = G, off = LPE / 2;
+        for (; off > 0 && cur > 1; off >>= 1) {
+          cur >>= 1;
+          if (l8 & off) hbase += cur;
+        }
+      }
+      const int plain_mask = (G >= LPE) ? 0 : (LPE / G) - 1;  // lanes repeating a head
+      const bool publisher = (l8 & plain_mask) == 0;
+      // (cos, sin) of the lane's 8 frequencies at its first position, and the
+      // rotation by CH positions that advances it chunk to chunk
       float cz[8], sz[8], cst[8], sst[8];
       {
-        const float2* r0 = cp.rope + (size_t)min(k0 + e_first, c - 1) * HALF + i0;
-        const float2* rs = cp.rope + (size_t)STRIDE * HALF + i0;
+        const float2* r0 = cp.rope + (size_t)min(k0 + e_w, c - 1) * HALF + i0;
+        const float2* rs = cp.rope + (size_t)CH * HALF + i0;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const float2 t0 = r0[j], ts = rs[j];
           cz[j] = t0.x; sz[j] = t0.y; cst[j] = ts.x; sst[j] = ts.y;
         }
       }
-      for (int eb = 0; eb < ne; eb += STRIDE) {
-        const int e = eb + e_first;
-        const bool live = e < ne;
-        float lo[8], hi[8];
-        const uint16_t* row = sK + (size_t)(live ? e : 0) * D;
-        bf16x8_to_f32(*reinterpret_cast<const uint4*>(row + i0), lo);
-        bf16x8_to_f32(*reinterpret_cast<const uint4*>(row + i0 + HALF), hi);
-        float rl[8], rh[8];
+      // running max (log2 units; moved only when a score exceeds it by more
+      // than kLazyRescale, so p <= 2^kLazyRescale) and sum for the held heads
+      float mrun[HPL], lrun[HPL];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          rl[j] = lo[j] * cz[j] - hi[j] * sz[j];
-          rh[j] = hi[j] * cz[j] + lo[j] * sz[j];
-        }
-#pragma unroll
-        for (int hh = 0; hh < G; ++hh) {
-          const float4* qa = reinterpret_cast<const float4*>(sQ + hh * D + i0);
-          const float4* qb = reinterpret_cast<const float4*>(sQ + hh * D + i0 + HALF);
-          const float4 a0 = qa[0], a1 = qa[1], b0 = qb[0], b1 = qb[1];
-          float acc = rl[0] * a0.x;
-          acc = fmaf(rl[1], a0.y, acc); acc = fmaf(rl[2], a0.z, acc); acc = fmaf(rl[3], a0.w, acc);
-          acc = fmaf(rl[4], a1.x, acc); acc = fmaf(rl[5], a1.y, acc); acc = fmaf(rl[6], a1.z, acc);
-          acc = fmaf(rl[7], a1.w, acc);
-          acc = fmaf(rh[0], b0.x, acc); acc = fmaf(rh[1], b0.y, acc); acc = fmaf(rh[2], b0.z, acc);
-          acc = fmaf(rh[3], b0.w, acc); acc = fmaf(rh[4], b1.x, acc); acc = fmaf(rh[5], b1.y, acc);
-          acc = fmaf(rh[6], b1.z, acc); acc = fmaf(rh[7], b1.w, acc);
-#pragma unroll
-          for (int off = LPE / 2; off > 0; off >>= 1)
-            acc += __shfl_xor_sync(0xffffffffu, acc, off);
-          if (live && l8 == 0) sP[hh * args.emax + e] = acc * args.scale_log2;
-        }
-        // advance the angles by STRIDE positions
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float cn = cz[j] * cst[j] - sz[j] * sst[j];
-          const float sn = sz[j] * cst[j] + cz[j] * sst[j];
-          cz[j] = cn;
-          sz[j] = sn;
-        }
+      for (int x = 0; x < HPL; ++x) {
+        mrun[x] = -INFINITY;
+        lrun[x] = 0.f;
       }
-    }
-    __syncthreads();
-    // ---- local softmax statistics, one warp per head
-    for (int hh = warp; hh < G; hh += kWarps) {
-      float* sc = sP + hh * args.emax;
-      float mx = -INFINITY;
-      if (att_ok)
-        for (int e = lane; e < ne; e += 32) mx = fmaxf(mx, sc[e]);
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-      float sum = 0.f;
-      if (att_ok)
-        for (int e = lane; e < ne; e += 32) {
-          const float p = exp2f(sc[e] - mx);
-          sc[e] = p;
-          sum += p;
-        }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-      if (lane == 0) {
-        sM[hh] = mx;
-        sL[hh] = sum;
-      }
-    }
-    __syncthreads();
-    // ---- P V: thread = (entry slice, 16-byte chunk of the row)
-    if (!mbar_wait(&bar_v, 0, status)) att_ok = false;
-    att_ok = __syncthreads_and(att_ok);
-    {
-      const int ch = tid % CPR, sl = tid / CPR;
-      float acc[G][8];
+      float acc[G][DPL];
 #pragma unroll
       for (int hh = 0; hh < G; ++hh)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[hh][j] = 0.f;
-      if (att_ok) {
-#pragma unroll 4
-        for (int e = sl; e < ne; e += NSLICE) {
-          float x[8];
-          bf16x8_to_f32(*reinterpret_cast<const uint4*>(sV + (size_t)e * D + 8 * ch), x);
+        for (int x = 0; x < DPL; ++x) acc[hh][x] = 0.f;
+      for (int ch = 0; ch < n_chunks; ++ch) {
+        const int st = ch % NST;
+        if (!mbar_wait(&full_bar[st], (ch / NST) & 1, status)) {
+          att_ok = false;
+          break;
+        }
+        const uint16_t* sK = reinterpret_cast<const uint16_t*>(dsm + L.ring + st * SS::STAGE);
+        const uint16_t* sV = sK + CH * D;
+        const bool live = ch * CH + e_w < ne;
+        // ---- partial dot products of the rotated key with the G queries
+        float part[G];
+        {
+          float lo[8], hi[8];
+          const uint16_t* row = sK + (size_t)(live ? e_w : 0) * D;
+          bf16x8_to_f32(*reinterpret_cast<const uint4*>(row + i0), lo);
+          bf16x8_to_f32(*reinterpret_cast<const uint4*>(row + i0 + HALF), hi);
+          float rl[8], rh[8];
+#pragma unroll
+          for (int j = 0; j < 8; j += 2) {
+            float t0, t1;
+            fmul2(t0, t1, hi[j], hi[j + 1], sz[j], sz[j + 1]);
+            ffma2(rl[j], rl[j + 1], lo[j], lo[j + 1], cz[j], cz[j + 1], -t0, -t1);
+            fmul2(t0, t1, lo[j], lo[j + 1], sz[j], sz[j + 1]);
+            ffma2(rh[j], rh[j + 1], hi[j], hi[j + 1], cz[j], cz[j + 1], t0, t1);
+          }
 #pragma unroll
           for (int hh = 0; hh < G; ++hh) {
-            const float p = sP[hh * args.emax + e];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) acc[hh][j] = fmaf(p, x[j], acc[hh][j]);
+            const float4* qv = reinterpret_cast<const float4*>(sQ + hh * D + l8 * 4);
+            const float4 a0 = qv[0], a1 = qv[LPE], b0 = qv[2 * LPE], b1 = qv[3 * LPE];
+            float u0, u1;
+            fmul2(u0, u1, rl[0], rl[1], a0.x, a0.y);
+            ffma2(u0, u1, rl[2], rl[3], a0.z, a0.w, u0, u1);
+            ffma2(u0, u1, rl[4], rl[5], a1.x, a1.y, u0, u1);
+            ffma2(u0, u1, rl[6], rl[7], a1.z, a1.w, u0, u1);
+            ffma2(u0, u1, rh[0], rh[1], b0.x, b0.y, u0, u1);
+            ffma2(u0, u1, rh[2], rh[3], b0.z, b0.w, u0, u1);
+            ffma2(u0, u1, rh[4], rh[5], b1.x, b1.y, u0, u1);
+            ffma2(u0, u1, rh[6], rh[7], b1.z, b1.w, u0, u1);
+            part[hh] = u0 + u1;
           }
         }
-      }
-      // slices inside a warp, then across warps through shared memory
+        // ---- reduce-scatter over the entry's LPE lanes: each lane ends up
+        // with the full scores of HPL heads (hbase ..)
+        float sc[HPL];
+        {
+          float cur[G];
 #pragma unroll
-      for (int hh = 0; hh < G; ++hh)
+          for (int hh = 0; hh < G; ++hh) cur[hh] = part[hh];
+          int n = G;
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
+          for (int off = LPE / 2; off > 0; off >>= 1) {
+            if (n > HPL) {
+              const int half = n / 2;
+              const bool up = (l8 & off) != 0;
 #pragma unroll
-          for (int off = CPR; off < 32; off <<= 1)
-            acc[hh][j] += __shfl_xor_sync(0xffffffffu, acc[hh][j], off);
-      __syncthreads();  // sK (aliased by sRed) is no longer read
-      if (lane < CPR) {
+              for (int x = 0; x < G / 2; ++x) {
+                if (x < half) {
+                  const float send = up ? cur[x] : cur[x + half];
+                  const float keep = up ? cur[x + half] : cur[x];
+                  cur[x] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                }
+              }
+              n = half;
+            } else {
 #pragma unroll
-        for (int hh = 0; hh < G; ++hh) {
-          float4* dst = reinterpret_cast<float4*>(sRed + (warp * G + hh) * D + 8 * ch);
-          dst[0] = make_float4(acc[hh][0], acc[hh][1], acc[hh][2], acc[hh][3]);
-          dst[1] = make_float4(acc[hh][4], acc[hh][5], acc[hh][6], acc[hh][7]);
+              for (int x = 0; x < HPL; ++x) cur[x] += __shfl_xor_sync(0xffffffffu, cur[x], off);
+            }
+          }
+#pragma unroll
+          for (int x = 0; x < HPL; ++x) sc[x] = live ? cur[x] * args.scale_log2 : -INFINITY;
+        }
+        // ---- online softmax over the warp's EPW entries, per held head
+#pragma unroll
+        for (int x = 0; x < HPL; ++x) {
+          float cm = sc[x];
+#pragma unroll
+          for (int off = LPE; off < 32; off <<= 1)
+            cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, off));
+          float alpha = 1.f;
+          if (cm > mrun[x] + kLazyRescale) {  // uniform across the lanes holding the head
+            alpha = mrun[x] == -INFINITY ? 0.f : exp2f(mrun[x] - cm);
+            mrun[x] = cm;
+          }
+          const float pe = live ? exp2f(sc[x] - mrun[x]) : 0.f;
+          float ps = pe;
+#pragma unroll
+          for (int off = LPE; off < 32; off <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+          lrun[x] = lrun[x] * alpha + ps;
+          if (publisher) {
+            sPw[sub * G + hbase + x] = pe;
+            if (sub == 0) sPw[EPW * G + hbase + x] = alpha;
+          }
+        }
+        __syncwarp();
+        // ---- P V: lane owns output dims [DPL*lane, DPL*lane + DPL)
+        {
+          const float* al = sPw + EPW * G;
+          bool rescale = false;
+#pragma unroll
+          for (int hh = 0; hh < G; ++hh) rescale |= al[hh] != 1.f;
+          if (rescale) {
+#pragma unroll
+            for (int hh = 0; hh < G; ++hh) {
+              const float f = al[hh];
+#pragma unroll
+              for (int x = 0; x < DPL; ++x) acc[hh][x] *= f;
+            }
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < EPW; ++e) {
+          if (ch * CH + warp * EPW + e >= ne) break;  // rows past the chunk hold stale data
+          float v[DPL];
+          const uint16_t* vr = sV + (size_t)(warp * EPW + e) * D + DPL * lane;
+          if (DPL == 4) {
+            const uint2 u = *reinterpret_cast<const uint2*>(vr);
+            v[0] = __uint_as_float(u.x << 16);
+            v[1] = __uint_as_float(u.x & 0xffff0000u);
+            v[2] = __uint_as_float(u.y << 16);
+            v[3] = __uint_as_float(u.y & 0xffff0000u);
+          } else {
+            const uint32_t u = *reinterpret_cast<const uint32_t*>(vr);
+            v[0] = __uint_as_float(u << 16);
+            v[1] = __uint_as_float(u & 0xffff0000u);
+          }
+          const float* pr = sPw + e * G;
+#pragma unroll
+          for (int hh = 0; hh < G; ++hh) {
+            const float pe = pr[hh];
+#pragma unroll
+            for (int x = 0; x < DPL; x += 2)
+              ffma2(acc[hh][x], acc[hh][x + 1], pe, pe, v[x], v[x + 1], acc[hh][x], acc[hh][x + 1]);
+          }
+        }
+        __syncwarp();  // p / alpha of this chunk are read before the next chunk rewrites them
+        if (lane == 0) mbar_arrive(&empty_bar[st]);
+        // advance the angles by CH positions
+#pragma unroll
+        for (int j = 0; j < 8; j += 2) {
+          float c0, c1, s0, s1;
+          fmul2(c0, c1, sz[j], sz[j + 1], sst[j], sst[j + 1]);
+          ffma2(c0, c1, cz[j], cz[j + 1], cst[j], cst[j + 1], -c0, -c1);
+          fmul2(s0, s1, cz[j], cz[j + 1], sst[j], sst[j + 1]);
+          ffma2(s0, s1, sz[j], sz[j + 1], cst[j], cst[j + 1], s0, s1);
+          cz[j] = c0; cz[j + 1] = c1; sz[j] = s0; sz[j + 1] = s1;
         }
       }
-      __syncthreads();
-      for (int e = tid; e < G * D; e += kThreads) {
-        float t = 0.f;
+      // merge the four warps' states into this CTA's partial: the lanes
+      // holding a head publish its running max and sum
 #pragma unroll
-        for (int r = 0; r < kWarps; ++r) t += sRed[r * G * D + e];
-        sAcc[e] = t;
+      for (int hh = 0; hh < G; ++hh) {
+        float* ws = sW + (warp * G + hh) * (D + 2);
+#pragma unroll
+        for (int x = 0; x < DPL; ++x) ws[DPL * lane + x] = acc[hh][x];
+      }
+      if (sub == 0 && publisher) {
+#pragma unroll
+        for (int x = 0; x < HPL; ++x) {
+          float* ws = sW + (warp * G + hbase + x) * (D + 2);
+          ws[D] = mrun[x];
+          ws[D + 1] = lrun[x];
+        }
+      }
+      consumer_sync();
+      for (int e = tid; e < G * D; e += kConsumerWarps * 32) {
+        const int hh = e / D, x = e % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int r = 0; r < kConsumerWarps; ++r) M = fmaxf(M, sW[(r * G + hh) * (D + 2) + D]);
+        float num = 0.f, den = 0.f;
+#pragma unroll
+        for (int r = 0; r < kConsumerWarps; ++r) {
+          const float* ws = sW + (r * G + hh) * (D + 2);
+          if (ws[D] != -INFINITY) {
+            const float f = exp2f(ws[D] - M);
+            num = fmaf(f, ws[x], num);
+            den = fmaf(f, ws[D + 1], den);
+          }
+        }
+        sAcc[e] = num;
+        if (x == 0) {
+          sM[hh] = M;
+          sL[hh] = den;
+        }
       }
     }
+    att_ok = __syncthreads_and(att_ok || warp == kConsumerWarps);
   }
 
-  // ---- merge the cluster's partial states, then (CTA 0) write the update
+  // ---- merge the cluster's partial states (each CTA a slice of the outputs),
+  // then CTA 0 writes the update once every CTA has finished reading
   cluster_arrive();
   cluster_wait();
-  // every CTA merges its own slice of the G*D outputs from all partials
   if (attend && att_ok) {
     const int per = (G * D + split - 1) / split;
     const int e_lo = rank * per, e_hi = min(G * D, e_lo + per);
@@ -560,7 +702,6 @@ __global__ void __launch_bounds__(kThreads)
     } else {
       // the update: surviving separators into the separator ring, then the
       // new token (its slot may be one a survivor was read from)
-      const size_t head_off = mh * (size_t)NSL * D;
       uint16_t* kh = cp.k + head_off;
       uint16_t* vh = cp.v + head_off;
       uint8_t* sepw = cp.issep + mh * NSL;
@@ -614,7 +755,7 @@ template <int D, int G>
 cudaError_t launch_step_t(const CachePtrs& cp, StepArgs args, const void* q, const void* k_new,
                           const void* v_new, const int32_t* ids_new, void* out, int* status,
                           cudaStream_t stream) {
-  const size_t smem = step_smem(D, G, args.emax).total;
+  const size_t smem = step_smem<D, G>(args.s).total;
   if (smem > 48 * 1024) {
     const cudaError_t e = cudaFuncSetAttribute(
         cache_step_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -738,7 +879,6 @@ SEP_API sep_status sep_cache_step(const sep_cache_params* p, void* cache_buf, co
   const CacheLayout l = cache_layout(p);
   args.NSL = l.NSL;
   args.split = q ? pick_split(p->S, p->Hkv, p->c) : 1;
-  args.emax = (p->c + args.split - 1) / args.split + 1;
   if (!(scale > 0.f)) scale = 1.0f / sqrtf(static_cast<float>(p->d));
   args.scale_log2 = scale * 1.4426950408889634f;
   int* status = device_status_ptr();
