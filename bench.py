@@ -238,13 +238,13 @@ def run_ours(args, rank, world, device):
         graph.replay()
     torch.cuda.synchronize()
 
-    kern_names = ["index", "fwd_gather", "fwd_attn", "bwd_gather", "bwd_prep", "bwd_kv_keep",
-                  "bwd_kv_dense", "bwd_dq"]
+    kern_names = ["index", "fwd_gather", "fwd_attn", "bwd_gather", "bwd_prep", "bwd_kv",
+                  "bwd_dq", "bwd_scatter"]
     marks = [step_ev[0], fwd_ev[0], fwd_ev[1], fwd_ev[2], bwd_ev[0], bwd_ev[1], bwd_ev[2],
              bwd_ev[3], bwd_ev[4], bwd_ev[5]]
     # index: step start -> fwd gather; fwd attn end -> bwd gather is launch glue
     spans = {"index": (0, 1), "fwd_gather": (1, 2), "fwd_attn": (2, 3), "bwd_gather": (4, 5),
-             "bwd_prep": (5, 6), "bwd_kv_keep": (6, 7), "bwd_kv_dense": (7, 8), "bwd_dq": (8, 9)}
+             "bwd_prep": (5, 6), "bwd_kv": (6, 7), "bwd_dq": (7, 8), "bwd_scatter": (8, 9)}
     sampler = ClockSampler(device.index if device.index is not None else 0)
     t_step = []
     t_kern = {n: [] for n in kern_names}
@@ -275,16 +275,15 @@ def run_ours(args, rank, world, device):
     mean = lambda xs: sum(xs) / len(xs)  # noqa: E731
     kern_ms = {n: mean(t_kern[n]) for n in kern_names}
     fwd_ms = kern_ms["fwd_gather"] + kern_ms["fwd_attn"]
-    bwd_ms = sum(kern_ms[n] for n in ("bwd_gather", "bwd_prep", "bwd_kv_keep", "bwd_kv_dense",
-                                      "bwd_dq"))
+    bwd_ms = sum(kern_ms[n] for n in ("bwd_gather", "bwd_prep", "bwd_kv", "bwd_dq",
+                                      "bwd_scatter"))
     fwd_tf = fwd_flops / (fwd_ms * 1e-3) / 1e12
     bwd_tf = bwd_flops / (bwd_ms * 1e-3) / 1e12
     # Algorithmic FLOPs of each tensor-core kernel over the visited pairs it
     # owns: attention forward 4d per pair; key-major dK/dV 8d per pair
     # (S and dP recomputed, dV, dK); query-major dQ 6d per pair (S, dP, dQ).
-    g_pairs, band_pairs = gathered_band_pairs_per_head(ids_np, cfg.a, cfg.n, 128)
-    kern_flops = {"fwd_attn": 4.0 * d * pairs * Hq, "bwd_kv_keep": 8.0 * d * g_pairs * Hq,
-                  "bwd_kv_dense": 8.0 * d * band_pairs * Hq, "bwd_dq": 6.0 * d * pairs * Hq}
+    kern_flops = {"fwd_attn": 4.0 * d * pairs * Hq, "bwd_kv": 8.0 * d * pairs * Hq,
+                  "bwd_dq": 6.0 * d * pairs * Hq}
     dom = max(kern_flops, key=lambda n: kern_ms[n])
     dom_tf = kern_flops[dom] / (kern_ms[dom] * 1e-3) / 1e12
     kernels = {n: {"ms": round(kern_ms[n], 5)} for n in kern_names}

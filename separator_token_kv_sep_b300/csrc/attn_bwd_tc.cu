@@ -57,8 +57,118 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
                : "memory");
 }
 
-// Named barrier among the 128 elementwise threads (warps 2-5).
-__device__ __forceinline__ void ew_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
+// Work schedule of the key-major pass.  An item is one 128-key tile and a
+// range of query tiles [t0, t1), walked for every q head of its kv group:
+//   KEEP   keys are gathered keep tokens [row0, row0+128) of K_keep/V_keep;
+//          query tile t sees keep token k iff k < n_gather(t).  A keep tile's
+//          query tiles are cut into chunks of kKeepChunk tiles.
+//   DENSE  keys are positions [row0, row0+128) of K/V; the query tiles are
+//          those whose dense band reaches the tile, element mask as in the
+//          forward.
+// Items are written by the last CTA of the prep kernel: keep items first
+// (they are the longest), then dense items.  Persistent CTAs take items
+// round-robin.
+// ---------------------------------------------------------------------------
+constexpr int kItemKeep = 0, kItemDense = 1;
+
+struct BwdSchedule {  // header of the schedule region; int4 items follow
+  int n_items, n_keep, pad0, pad1;
+};
+
+__host__ __device__ inline size_t bwd_max_items(int B, int Hkv, int T) {
+  const size_t chunks = (size_t)(T + kKeepChunk - 1) / kKeepChunk + 1;
+  return (size_t)B * Hkv * T * (chunks + 1);
+}
+
+// Block-wide exclusive scan of one int per thread (blockDim.x threads,
+// a multiple of 32, at most 1024).  Returns the exclusive prefix; *total
+// receives the sum.  `sh` holds 33 ints.
+__device__ __forceinline__ int block_exclusive_scan(int x, int* sh, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int incl = x;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  if (lane == 31) sh[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int v = lane < nw ? sh[lane] : 0;
+    int vi = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, vi, off);
+      if (lane >= off) vi += y;
+    }
+    sh[lane] = vi - v;
+    if (lane == 31) sh[32] = vi;
+  }
+  __syncthreads();
+  const int r = sh[warp] + incl - x;
+  *total = sh[32];
+  __syncthreads();
+  return r;
+}
+
+// Builds the schedule (one CTA).  blocks[b][t] = {n_gather, dense_lo, dense_hi, flags}.
+__device__ void build_bwd_schedule(IndexPtrs idx, int B, int Hkv, int L, int T,
+                                   BwdSchedule* sched, int4* items) {
+  __shared__ int sh[33];
+  int total = 0;
+  // keep items: (b, keep tile kt) -> chunks of query tiles from t_begin(kt)
+  for (int base = 0; base < B * T; base += blockDim.x) {
+    const int id = base + threadIdx.x;
+    int n = 0, tb = T;
+    if (id < B * T) {
+      const int b = id / T, kt = id % T;
+      const int count = min(max(idx.keep_count[b], 0), L);
+      if (kt * 128 < count) {
+        const int32_t* blk = idx.blocks + (size_t)b * T * 4;
+        int lo = 0, hi = T;  // first t with n_gather(t) > 128 kt
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (blk[4 * mid] > kt * 128) hi = mid; else lo = mid + 1;
+        }
+        tb = lo;
+        n = (T - tb + kKeepChunk - 1) / kKeepChunk;
+      }
+    }
+    int sum;
+    const int ex = block_exclusive_scan(n, sh, &sum);
+    if (n > 0) {
+      const int b = id / T, kt = id % T;
+      for (int cc = 0; cc < n; ++cc) {
+        const int t0 = tb + cc * kKeepChunk, t1 = min(T, t0 + kKeepChunk);
+        for (int g = 0; g < Hkv; ++g)
+          items[total + (size_t)(ex + cc) * Hkv + g] =
+              make_int4(kItemKeep, b * Hkv + g, kt * 128, (t0 << 16) | t1);
+      }
+    }
+    total += sum * Hkv;
+  }
+  const int n_keep = total;
+  // dense items: (b, key tile jt) -> query tiles jt .. (last whose band starts
+  // before the tile ends)
+  for (int id = threadIdx.x; id < B * T; id += blockDim.x) {
+    const int b = id / T, jt = id % T;
+    const int32_t* blk = idx.blocks + (size_t)b * T * 4;
+    int lo = jt, hi = T;  // first t >= jt with dense_lo(t) >= 128 jt + 128
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (blk[4 * mid + 1] < jt * 128 + 128) lo = mid + 1; else hi = mid;
+    }
+    for (int g = 0; g < Hkv; ++g)
+      items[n_keep + (size_t)id * Hkv + g] =
+          make_int4(kItemDense, b * Hkv + g, jt * 128, (jt << 16) | max(lo, jt + 1));
+  }
+  if (threadIdx.x == 0) {
+    sched->n_items = n_keep + B * T * Hkv;
+    sched->n_keep = n_keep;
+  }
+}
 
 // ---------------------------------------------------------------------------
 // Prep: Delta = rowsum(dO o O) in fp32, and zeroed keep-token accumulators.
@@ -78,25 +188,39 @@ __host__ __device__ constexpr int prep_rows_per_block() {
 template <int D>
 __global__ void __launch_bounds__(kPrepThreads)
     bwd_prep_kernel(IndexPtrs idx, const uint4* __restrict__ o, const uint4* __restrict__ dout,
-                    float* __restrict__ delta, float4* __restrict__ dk_keep,
+                    const float* __restrict__ lse, float2* __restrict__ stats,
+                    float4* __restrict__ dk_keep,
                     float4* __restrict__ dv_keep, int B, int Hq, int Hkv, int L,
-                    int delta_blocks) {
+                    int delta_blocks, BwdSchedule* __restrict__ sched,
+                    int4* __restrict__ items) {
   constexpr int U = D / 8;         // 16-byte units per row
   constexpr int RPI = 32 / U;      // rows per warp instruction
   constexpr int IT = kPrepRows / RPI;
   const IndexHeader hdr = *idx.header;
   if (hdr.magic != kIndexMagic || hdr.B != B || hdr.L != L) return;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (blockIdx.x == gridDim.x - 1) {  // the last block writes the dK/dV work schedule
+    build_bwd_schedule(idx, B, Hkv, L, (L + 127) / 128, sched, items);
+    return;
+  }
   if (static_cast<int>(blockIdx.x) < delta_blocks) {
-    const size_t R = (size_t)B * Hq * L;
+    // rows of the padded [B*Hq][T*128] stats space; rows past L get (0, 0)
+    const int LP = (L + 127) / 128 * 128;
+    const size_t R = (size_t)B * Hq * LP;
     const size_t row0 = ((size_t)blockIdx.x * (kPrepThreads / 32) + warp) * kPrepRows;
     const int sub = lane / U, u = lane % U;
     uint4 xo[IT], xd[IT];
+    size_t src[IT];
+    bool live[IT];
 #pragma unroll
     for (int it = 0; it < IT; ++it) {
       const size_t row = row0 + it * RPI + sub;
-      xo[it] = row < R ? o[row * U + u] : make_uint4(0, 0, 0, 0);
-      xd[it] = row < R ? dout[row * U + u] : make_uint4(0, 0, 0, 0);
+      const size_t plane = row / LP;
+      const int i = static_cast<int>(row % LP);
+      live[it] = row < R && i < L;
+      src[it] = plane * L + i;
+      xo[it] = live[it] ? o[src[it] * U + u] : make_uint4(0, 0, 0, 0);
+      xd[it] = live[it] ? dout[src[it] * U + u] : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int it = 0; it < IT; ++it) {
@@ -112,7 +236,8 @@ __global__ void __launch_bounds__(kPrepThreads)
 #pragma unroll
       for (int off = U / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
       const size_t row = row0 + it * RPI + sub;
-      if (u == 0 && row < R) delta[row] = acc;
+      if (u == 0 && row < R)
+        stats[row] = live[it] ? make_float2(lse[src[it]] * kLog2e, acc) : make_float2(0.f, 0.f);
     }
     return;
   }
@@ -170,117 +295,85 @@ __global__ void __launch_bounds__(256)
 }
 
 // ---------------------------------------------------------------------------
-// Key-major dK / dV
+// Key-major dK / dV, persistent
 // ---------------------------------------------------------------------------
-template <int D, int NST>
+template <int D>
 struct KvCfg {
   static constexpr int DCH = D / 64;
   static constexpr int TILE = DCH * kChunk;
-  static constexpr int OFF_K = 0;
-  static constexpr int OFF_V = TILE;
-  static constexpr int OFF_Q = 2 * TILE;
+  static constexpr int KVB = D == 64 ? 2 : 1;   // K/V tile buffers
+  static constexpr int NST = D == 64 ? 2 : 1;   // Q/dO ring stages
+  static constexpr int ACB = D == 64 ? 2 : 1;   // dK/dV accumulator buffers in TMEM
+  static constexpr int OFF_KV = 0;              // [KVB][K, V]
+  static constexpr int OFF_Q = OFF_KV + KVB * 2 * TILE;
   static constexpr int OFF_DO = OFF_Q + NST * TILE;
   static constexpr int OFF_P = OFF_DO + NST * TILE;
   static constexpr int OFF_DS = OFF_P + 2 * kChunk;
-  static constexpr int OFF_STAT = OFF_DS + 2 * kChunk;  // [2][2][128] floats
-  static constexpr int SMEM = OFF_STAT + 2 * 2 * 128 * 4 + 1024;
-  static constexpr int TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 256 + D;
+  static constexpr int OFF_STAT = OFF_DS + 2 * kChunk;  // [NST][128] (LSE log2, Delta)
+  static constexpr int SMEM = OFF_STAT + NST * 128 * 8 + 1024;
+  static constexpr int TM_S = 0, TM_DP = 128, TM_ACC = 256;  // acc b: dV at +2bD, dK at +2bD+D
   static constexpr int TM_COLS = 512;
   static_assert(SMEM <= 227 * 1024, "shared memory");
+  static_assert(TM_ACC + ACB * 2 * D <= TM_COLS, "tensor memory");
 };
 
-template <int D, bool KEEP, int NST>
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-    bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_kx,
-                  const __grid_constant__ CUtensorMap tm_vx,
-                  const __grid_constant__ CUtensorMap tm_q,
-                  const __grid_constant__ CUtensorMap tm_do, IndexPtrs idx,
-                  const float* __restrict__ lse, const float* __restrict__ delta,
-                  float* __restrict__ dk_keep, float* __restrict__ dv_keep,
-                  __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int B, int Hq,
-                  int Hkv, int L, float scale, float scale_log2, int* status) {
-  using C = KvCfg<D, NST>;
+    bwd_kv_persistent(const __grid_constant__ CUtensorMap tm_kk,
+                      const __grid_constant__ CUtensorMap tm_vk,
+                      const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_do, IndexPtrs idx,
+                      const BwdSchedule* __restrict__ sched, const int4* __restrict__ items,
+                      const float2* __restrict__ stats,
+                      float* __restrict__ dk_keep, float* __restrict__ dv_keep,
+                      __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int B,
+                      int Hq, int Hkv, int L, float scale, float scale_log2, int* status) {
+  using C = KvCfg<D>;
+  constexpr int KVB = C::KVB, NST = C::NST, ACB = C::ACB;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  __shared__ __align__(8) uint64_t kv_full, sd_full, sd_free, ps_full, pd_done, mma_final;
-  __shared__ __align__(8) uint64_t qd_full[NST], qd_empty[NST];
+  __shared__ __align__(8) uint64_t kv_full[KVB], kv_empty[KVB], qd_full[NST], qd_empty[NST];
+  __shared__ __align__(8) uint64_t sd_full, sd_free, ps_full, pd_done, acc_full[ACB],
+      acc_empty[ACB], mma_final;
   __shared__ uint32_t tmem_slot;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = (L + 127) >> 7;
   const int G = Hq / Hkv;
-  // DENSE: one key tile per CTA (longest first).  KEEP: one keep tile and one
-  // chunk of kKeepChunk query tiles per CTA, so a keep tile's many query
-  // tiles spread over several CTAs (their partial sums meet in the fp32 keep
-  // accumulators).
-  const int n_qc = (T + kKeepChunk - 1) / kKeepChunk;
-  const int tile = KEEP ? static_cast<int>(blockIdx.x) / n_qc
-                        : T - 1 - static_cast<int>(blockIdx.x);
-  const int qc = KEEP ? static_cast<int>(blockIdx.x) % n_qc : 0;
-  const int b = blockIdx.z;
-  // KEEP: blockIdx.y is the q head; DENSE: the kv head
-  const int g = KEEP ? static_cast<int>(blockIdx.y) / G : static_cast<int>(blockIdx.y);
-  const int h_fixed = KEEP ? static_cast<int>(blockIdx.y) : -1;
 
   const IndexHeader hdr = *idx.header;
   if (hdr.magic != kIndexMagic || hdr.B != B || hdr.L != L || hdr.block_m != 128) {
     if (threadIdx.x == 0) report(status, SEP_ERR_DEVICE_BOUNDS);
     return;
   }
-  const int32_t* blocks = idx.blocks + (size_t)b * T * 4;
-  const int count = idx.keep_count[b];
-  if (count < 0 || count > L) {
+  const int n_items = sched->n_items;
+  if (n_items < 0 || (size_t)n_items > bwd_max_items(B, Hkv, T)) {
     if (threadIdx.x == 0) report(status, SEP_ERR_DEVICE_BOUNDS);
     return;
   }
-  const int j0 = tile * 128;  // first key (KEEP: first keep index) of the tile
-  int t_begin, n_t;
-  if (KEEP) {
-    if (j0 >= count) return;
-    // first query tile whose gathered list reaches past j0 (n_gather is
-    // non-decreasing in t)
-    int lo_t = 0, hi_t = T;
-    while (lo_t < hi_t) {
-      const int mid = (lo_t + hi_t) >> 1;
-      if (blocks[4 * mid] > j0) hi_t = mid; else lo_t = mid + 1;
-    }
-    t_begin = max(lo_t, qc * kKeepChunk);
-    n_t = min(T, (qc + 1) * kKeepChunk) - t_begin;
-    if (n_t <= 0) return;
-  } else {
-    // query tiles t >= tile whose dense band starts before this key tile ends
-    t_begin = tile;
-    int lo_t = tile, hi_t = T;
-    while (lo_t < hi_t) {
-      const int mid = (lo_t + hi_t) >> 1;
-      if (blocks[4 * mid + 1] < j0 + 128) lo_t = mid + 1; else hi_t = mid;
-    }
-    n_t = lo_t - tile;
-    if (n_t <= 0) return;  // unreachable: tile t = `tile` always covers its own keys
-  }
-  const int nU = KEEP ? n_t : G * n_t;
   const int n_win = hdr.n;
 
-  uint8_t* sK = smem + C::OFF_K;
-  uint8_t* sV = smem + C::OFF_V;
-  uint8_t* sQ = smem + C::OFF_Q;
-  uint8_t* sDO = smem + C::OFF_DO;
-  uint8_t* sP = smem + C::OFF_P;
-  uint8_t* sDS = smem + C::OFF_DS;
-  float* sStat = reinterpret_cast<float*>(smem + C::OFF_STAT);
-
   if (threadIdx.x == 0) {
-    mbar_init(&kv_full, 1);
+    for (int i = 0; i < KVB; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+    }
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(&qd_full[i], 1);
+      mbar_init(&qd_empty[i], 1);
+    }
+    for (int i = 0; i < ACB; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], 128);
+    }
     mbar_init(&sd_full, 1);
     mbar_init(&sd_free, 128);
     mbar_init(&ps_full, 128);
     mbar_init(&pd_done, 1);
     mbar_init(&mma_final, 1);
-    for (int s = 0; s < NST; ++s) {
-      mbar_init(&qd_full[s], 1);
-      mbar_init(&qd_empty[s], 1);
-    }
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -292,98 +385,171 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
-  auto head_of = [&](int u) { return KEEP ? h_fixed : g * G + u / n_t; };
-  auto qtile_of = [&](int u) { return t_begin + (KEEP ? u : u % n_t); };
+  // item decoding shared by every role
+  struct Item {
+    int kind, b, g, row0, t0, nt;
+  };
+  auto item_at = [&](int i) -> Item {
+    const int4 it = items[i];
+    Item r;
+    r.kind = it.x;
+    r.b = it.y / Hkv;
+    r.g = it.y % Hkv;
+    r.row0 = it.z;
+    r.t0 = it.w >> 16;
+    r.nt = (it.w & 0xffff) - r.t0;
+    return r;
+  };
 
   if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      const int plane_kv = b * Hkv + g;
-      mbar_arrive_expect_tx(&kv_full, 2 * C::TILE);
-      for (int c = 0; c < C::DCH; ++c) {
-        tma_load_3d(sK + c * kChunk, &tm_kx, &kv_full, 64 * c, j0, plane_kv);
-        tma_load_3d(sV + c * kChunk, &tm_vx, &kv_full, 64 * c, j0, plane_kv);
-      }
-      int issued = 0;
+      int k = 0, ug = 0, kv_issued = 0;
       bool ok = true;
-      for (int u = 0; u < nU; ++u) {
-        const int st = u % NST;
-        if (u >= NST && !mbar_wait(&qd_empty[st], ((u / NST) - 1) & 1, status)) {
+      for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x, ++k) {
+        const Item it = item_at(i);
+        const int kb = k % KVB;
+        if (k >= KVB && !mbar_wait(&kv_empty[kb], ((k / KVB) - 1) & 1, status)) {
           ok = false;
           break;
         }
-        const int plane_q = b * Hq + head_of(u), row = qtile_of(u) * 128;
-        mbar_arrive_expect_tx(&qd_full[st], 2 * C::TILE);
+        const bool keep = it.kind == kItemKeep;
+        const int plane_kv = it.b * Hkv + it.g;
+        uint8_t* sK = smem + C::OFF_KV + kb * 2 * C::TILE;
+        uint8_t* sV = sK + C::TILE;
+        mbar_arrive_expect_tx(&kv_full[kb], 2 * C::TILE);
         for (int c = 0; c < C::DCH; ++c) {
-          tma_load_3d(sQ + st * C::TILE + c * kChunk, &tm_q, &qd_full[st], 64 * c, row, plane_q);
-          tma_load_3d(sDO + st * C::TILE + c * kChunk, &tm_do, &qd_full[st], 64 * c, row,
-                      plane_q);
+          tma_load_3d(sK + c * kChunk, keep ? &tm_kk : &tm_k, &kv_full[kb], 64 * c, it.row0,
+                      plane_kv);
+          tma_load_3d(sV + c * kChunk, keep ? &tm_vk : &tm_v, &kv_full[kb], 64 * c, it.row0,
+                      plane_kv);
         }
-        issued = u + 1;
+        kv_issued = k + 1;
+        const int nU = G * it.nt;
+        for (int u = 0; u < nU; ++u) {
+          const int st = ug % NST;
+          if (ug >= NST && !mbar_wait(&qd_empty[st], ((ug / NST) - 1) & 1, status)) {
+            ok = false;
+            break;
+          }
+          ++ug;  // counts issued Q/dO tiles
+          const int h = it.g * G + u / it.nt, t = it.t0 + u % it.nt;
+          const int plane_q = it.b * Hq + h;
+          mbar_arrive_expect_tx(&qd_full[st], 2 * C::TILE + 128 * 8);
+          bulk_g2s(smem + C::OFF_STAT + st * 1024, stats + ((size_t)plane_q * T + t) * 128, 1024,
+                   &qd_full[st]);
+          for (int c = 0; c < C::DCH; ++c) {
+            tma_load_3d(smem + C::OFF_Q + st * C::TILE + c * kChunk, &tm_q, &qd_full[st],
+                        64 * c, t * 128, plane_q);
+            tma_load_3d(smem + C::OFF_DO + st * C::TILE + c * kChunk, &tm_do, &qd_full[st],
+                        64 * c, t * 128, plane_q);
+          }
+        }
       }
       if (!ok) {
-        for (int u = issued - NST; u < issued; ++u)
-          if (u >= 0) mbar_wait(&qd_full[u % NST], (u / NST) & 1, status);
-        mbar_wait(&kv_full, 0, status);
+        // after a failed wait, let the copies still in flight land before
+        // the CTA's shared memory goes away (on the normal path the MMA
+        // thread has consumed every one of them)
+        for (int x = max(0, kv_issued - KVB); x < kv_issued; ++x)
+          mbar_wait(&kv_full[x % KVB], (x / KVB) & 1, status);
+        for (int x = max(0, ug - NST); x < ug; ++x)
+          mbar_wait(&qd_full[x % NST], (x / NST) & 1, status);
       }
     }
   } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_ss = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idesc_acc = idesc_bf16_f32(128, D, false, true);
-      const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV), q_base = smem_u32(sQ),
-                     do_base = smem_u32(sDO), p_base = smem_u32(sP), ds_base = smem_u32(sDS);
-      auto issue_sdp = [&](int u) -> bool {
-        const int st = u % NST;
-        if (!mbar_wait(&qd_full[st], (u / NST) & 1, status)) return false;
+      const uint32_t q_base = smem_u32(smem + C::OFF_Q), do_base = smem_u32(smem + C::OFF_DO),
+                     p_base = smem_u32(smem + C::OFF_P), ds_base = smem_u32(smem + C::OFF_DS);
+      int k = 0, ug = 0;
+      bool ok = true;
+      for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x, ++k) {
+        const Item it = item_at(i);
+        const int kb = k % KVB, ab = k % ACB;
+        const uint32_t k_base = smem_u32(smem + C::OFF_KV + kb * 2 * C::TILE);
+        const uint32_t v_base = k_base + C::TILE;
+        const uint32_t tm_dv = tmem + C::TM_ACC + ab * 2 * D, tm_dk = tm_dv + D;
+        if (!mbar_wait(&kv_full[kb], (k / KVB) & 1, status)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
+        const int nU = G * it.nt;
+        auto issue_sdp = [&](int ugl) -> bool {  // S^T and dP^T of global iteration ugl
+          const int st = ugl % NST;
+          if (!mbar_wait(&qd_full[st], (ugl / NST) & 1, status)) return false;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
-          umma_bf16_ss(tmem + C::TM_S, sdesc_sw128(k_base + off, 16, 1024),
-                       sdesc_sw128(q_base + st * C::TILE + off, 16, 1024), idesc_ss, kk > 0);
-        }
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
+            umma_bf16_ss(tmem + C::TM_S, sdesc_sw128(k_base + off, 16, 1024),
+                         sdesc_sw128(q_base + st * C::TILE + off, 16, 1024), idesc_ss, kk > 0);
+          }
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
-          umma_bf16_ss(tmem + C::TM_DP, sdesc_sw128(v_base + off, 16, 1024),
-                       sdesc_sw128(do_base + st * C::TILE + off, 16, 1024), idesc_ss, kk > 0);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
+            umma_bf16_ss(tmem + C::TM_DP, sdesc_sw128(v_base + off, 16, 1024),
+                         sdesc_sw128(do_base + st * C::TILE + off, 16, 1024), idesc_ss, kk > 0);
+          }
+          umma_commit(&sd_full);
+          return true;
+        };
+        // S^T / dP^T of the item's first iteration (TMEM S/dP freed by the
+        // elementwise warps of the previous iteration)
+        if (ug > 0 && !mbar_wait(&sd_free, (ug - 1) & 1, status)) {
+          ok = false;
+          break;
         }
-        umma_commit(&sd_full);
-        return true;
-      };
-      auto issue_acc = [&](int u) -> bool {
-        const int st = u % NST;
-        if (!mbar_wait(&ps_full, u & 1, status)) return false;
+        if (!issue_sdp(ug)) {
+          ok = false;
+          break;
+        }
+        // the accumulators of buffer ab must have been drained by the epilogue
+        if (k >= ACB && !mbar_wait(&acc_empty[ab], ((k / ACB) - 1) & 1, status)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
+        for (int u = 0; ok && u < nU; ++u) {
+          const int ugl = ug + u;
+          // S^T / dP^T of the next iteration go ahead of this iteration's
+          // dV / dK when the Q/dO ring has a second stage; with one stage the
+          // next tile only arrives once this iteration's MMAs release it.
+          if (NST > 1 && u + 1 < nU) {
+            ok = mbar_wait(&sd_free, ugl & 1, status) && issue_sdp(ugl + 1);
+            if (!ok) break;
+          }
+          if (!mbar_wait(&ps_full, ugl & 1, status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int st = ugl % NST;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t aoff = (kk >> 2) * kChunk + (kk & 3) * 32;
-          const uint32_t boff = st * C::TILE + kk * 2048;
-          const uint32_t acc = (u > 0 || kk > 0) ? 1u : 0u;
-          umma_bf16_ss(tmem + C::TM_DV, sdesc_sw128(p_base + aoff, 16, 1024),
-                       sdesc_sw128(do_base + boff, kChunk, 1024), idesc_acc, acc);
-          umma_bf16_ss(tmem + C::TM_DK, sdesc_sw128(ds_base + aoff, 16, 1024),
-                       sdesc_sw128(q_base + boff, kChunk, 1024), idesc_acc, acc);
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t aoff = (kk >> 2) * kChunk + (kk & 3) * 32;
+            const uint32_t boff = st * C::TILE + kk * 2048;
+            const uint32_t acc = (u > 0 || kk > 0) ? 1u : 0u;
+            umma_bf16_ss(tm_dv, sdesc_sw128(p_base + aoff, 16, 1024),
+                         sdesc_sw128(do_base + boff, kChunk, 1024), idesc_acc, acc);
+            umma_bf16_ss(tm_dk, sdesc_sw128(ds_base + aoff, 16, 1024),
+                         sdesc_sw128(q_base + boff, kChunk, 1024), idesc_acc, acc);
+          }
+          umma_commit(&pd_done);
+          umma_commit(&qd_empty[st]);
+          if (NST == 1 && u + 1 < nU) {
+            ok = mbar_wait(&sd_free, ugl & 1, status) && issue_sdp(ugl + 1);
+            if (!ok) break;
+          }
         }
-        umma_commit(&pd_done);
-        umma_commit(&qd_empty[st]);
-        return true;
-      };
-      auto next_sdp = [&](int u) -> bool {  // S^T / dP^T of tile u+1
-        if (u + 1 >= nU) return true;
-        if (!mbar_wait(&sd_free, u & 1, status)) return false;
-        return issue_sdp(u + 1);
-      };
-      bool ok = mbar_wait(&kv_full, 0, status);
-      tc_fence_after();
-      if (ok) ok = issue_sdp(0);
-      for (int u = 0; ok && u < nU; ++u) {
-        // With one Q/dO stage, tile u+1 cannot be loaded before dV/dK of tile
-        // u release the stage, so the order flips.
-        if (NST > 1) ok = next_sdp(u);
-        if (ok) ok = issue_acc(u);
-        if (ok && NST == 1) ok = next_sdp(u);
+        if (!ok) break;
+        umma_commit(&kv_empty[kb]);  // every MMA reading this item's K and V is issued
+        umma_commit(&acc_full[ab]);
+        ug += nU;
       }
+      // every MMA issued by this thread completes before TMEM is released
       umma_commit(&mma_final);
       mbar_wait(&mma_final, 0, status);
     }
@@ -394,150 +560,145 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = quad * 32 + lane;   // key row of the tile
     const int ew = threadIdx.x - 64;  // 0..127
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-    const int j = j0 + r;  // KEEP: keep index; DENSE: key position
-    bool keep_j = false;
-    if (!KEEP && j < L)
-      keep_j = (idx.keep_bits[(size_t)b * hdr.nwords + (j >> 5)] >> (j & 31)) & 1u;
+    uint8_t* sP = smem + C::OFF_P;
+    uint8_t* sDS = smem + C::OFF_DS;
+    int k = 0, ug = 0;
     bool ok = true;
-    for (int u = 0; u < nU; ++u) {
-      const int h = head_of(u), t = qtile_of(u);
-      const int i0 = t * 128;
-      // stage this query tile's LSE (log2 units) and Delta for all 128 columns
-      {
-        float* st = sStat + (u & 1) * 256;
-        const int i = i0 + ew;
-        const size_t ri = ((size_t)b * Hq + h) * L + i;
-        st[ew] = i < L ? lse[ri] * kLog2e : 0.f;
-        st[128 + ew] = i < L ? delta[ri] : 0.f;
-      }
-      ew_sync();
-      const float* sl = sStat + (u & 1) * 256;
-      const float* sd = sl + 128;
-      // visible columns of this row as 4 words
-      uint32_t vm[4];
-      const int4 blk = *reinterpret_cast<const int4*>(blocks + 4 * t);
-      const int c_end = min(128, L - i0);  // query rows past L are padding
-      if (KEEP) {
-        const bool row_ok = j < blk.x;  // gathered by this query tile
+    for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x, ++k) {
+      const Item it = item_at(i);
+      const bool keep = it.kind == kItemKeep;
+      const int ab = k % ACB;
+      const int count = min(max(idx.keep_count[it.b], 0), L);
+      const int32_t* blocks = idx.blocks + (size_t)it.b * T * 4;
+      const int j = it.row0 + r;  // KEEP: keep index; DENSE: key position
+      bool keep_j = false;
+      if (!keep && j < L)
+        keep_j = (idx.keep_bits[(size_t)it.b * hdr.nwords + (j >> 5)] >> (j & 31)) & 1u;
+      const int nU = G * it.nt;
+      for (int u = 0; u < nU; ++u) {
+        const int ugl = ug + u;
+        const int h = it.g * G + u / it.nt, t = it.t0 + u % it.nt;
+        const int i0 = t * 128;
+        (void)h;
+        uint32_t vm[4];
+        const int4 blk = *reinterpret_cast<const int4*>(blocks + 4 * t);
+        const int c_end = min(128, L - i0);  // query rows past L are padding
+        if (keep) {
+          const bool row_ok = j < blk.x && j < count;  // gathered by this query tile
 #pragma unroll
-        for (int w = 0; w < 4; ++w) vm[w] = row_ok ? range_bits(0, c_end, w) : 0u;
-      } else {
-        const bool in_band = j >= blk.y && j < blk.z && j < L;
-        // columns i with i >= j, and i <= j + n - 1 unless j is a keep token
-        const int c_lo = j - i0;
-        const int c_hi = keep_j ? c_end : min(c_end, j + n_win - i0);
+          for (int w = 0; w < 4; ++w) vm[w] = row_ok ? range_bits(0, c_end, w) : 0u;
+        } else {
+          const bool in_band = j >= blk.y && j < blk.z && j < L;
+          const int c_lo = j - i0;
+          const int c_hi = keep_j ? c_end : min(c_end, j + n_win - i0);
 #pragma unroll
-        for (int w = 0; w < 4; ++w) vm[w] = in_band ? range_bits(c_lo, c_hi, w) : 0u;
+          for (int w = 0; w < 4; ++w) vm[w] = in_band ? range_bits(c_lo, c_hi, w) : 0u;
+        }
+        if (!mbar_wait(&sd_full, ugl & 1, status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // the query tile's (LSE log2, Delta) arrived with its Q / dO tiles
+        const int stg = ugl % NST;
+        if (!mbar_wait(&qd_full[stg], (ugl / NST) & 1, status)) {
+          ok = false;
+          break;
+        }
+        const float2* sst = reinterpret_cast<const float2*>(smem + C::OFF_STAT + stg * 1024);
+        uint32_t pk[64], dk2[64];
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t sr[32], dr[32];
+          tmem_ld32(tmem + lane_base + C::TM_S + 32 * cc, sr);
+          tmem_ld32(tmem + lane_base + C::TM_DP + 32 * cc, dr);
+          tmem_ld_wait();
+#pragma unroll
+          for (int x = 0; x < 32; x += 2) {
+            const int c = 32 * cc + x;
+            const bool v0 = (vm[cc] >> x) & 1u, v1 = (vm[cc] >> (x + 1)) & 1u;
+            const float4 st2 = *reinterpret_cast<const float4*>(sst + c);  // columns c, c+1
+            const float p0 = v0 ? fast_exp2(__uint_as_float(sr[x]) * scale_log2 - st2.x) : 0.f;
+            const float p1 =
+                v1 ? fast_exp2(__uint_as_float(sr[x + 1]) * scale_log2 - st2.z) : 0.f;
+            const float d0 = p0 * (__uint_as_float(dr[x]) - st2.y);
+            const float d1 = p1 * (__uint_as_float(dr[x + 1]) - st2.w);
+            pk[c >> 1] = pack_bf16x2(p0, p1);
+            dk2[c >> 1] = pack_bf16x2(d0, d1);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&sd_free);
+        if (ugl > 0 && !mbar_wait(&pd_done, (ugl - 1) & 1, status)) {
+          ok = false;
+          break;
+        }
+#pragma unroll
+        for (int un = 0; un < 16; ++un) {
+          const uint32_t off = (un >> 3) * kChunk + sw128_offset(r, (un & 7) * 8);
+          *reinterpret_cast<uint4*>(sP + off) =
+              make_uint4(pk[4 * un], pk[4 * un + 1], pk[4 * un + 2], pk[4 * un + 3]);
+          *reinterpret_cast<uint4*>(sDS + off) =
+              make_uint4(dk2[4 * un], dk2[4 * un + 1], dk2[4 * un + 2], dk2[4 * un + 3]);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&ps_full);
       }
-      if (!mbar_wait(&sd_full, u & 1, status)) {
+      if (!ok) break;
+      ug += nU;
+      // ---- epilogue of the item: accumulators -> global
+      if (!mbar_wait(&acc_full[ab], (k / ACB) & 1, status)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t pk[64], dk2[64];
+      const uint32_t tm_dv = tmem + C::TM_ACC + ab * 2 * D, tm_dk = tm_dv + D;
+      // KEEP rows and DENSE keep tokens add into the fp32 keep accumulators
+      // (written to dK/dV by the scatter kernel); other DENSE rows are final.
+      const bool to_acc = keep ? (j < count) : (j < L && keep_j);
+      const bool to_out = !keep && j < L && !keep_j;
+      const int kidx = keep ? j : (keep_j ? idx.keep_prefix[(size_t)it.b * (L + 1) + j] : 0);
+      float* dkr = dk_keep + (((size_t)it.b * Hkv + it.g) * L + kidx) * D;
+      float* dvr = dv_keep + (((size_t)it.b * Hkv + it.g) * L + kidx) * D;
+      __nv_bfloat16* dko = dk + (((size_t)it.b * Hkv + it.g) * L + (to_out ? j : 0)) * D;
+      __nv_bfloat16* dvo = dv + (((size_t)it.b * Hkv + it.g) * L + (to_out ? j : 0)) * D;
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t sr[32], dr[32];
-        tmem_ld32(tmem + lane_base + C::TM_S + 32 * cc, sr);
-        tmem_ld32(tmem + lane_base + C::TM_DP + 32 * cc, dr);
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t vb[32], kb[32];
+        tmem_ld32(tm_dv + lane_base + c0, vb);
+        tmem_ld32(tm_dk + lane_base + c0, kb);
         tmem_ld_wait();
+        if (to_acc) {
 #pragma unroll
-        for (int x = 0; x < 32; x += 2) {
-          const int c = 32 * cc + x;
-          const bool v0 = (vm[cc] >> x) & 1u, v1 = (vm[cc] >> (x + 1)) & 1u;
-          const float p0 = v0 ? fast_exp2(__uint_as_float(sr[x]) * scale_log2 - sl[c]) : 0.f;
-          const float p1 =
-              v1 ? fast_exp2(__uint_as_float(sr[x + 1]) * scale_log2 - sl[c + 1]) : 0.f;
-          const float d0 = p0 * (__uint_as_float(dr[x]) - sd[c]);
-          const float d1 = p1 * (__uint_as_float(dr[x + 1]) - sd[c + 1]);
-          pk[c >> 1] = pack_bf16x2(p0, p1);
-          dk2[c >> 1] = pack_bf16x2(d0, d1);
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(&sd_free);
-      if (u > 0 && !mbar_wait(&pd_done, (u - 1) & 1, status)) {
-        ok = false;
-        break;
-      }
-#pragma unroll
-      for (int un = 0; un < 16; ++un) {
-        const uint32_t off = (un >> 3) * kChunk + sw128_offset(r, (un & 7) * 8);
-        *reinterpret_cast<uint4*>(sP + off) =
-            make_uint4(pk[4 * un], pk[4 * un + 1], pk[4 * un + 2], pk[4 * un + 3]);
-        *reinterpret_cast<uint4*>(sDS + off) =
-            make_uint4(dk2[4 * un], dk2[4 * un + 1], dk2[4 * un + 2], dk2[4 * un + 3]);
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&ps_full);
-    }
-    if (ok && mbar_wait(&pd_done, (nU - 1) & 1, status)) {
-      tc_fence_after();
-      uint32_t vb[32], kb[32];
-      if (KEEP) {
-        const bool live = j < count;
-        float* dkr = dk_keep + (((size_t)b * Hkv + g) * L + j) * D;
-        float* dvr = dv_keep + (((size_t)b * Hkv + g) * L + j) * D;
-#pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          tmem_ld32(tmem + lane_base + C::TM_DV + c0, vb);
-          tmem_ld32(tmem + lane_base + C::TM_DK + c0, kb);
-          tmem_ld_wait();
-          if (live) {
-#pragma unroll
-            for (int x = 0; x < 32; x += 4) {
-              red_add_v4(dvr + c0 + x, __uint_as_float(vb[x]), __uint_as_float(vb[x + 1]),
-                         __uint_as_float(vb[x + 2]), __uint_as_float(vb[x + 3]));
-              red_add_v4(dkr + c0 + x, __uint_as_float(kb[x]), __uint_as_float(kb[x + 1]),
-                         __uint_as_float(kb[x + 2]), __uint_as_float(kb[x + 3]));
-            }
+          for (int x = 0; x < 32; x += 4) {
+            red_add_v4(dvr + c0 + x, __uint_as_float(vb[x]), __uint_as_float(vb[x + 1]),
+                       __uint_as_float(vb[x + 2]), __uint_as_float(vb[x + 3]));
+            red_add_v4(dkr + c0 + x, __uint_as_float(kb[x]), __uint_as_float(kb[x + 1]),
+                       __uint_as_float(kb[x + 2]), __uint_as_float(kb[x + 3]));
           }
-        }
-      } else {
-        const bool live = j < L;
-        const int kidx = keep_j ? idx.keep_prefix[(size_t)b * (L + 1) + j] : 0;
-        const float* dkr = dk_keep + (((size_t)b * Hkv + g) * L + kidx) * D;
-        const float* dvr = dv_keep + (((size_t)b * Hkv + g) * L + kidx) * D;
-        __nv_bfloat16* dko = dk + (((size_t)b * Hkv + g) * L + j) * D;
-        __nv_bfloat16* dvo = dv + (((size_t)b * Hkv + g) * L + j) * D;
+        } else if (to_out) {
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          tmem_ld32(tmem + lane_base + C::TM_DV + c0, vb);
-          tmem_ld32(tmem + lane_base + C::TM_DK + c0, kb);
-          tmem_ld_wait();
-          if (live) {
-#pragma unroll
-            for (int x = 0; x < 32; x += 8) {
-              float fv[8], fk[8];
-#pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                fv[e] = __uint_as_float(vb[x + e]);
-                fk[e] = __uint_as_float(kb[x + e]);
-              }
-              if (keep_j) {
-                const float4 a0 = *reinterpret_cast<const float4*>(dvr + c0 + x);
-                const float4 a1 = *reinterpret_cast<const float4*>(dvr + c0 + x + 4);
-                const float4 b0 = *reinterpret_cast<const float4*>(dkr + c0 + x);
-                const float4 b1 = *reinterpret_cast<const float4*>(dkr + c0 + x + 4);
-                fv[0] += a0.x; fv[1] += a0.y; fv[2] += a0.z; fv[3] += a0.w;
-                fv[4] += a1.x; fv[5] += a1.y; fv[6] += a1.z; fv[7] += a1.w;
-                fk[0] += b0.x; fk[1] += b0.y; fk[2] += b0.z; fk[3] += b0.w;
-                fk[4] += b1.x; fk[5] += b1.y; fk[6] += b1.z; fk[7] += b1.w;
-              }
-              uint4 ov, ok4;
-              ov.x = pack_bf16x2(fv[0], fv[1]); ov.y = pack_bf16x2(fv[2], fv[3]);
-              ov.z = pack_bf16x2(fv[4], fv[5]); ov.w = pack_bf16x2(fv[6], fv[7]);
-              ok4.x = pack_bf16x2(fk[0] * scale, fk[1] * scale);
-              ok4.y = pack_bf16x2(fk[2] * scale, fk[3] * scale);
-              ok4.z = pack_bf16x2(fk[4] * scale, fk[5] * scale);
-              ok4.w = pack_bf16x2(fk[6] * scale, fk[7] * scale);
-              *reinterpret_cast<uint4*>(dvo + c0 + x) = ov;
-              *reinterpret_cast<uint4*>(dko + c0 + x) = ok4;
-            }
+          for (int x = 0; x < 32; x += 8) {
+            uint4 ov, ok4;
+            ov.x = pack_bf16x2(__uint_as_float(vb[x]), __uint_as_float(vb[x + 1]));
+            ov.y = pack_bf16x2(__uint_as_float(vb[x + 2]), __uint_as_float(vb[x + 3]));
+            ov.z = pack_bf16x2(__uint_as_float(vb[x + 4]), __uint_as_float(vb[x + 5]));
+            ov.w = pack_bf16x2(__uint_as_float(vb[x + 6]), __uint_as_float(vb[x + 7]));
+            ok4.x = pack_bf16x2(__uint_as_float(kb[x]) * scale, __uint_as_float(kb[x + 1]) * scale);
+            ok4.y = pack_bf16x2(__uint_as_float(kb[x + 2]) * scale,
+                                __uint_as_float(kb[x + 3]) * scale);
+            ok4.z = pack_bf16x2(__uint_as_float(kb[x + 4]) * scale,
+                                __uint_as_float(kb[x + 5]) * scale);
+            ok4.w = pack_bf16x2(__uint_as_float(kb[x + 6]) * scale,
+                                __uint_as_float(kb[x + 7]) * scale);
+            *reinterpret_cast<uint4*>(dvo + c0 + x) = ov;
+            *reinterpret_cast<uint4*>(dko + c0 + x) = ok4;
           }
         }
       }
+      tc_fence_before();
+      mbar_arrive(&acc_empty[ab]);
     }
   }
 
@@ -547,83 +708,106 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, C::TM_COLS);
 }
 
+// dK / dV rows of keep tokens from the fp32 accumulators (dK scaled).
+template <int D>
+__global__ void __launch_bounds__(256)
+    bwd_keep_scatter_kernel(IndexPtrs idx, const float4* __restrict__ dk_keep,
+                            const float4* __restrict__ dv_keep, __nv_bfloat16* __restrict__ dk,
+                            __nv_bfloat16* __restrict__ dv, int B, int Hkv, int L, float scale) {
+  constexpr int U = D / 4;  // float4 per row
+  const IndexHeader hdr = *idx.header;
+  if (hdr.magic != kIndexMagic || hdr.B != B || hdr.L != L) return;
+  const int g = blockIdx.y, b = blockIdx.z;
+  const int count = min(max(idx.keep_count[b], 0), L);
+  const int32_t* kpos = idx.keep_pos + (size_t)b * L;
+  const size_t plane = (size_t)b * Hkv + g;
+  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < count * U; e += gridDim.x * blockDim.x) {
+    const int row = e / U, u = e % U;
+    const int j = kpos[row];
+    if (j < 0 || j >= L) continue;
+    const float4 a = dk_keep[(plane * L + row) * U + u];
+    const float4 c = dv_keep[(plane * L + row) * U + u];
+    uint2 ko, vo;
+    ko.x = pack_bf16x2(a.x * scale, a.y * scale);
+    ko.y = pack_bf16x2(a.z * scale, a.w * scale);
+    vo.x = pack_bf16x2(c.x, c.y);
+    vo.y = pack_bf16x2(c.z, c.w);
+    *reinterpret_cast<uint2*>(dk + (plane * L + j) * D + 4 * u) = ko;
+    *reinterpret_cast<uint2*>(dv + (plane * L + j) * D + 4 * u) = vo;
+  }
+}
+
 // ---------------------------------------------------------------------------
-// Query-major dQ
+// Query-major dQ, persistent: items are (batch, q head, query tile), longest
+// query tiles first, taken round-robin by one CTA per SM.
 // ---------------------------------------------------------------------------
-template <int D, int NST>
+template <int D>
 struct DqCfg {
   static constexpr int DCH = D / 64;
   static constexpr int TILE = DCH * kChunk;
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_DO = TILE;
-  static constexpr int OFF_K = 2 * TILE;
+  static constexpr int QB = D == 64 ? 2 : 1;    // Q/dO tile buffers
+  static constexpr int NST = D == 64 ? 3 : 2;   // K/V ring stages
+  static constexpr int OFF_QD = 0;              // [QB][Q, dO]
+  static constexpr int OFF_K = OFF_QD + QB * 2 * TILE;
   static constexpr int OFF_V = OFF_K + NST * TILE;
   static constexpr int OFF_DS = OFF_V + NST * TILE;
   static constexpr int SMEM = OFF_DS + 2 * kChunk + 1024;
-  static constexpr int TM_S = 0, TM_DP = 128, TM_DQ = 256;
+  static constexpr int TM_S = 0, TM_DP = 128, TM_DQ = 256;  // dQ buffer b at +bD
   static constexpr int TM_COLS = 512;
   static_assert(SMEM <= 227 * 1024, "shared memory");
-  static_assert(NST >= 2, "the next tile's S/dP is issued before this tile's dQ");
+  static_assert(TM_DQ + 2 * D <= TM_COLS, "tensor memory");
 };
 
-template <int D, int NST>
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-    bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
-                  const __grid_constant__ CUtensorMap tm_do,
-                  const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v,
-                  const __grid_constant__ CUtensorMap tm_kk,
-                  const __grid_constant__ CUtensorMap tm_vk, IndexPtrs idx,
-                  const float* __restrict__ lse, const float* __restrict__ delta,
-                  __nv_bfloat16* __restrict__ dq, int B, int Hq, int Hkv, int L, float scale,
-                  float scale_log2, int* status) {
-  using C = DqCfg<D, NST>;
+    bwd_dq_persistent(const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_do,
+                      const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ CUtensorMap tm_kk,
+                      const __grid_constant__ CUtensorMap tm_vk, IndexPtrs idx,
+                      const float2* __restrict__ stats,
+                      __nv_bfloat16* __restrict__ dq, int B, int Hq, int Hkv, int L, float scale,
+                      float scale_log2, int* status) {
+  using C = DqCfg<D>;
+  constexpr int QB = C::QB, NST = C::NST;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  __shared__ __align__(8) uint64_t qd_full, sd_full, sd_free, ds_full, dq_done, mma_final;
-  __shared__ __align__(8) uint64_t kv_full[NST], kv_empty[NST];
+  __shared__ __align__(8) uint64_t qd_full[QB], qd_empty[QB], kv_full[NST], kv_empty[NST];
+  __shared__ __align__(8) uint64_t sd_full, sd_free, ds_full, dq_done, acc_full[2], acc_empty[2],
+      mma_final;
   __shared__ uint32_t tmem_slot;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = (L + 127) >> 7;
-  const int t = T - 1 - static_cast<int>(blockIdx.x);
-  const int h = blockIdx.y, b = blockIdx.z;
-  const int g = h / (Hq / Hkv);
-  const int q0 = t * 128;
+  const int n_items = B * Hq * T;
 
   const IndexHeader hdr = *idx.header;
   if (hdr.magic != kIndexMagic || hdr.B != B || hdr.L != L || hdr.block_m != 128) {
     if (threadIdx.x == 0) report(status, SEP_ERR_DEVICE_BOUNDS);
     return;
   }
-  const int4 blk = *reinterpret_cast<const int4*>(idx.blocks + ((size_t)b * T + t) * 4);
-  const int n_gather = blk.x, lo = blk.y, hi = blk.z;
-  if (n_gather < 0 || n_gather > lo || lo < 0 || lo > q0 || hi <= q0 || hi > L) {
-    if (threadIdx.x == 0) report(status, SEP_ERR_DEVICE_BOUNDS);
-    return;
-  }
-  const int nG = (n_gather + 127) >> 7;
-  const int nT = nG + ((hi - lo + 127) >> 7);
   const int n_win = hdr.n;
 
-  uint8_t* sQ = smem + C::OFF_Q;
-  uint8_t* sDO = smem + C::OFF_DO;
-  uint8_t* sK = smem + C::OFF_K;
-  uint8_t* sV = smem + C::OFF_V;
-  uint8_t* sDS = smem + C::OFF_DS;
-
   if (threadIdx.x == 0) {
-    mbar_init(&qd_full, 1);
+    for (int i = 0; i < QB; ++i) {
+      mbar_init(&qd_full[i], 1);
+      mbar_init(&qd_empty[i], 1);
+    }
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], 128);
+    }
     mbar_init(&sd_full, 1);
     mbar_init(&sd_free, 128);
     mbar_init(&ds_full, 128);
     mbar_init(&dq_done, 1);
     mbar_init(&mma_final, 1);
-    for (int s = 0; s < NST; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
-    }
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -635,187 +819,275 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
+  struct Item {
+    int b, h, g, t, n_gather, lo, hi, nG, nT;
+    bool ok;
+  };
+  auto item_at = [&](int i) -> Item {
+    Item r;
+    r.t = T - 1 - i / (B * Hq);
+    const int bh = i % (B * Hq);
+    r.b = bh / Hq;
+    r.h = bh % Hq;
+    r.g = r.h / (Hq / Hkv);
+    const int4 blk = *reinterpret_cast<const int4*>(idx.blocks + ((size_t)r.b * T + r.t) * 4);
+    r.n_gather = blk.x;
+    r.lo = blk.y;
+    r.hi = blk.z;
+    const int q0 = r.t * 128;
+    r.ok = !(blk.x < 0 || blk.x > blk.y || blk.y < 0 || blk.y > q0 || blk.z <= q0 || blk.z > L);
+    r.nG = r.ok ? (blk.x + 127) >> 7 : 0;
+    r.nT = r.ok ? r.nG + ((blk.z - blk.y + 127) >> 7) : 0;
+    return r;
+  };
+
   if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      const int plane_q = b * Hq + h, plane_kv = b * Hkv + g;
-      mbar_arrive_expect_tx(&qd_full, 2 * C::TILE);
-      for (int c = 0; c < C::DCH; ++c) {
-        tma_load_3d(sQ + c * kChunk, &tm_q, &qd_full, 64 * c, q0, plane_q);
-        tma_load_3d(sDO + c * kChunk, &tm_do, &qd_full, 64 * c, q0, plane_q);
-      }
-      int issued = 0;
+      int k = 0, ug = 0, qd_issued = 0;
       bool ok = true;
-      for (int u = 0; u < nT; ++u) {
-        const int st = u % NST;
-        if (u >= NST && !mbar_wait(&kv_empty[st], ((u / NST) - 1) & 1, status)) {
+      for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x, ++k) {
+        const Item it = item_at(i);
+        if (!it.ok) {
+          report(status, SEP_ERR_DEVICE_BOUNDS);
           ok = false;
           break;
         }
-        const bool gat = u < nG;
-        const CUtensorMap* mk = gat ? &tm_kk : &tm_k;
-        const CUtensorMap* mv = gat ? &tm_vk : &tm_v;
-        const int row = gat ? 128 * u : lo + 128 * (u - nG);
-        mbar_arrive_expect_tx(&kv_full[st], 2 * C::TILE);
-        for (int c = 0; c < C::DCH; ++c) {
-          tma_load_3d(sK + st * C::TILE + c * kChunk, mk, &kv_full[st], 64 * c, row, plane_kv);
-          tma_load_3d(sV + st * C::TILE + c * kChunk, mv, &kv_full[st], 64 * c, row, plane_kv);
+        const int qb = k % QB;
+        if (k >= QB && !mbar_wait(&qd_empty[qb], ((k / QB) - 1) & 1, status)) {
+          ok = false;
+          break;
         }
-        issued = u + 1;
+        const int plane_q = it.b * Hq + it.h, plane_kv = it.b * Hkv + it.g;
+        uint8_t* sQ = smem + C::OFF_QD + qb * 2 * C::TILE;
+        mbar_arrive_expect_tx(&qd_full[qb], 2 * C::TILE);
+        for (int c = 0; c < C::DCH; ++c) {
+          tma_load_3d(sQ + c * kChunk, &tm_q, &qd_full[qb], 64 * c, it.t * 128, plane_q);
+          tma_load_3d(sQ + C::TILE + c * kChunk, &tm_do, &qd_full[qb], 64 * c, it.t * 128,
+                      plane_q);
+        }
+        qd_issued = k + 1;
+        for (int u = 0; u < it.nT; ++u) {
+          const int st = ug % NST;
+          if (ug >= NST && !mbar_wait(&kv_empty[st], ((ug / NST) - 1) & 1, status)) {
+            ok = false;
+            break;
+          }
+          ++ug;  // counts issued K/V tiles
+          const bool gat = u < it.nG;
+          const int row = gat ? 128 * u : it.lo + 128 * (u - it.nG);
+          mbar_arrive_expect_tx(&kv_full[st], 2 * C::TILE);
+          for (int c = 0; c < C::DCH; ++c) {
+            tma_load_3d(smem + C::OFF_K + st * C::TILE + c * kChunk, gat ? &tm_kk : &tm_k,
+                        &kv_full[st], 64 * c, row, plane_kv);
+            tma_load_3d(smem + C::OFF_V + st * C::TILE + c * kChunk, gat ? &tm_vk : &tm_v,
+                        &kv_full[st], 64 * c, row, plane_kv);
+          }
+        }
       }
       if (!ok) {
-        for (int u = issued - NST; u < issued; ++u)
-          if (u >= 0) mbar_wait(&kv_full[u % NST], (u / NST) & 1, status);
-        mbar_wait(&qd_full, 0, status);
+        // after a failed wait, let the copies still in flight land
+        for (int x = max(0, qd_issued - QB); x < qd_issued; ++x)
+          mbar_wait(&qd_full[x % QB], (x / QB) & 1, status);
+        for (int x = max(0, ug - NST); x < ug; ++x)
+          mbar_wait(&kv_full[x % NST], (x / NST) & 1, status);
       }
     }
   } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_ss = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idesc_acc = idesc_bf16_f32(128, D, false, true);
-      const uint32_t q_base = smem_u32(sQ), do_base = smem_u32(sDO), k_base = smem_u32(sK),
-                     v_base = smem_u32(sV), ds_base = smem_u32(sDS);
-      auto issue_sdp = [&](int u) -> bool {
-        const int st = u % NST;
-        if (!mbar_wait(&kv_full[st], (u / NST) & 1, status)) return false;
+      const uint32_t k_base = smem_u32(smem + C::OFF_K), v_base = smem_u32(smem + C::OFF_V),
+                     ds_base = smem_u32(smem + C::OFF_DS);
+      int k = 0, ug = 0;
+      bool ok = true;
+      for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x, ++k) {
+        const Item it = item_at(i);
+        if (!it.ok) break;
+        const int qb = k % QB, ab = k & 1;
+        const uint32_t q_base = smem_u32(smem + C::OFF_QD + qb * 2 * C::TILE);
+        const uint32_t do_base = q_base + C::TILE;
+        const uint32_t tm_dq = tmem + C::TM_DQ + ab * D;
+        if (!mbar_wait(&qd_full[qb], (k / QB) & 1, status)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
+        auto issue_sdp = [&](int ugl) -> bool {
+          const int st = ugl % NST;
+          if (!mbar_wait(&kv_full[st], (ugl / NST) & 1, status)) return false;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
-          umma_bf16_ss(tmem + C::TM_S, sdesc_sw128(q_base + off, 16, 1024),
-                       sdesc_sw128(k_base + st * C::TILE + off, 16, 1024), idesc_ss, kk > 0);
-        }
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
+            umma_bf16_ss(tmem + C::TM_S, sdesc_sw128(q_base + off, 16, 1024),
+                         sdesc_sw128(k_base + st * C::TILE + off, 16, 1024), idesc_ss, kk > 0);
+          }
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
-          umma_bf16_ss(tmem + C::TM_DP, sdesc_sw128(do_base + off, 16, 1024),
-                       sdesc_sw128(v_base + st * C::TILE + off, 16, 1024), idesc_ss, kk > 0);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
+            umma_bf16_ss(tmem + C::TM_DP, sdesc_sw128(do_base + off, 16, 1024),
+                         sdesc_sw128(v_base + st * C::TILE + off, 16, 1024), idesc_ss, kk > 0);
+          }
+          umma_commit(&sd_full);
+          return true;
+        };
+        if (ug > 0 && !mbar_wait(&sd_free, (ug - 1) & 1, status)) {
+          ok = false;
+          break;
         }
-        umma_commit(&sd_full);
-        return true;
-      };
-      auto issue_dq = [&](int u) -> bool {
-        const int st = u % NST;
-        if (!mbar_wait(&ds_full, u & 1, status)) return false;
+        if (!issue_sdp(ug)) {
+          ok = false;
+          break;
+        }
+        if (k >= 2 && !mbar_wait(&acc_empty[ab], ((k >> 1) - 1) & 1, status)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
+        for (int u = 0; ok && u < it.nT; ++u) {
+          const int ugl = ug + u;
+          if (u + 1 < it.nT) {
+            ok = mbar_wait(&sd_free, ugl & 1, status) && issue_sdp(ugl + 1);
+            if (!ok) break;
+          }
+          if (!mbar_wait(&ds_full, ugl & 1, status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int st = ugl % NST;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t aoff = (kk >> 2) * kChunk + (kk & 3) * 32;
-          umma_bf16_ss(tmem + C::TM_DQ, sdesc_sw128(ds_base + aoff, 16, 1024),
-                       sdesc_sw128(k_base + st * C::TILE + kk * 2048, kChunk, 1024), idesc_acc,
-                       (u > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t aoff = (kk >> 2) * kChunk + (kk & 3) * 32;
+            umma_bf16_ss(tm_dq, sdesc_sw128(ds_base + aoff, 16, 1024),
+                         sdesc_sw128(k_base + st * C::TILE + kk * 2048, kChunk, 1024), idesc_acc,
+                         (u > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(&dq_done);
+          umma_commit(&kv_empty[st]);
+          if (u + 1 == it.nT) umma_commit(&qd_empty[qb]);  // Q / dO of this item are done
         }
-        umma_commit(&dq_done);
-        umma_commit(&kv_empty[st]);
-        return true;
-      };
-      bool ok = mbar_wait(&qd_full, 0, status);
-      tc_fence_after();
-      if (ok) ok = issue_sdp(0);
-      for (int u = 0; ok && u < nT; ++u) {
-        if (u + 1 < nT) {
-          ok = mbar_wait(&sd_free, u & 1, status);
-          if (ok) ok = issue_sdp(u + 1);
-        }
-        if (ok) ok = issue_dq(u);
+        if (!ok) break;
+        umma_commit(&acc_full[ab]);
+        ug += it.nT;
       }
       umma_commit(&mma_final);
       mbar_wait(&mma_final, 0, status);
     }
     __syncwarp();
   } else {
+    // ---------------------------------------------------------- elementwise
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
-    const int i = q0 + r;
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t* kbits = idx.keep_bits + (size_t)b * hdr.nwords;
+    const uint32_t* kb_all = idx.keep_bits;
     const int nwords = hdr.nwords;
-    const bool row_live = i < L;
-    const size_t ri = ((size_t)b * Hq + h) * L + (row_live ? i : 0);
-    const float lse2 = row_live ? lse[ri] * kLog2e : 0.f;
-    const float dlt = row_live ? delta[ri] : 0.f;
+    uint8_t* sDS = smem + C::OFF_DS;
+    int k = 0, ug = 0;
     bool ok = true;
-    for (int u = 0; u < nT; ++u) {
-      uint32_t vm[4];
-      if (!row_live) {
-        vm[0] = vm[1] = vm[2] = vm[3] = 0u;
-      } else if (u < nG) {
-        const int nv = min(128, n_gather - 128 * u);
+    for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x, ++k) {
+      const Item it = item_at(i);
+      if (!it.ok) break;
+      const int ab = k & 1;
+      const int i_row = it.t * 128 + r;
+      const bool row_live = i_row < L;
+      const float2 st2 = stats[((size_t)it.b * Hq + it.h) * T * 128 + it.t * 128 + r];
+      const float lse2 = st2.x, dlt = st2.y;
+      const uint32_t* kbits = kb_all + (size_t)it.b * nwords;
+      for (int u = 0; u < it.nT; ++u) {
+        const int ugl = ug + u;
+        uint32_t vm[4];
+        if (!row_live) {
+          vm[0] = vm[1] = vm[2] = vm[3] = 0u;
+        } else if (u < it.nG) {
+          const int nv = min(128, it.n_gather - 128 * u);
 #pragma unroll
-        for (int w = 0; w < 4; ++w) vm[w] = range_bits(0, nv, w);
-      } else {
-        const int jt = lo + 128 * (u - nG);
-        const int n_causal = min(128, max(0, i - jt + 1));
-        const int c_win = i - n_win + 1 - jt;
-        const int wj = jt >> 5, sh = jt & 31;
-        uint32_t kw[5];
+          for (int w = 0; w < 4; ++w) vm[w] = range_bits(0, nv, w);
+        } else {
+          const int jt = it.lo + 128 * (u - it.nG);
+          const int n_causal = min(128, max(0, i_row - jt + 1));
+          const int c_win = i_row - n_win + 1 - jt;
+          const int wj = jt >> 5, sh = jt & 31;
+          uint32_t kw[5];
 #pragma unroll
-        for (int x = 0; x < 5; ++x) kw[x] = (wj + x < nwords) ? __ldg(kbits + wj + x) : 0u;
+          for (int x = 0; x < 5; ++x) kw[x] = (wj + x < nwords) ? __ldg(kbits + wj + x) : 0u;
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const uint32_t keepw = sh ? ((kw[w] >> sh) | (kw[w + 1] << (32 - sh))) : kw[w];
-          vm[w] = range_bits(0, n_causal, w) & (range_bits(c_win, 128, w) | keepw);
+          for (int w = 0; w < 4; ++w) {
+            const uint32_t keepw = sh ? ((kw[w] >> sh) | (kw[w + 1] << (32 - sh))) : kw[w];
+            vm[w] = range_bits(0, n_causal, w) & (range_bits(c_win, 128, w) | keepw);
+          }
         }
+        if (!mbar_wait(&sd_full, ugl & 1, status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t dsk[64];
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t sr[32], dr[32];
+          tmem_ld32(tmem + lane_base + C::TM_S + 32 * cc, sr);
+          tmem_ld32(tmem + lane_base + C::TM_DP + 32 * cc, dr);
+          tmem_ld_wait();
+#pragma unroll
+          for (int x = 0; x < 32; x += 2) {
+            const bool v0 = (vm[cc] >> x) & 1u, v1 = (vm[cc] >> (x + 1)) & 1u;
+            const float p0 = v0 ? fast_exp2(__uint_as_float(sr[x]) * scale_log2 - lse2) : 0.f;
+            const float p1 =
+                v1 ? fast_exp2(__uint_as_float(sr[x + 1]) * scale_log2 - lse2) : 0.f;
+            dsk[(32 * cc + x) >> 1] = pack_bf16x2(p0 * (__uint_as_float(dr[x]) - dlt),
+                                                  p1 * (__uint_as_float(dr[x + 1]) - dlt));
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&sd_free);
+        if (ugl > 0 && !mbar_wait(&dq_done, (ugl - 1) & 1, status)) {
+          ok = false;
+          break;
+        }
+#pragma unroll
+        for (int un = 0; un < 16; ++un) {
+          const uint32_t off = (un >> 3) * kChunk + sw128_offset(r, (un & 7) * 8);
+          *reinterpret_cast<uint4*>(sDS + off) =
+              make_uint4(dsk[4 * un], dsk[4 * un + 1], dsk[4 * un + 2], dsk[4 * un + 3]);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&ds_full);
       }
-      if (!mbar_wait(&sd_full, u & 1, status)) {
+      if (!ok) break;
+      ug += it.nT;
+      if (!mbar_wait(&acc_full[ab], (k >> 1) & 1, status)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t dsk[64];
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t sr[32], dr[32];
-        tmem_ld32(tmem + lane_base + C::TM_S + 32 * cc, sr);
-        tmem_ld32(tmem + lane_base + C::TM_DP + 32 * cc, dr);
-        tmem_ld_wait();
-#pragma unroll
-        for (int x = 0; x < 32; x += 2) {
-          const bool v0 = (vm[cc] >> x) & 1u, v1 = (vm[cc] >> (x + 1)) & 1u;
-          const float p0 = v0 ? fast_exp2(__uint_as_float(sr[x]) * scale_log2 - lse2) : 0.f;
-          const float p1 = v1 ? fast_exp2(__uint_as_float(sr[x + 1]) * scale_log2 - lse2) : 0.f;
-          dsk[(32 * cc + x) >> 1] = pack_bf16x2(p0 * (__uint_as_float(dr[x]) - dlt),
-                                                p1 * (__uint_as_float(dr[x + 1]) - dlt));
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(&sd_free);
-      if (u > 0 && !mbar_wait(&dq_done, (u - 1) & 1, status)) {
-        ok = false;
-        break;
-      }
-#pragma unroll
-      for (int un = 0; un < 16; ++un) {
-        const uint32_t off = (un >> 3) * kChunk + sw128_offset(r, (un & 7) * 8);
-        *reinterpret_cast<uint4*>(sDS + off) =
-            make_uint4(dsk[4 * un], dsk[4 * un + 1], dsk[4 * un + 2], dsk[4 * un + 3]);
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&ds_full);
-    }
-    if (ok && mbar_wait(&dq_done, (nT - 1) & 1, status)) {
-      tc_fence_after();
-      uint32_t qb[32];
-      __nv_bfloat16* qrow = dq + (((size_t)b * Hq + h) * L + i) * D;
+      const uint32_t tm_dq = tmem + C::TM_DQ + ab * D;
+      __nv_bfloat16* qrow = dq + (((size_t)it.b * Hq + it.h) * L + (row_live ? i_row : 0)) * D;
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
-        tmem_ld32(tmem + lane_base + C::TM_DQ + c0, qb);
+        uint32_t qb2[32];
+        tmem_ld32(tm_dq + lane_base + c0, qb2);
         tmem_ld_wait();
         if (row_live) {
 #pragma unroll
           for (int x = 0; x < 32; x += 8) {
             uint4 pk;
-            pk.x = pack_bf16x2(__uint_as_float(qb[x]) * scale, __uint_as_float(qb[x + 1]) * scale);
-            pk.y = pack_bf16x2(__uint_as_float(qb[x + 2]) * scale,
-                               __uint_as_float(qb[x + 3]) * scale);
-            pk.z = pack_bf16x2(__uint_as_float(qb[x + 4]) * scale,
-                               __uint_as_float(qb[x + 5]) * scale);
-            pk.w = pack_bf16x2(__uint_as_float(qb[x + 6]) * scale,
-                               __uint_as_float(qb[x + 7]) * scale);
+            pk.x = pack_bf16x2(__uint_as_float(qb2[x]) * scale, __uint_as_float(qb2[x + 1]) * scale);
+            pk.y = pack_bf16x2(__uint_as_float(qb2[x + 2]) * scale,
+                               __uint_as_float(qb2[x + 3]) * scale);
+            pk.z = pack_bf16x2(__uint_as_float(qb2[x + 4]) * scale,
+                               __uint_as_float(qb2[x + 5]) * scale);
+            pk.w = pack_bf16x2(__uint_as_float(qb2[x + 6]) * scale,
+                               __uint_as_float(qb2[x + 7]) * scale);
             *reinterpret_cast<uint4*>(qrow + c0 + x) = pk;
           }
         }
       }
+      tc_fence_before();
+      mbar_arrive(&acc_empty[ab]);
     }
   }
 
@@ -827,7 +1099,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 struct BwdWs {
   uint8_t *kk, *vk;
-  float *dk_keep, *dv_keep, *delta;
+  float *dk_keep, *dv_keep;
+  float2* stats;  // [B*Hq][ceil(L/128)*128] (LSE in log2 units, Delta)
+  BwdSchedule* sched;
+  int4* items;
   size_t total;
 };
 
@@ -841,12 +1116,25 @@ BwdWs bwd_ws(void* base, int B, int Hq, int Hkv, int L, int d) {
   w.vk = p + off; off += kv_bf16;
   w.dk_keep = reinterpret_cast<float*>(p + off); off += kv_f32;
   w.dv_keep = reinterpret_cast<float*>(p + off); off += kv_f32;
-  w.delta = reinterpret_cast<float*>(p + off); off += align_up((size_t)B * Hq * L * 4, 256);
+  w.stats = reinterpret_cast<float2*>(p + off);
+  off += align_up((size_t)B * Hq * ((L + 127) / 128 * 128) * 8, 256);
+  w.sched = reinterpret_cast<BwdSchedule*>(p + off); off += 256;
+  w.items = reinterpret_cast<int4*>(p + off);
+  off += align_up(sizeof(int4) * bwd_max_items(B, Hkv, (L + 127) / 128), 256);
   w.total = off;
   return w;
 }
 
-template <int D, int NST_KV, int NST_DQ>
+int num_sms() {
+  static int n[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!n[dev] && cudaDeviceGetAttribute(&n[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    n[dev] = 148;
+  return n[dev];
+}
+
+template <int D>
 int launch_bwd_impl(IndexPtrs idx, const void* q, const void* k, const void* v, const void* o,
                     const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
                     int Hq, int Hkv, int L, float scale, void* ws, int* status,
@@ -859,14 +1147,14 @@ int launch_bwd_impl(IndexPtrs idx, const void* q, const void* k, const void* v, 
       reinterpret_cast<uint4*>(w.kk), reinterpret_cast<uint4*>(w.vk), Hkv, L);
   profile_mark(1, s);
   {
-    const size_t rows = (size_t)B * Hq * L;
+    const size_t rows = (size_t)B * Hq * T * 128;
     const int delta_blocks =
         static_cast<int>((rows + prep_rows_per_block<D>() - 1) / prep_rows_per_block<D>());
     const int per_plane = (L * (D / 4) + kPrepThreads * 4 - 1) / (kPrepThreads * 4);
-    bwd_prep_kernel<D><<<delta_blocks + B * Hkv * per_plane, kPrepThreads, 0, s>>>(
-        idx, static_cast<const uint4*>(o), static_cast<const uint4*>(dout), w.delta,
+    bwd_prep_kernel<D><<<delta_blocks + B * Hkv * per_plane + 1, kPrepThreads, 0, s>>>(
+        idx, static_cast<const uint4*>(o), static_cast<const uint4*>(dout), lse, w.stats,
         reinterpret_cast<float4*>(w.dk_keep), reinterpret_cast<float4*>(w.dv_keep), B, Hq, Hkv,
-        L, delta_blocks);
+        L, delta_blocks, w.sched, w.items);
   }
   CUtensorMap mq, mdo, mk, mv, mkk, mvk;
   if (!make_bf16_map(&mq, q, (uint64_t)B * Hq, L, D, 128) ||
@@ -877,30 +1165,31 @@ int launch_bwd_impl(IndexPtrs idx, const void* q, const void* k, const void* v, 
       !make_bf16_map(&mvk, w.vk, (uint64_t)B * Hkv, L, D, 128))
     return static_cast<int>(cudaErrorInvalidValue);
   const float scale_log2 = scale * kLog2e;
-  using KC = KvCfg<D, NST_KV>;
-  using QC = DqCfg<D, NST_DQ>;
-  auto keep_k = bwd_kv_kernel<D, true, NST_KV>;
-  auto dense_k = bwd_kv_kernel<D, false, NST_KV>;
-  auto dq_k = bwd_dq_kernel<D, NST_DQ>;
+  using KC = KvCfg<D>;
+  using QC = DqCfg<D>;
+  auto kv_k = bwd_kv_persistent<D>;
+  auto dq_k = bwd_dq_persistent<D>;
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(keep_k, cudaFuncAttributeMaxDynamicSharedMemorySize, KC::SMEM)) ||
-      (e = cudaFuncSetAttribute(dense_k, cudaFuncAttributeMaxDynamicSharedMemorySize, KC::SMEM)) ||
+  if ((e = cudaFuncSetAttribute(kv_k, cudaFuncAttributeMaxDynamicSharedMemorySize, KC::SMEM)) ||
       (e = cudaFuncSetAttribute(dq_k, cudaFuncAttributeMaxDynamicSharedMemorySize, QC::SMEM)))
     return static_cast<int>(e);
   __nv_bfloat16* dkb = static_cast<__nv_bfloat16*>(dk);
   __nv_bfloat16* dvb = static_cast<__nv_bfloat16*>(dv);
+  const int sms = num_sms();
   profile_mark(2, s);
-  keep_k<<<dim3(T * ((T + kKeepChunk - 1) / kKeepChunk), Hq, B), kThreads, KC::SMEM, s>>>(mkk, mvk, mq, mdo, idx, lse, w.delta,
-                                                      w.dk_keep, w.dv_keep, dkb, dvb, B, Hq, Hkv,
-                                                      L, scale, scale_log2, status);
+  kv_k<<<sms, kThreads, KC::SMEM, s>>>(mkk, mvk, mk, mv, mq, mdo, idx, w.sched, w.items,
+                                       w.stats, w.dk_keep, w.dv_keep, dkb, dvb, B, Hq, Hkv, L,
+                                       scale, scale_log2, status);
   profile_mark(3, s);
-  dense_k<<<dim3(T, Hkv, B), kThreads, KC::SMEM, s>>>(mk, mv, mq, mdo, idx, lse, w.delta,
-                                                        w.dk_keep, w.dv_keep, dkb, dvb, B, Hq,
-                                                        Hkv, L, scale, scale_log2, status);
+  const int dq_items = B * Hq * T;
+  dq_k<<<dq_items < sms ? dq_items : sms, kThreads, QC::SMEM, s>>>(
+      mq, mdo, mk, mv, mkk, mvk, idx, w.stats, static_cast<__nv_bfloat16*>(dq), B, Hq, Hkv,
+      L, scale, scale_log2, status);
   profile_mark(4, s);
-  dq_k<<<dim3(T, Hq, B), kThreads, QC::SMEM, s>>>(mq, mdo, mk, mv, mkk, mvk, idx, lse, w.delta,
-                                                    static_cast<__nv_bfloat16*>(dq), B, Hq, Hkv,
-                                                    L, scale, scale_log2, status);
+  bwd_keep_scatter_kernel<D><<<dim3((L * (D / 4) + 255) / 256 < 64 ? (L * (D / 4) + 255) / 256 : 64,
+                                    Hkv, B), 256, 0, s>>>(
+      idx, reinterpret_cast<const float4*>(w.dk_keep), reinterpret_cast<const float4*>(w.dv_keep),
+      dkb, dvb, B, Hkv, L, scale);
   const cudaError_t err = cudaGetLastError();
   profile_mark(5, s);
   return static_cast<int>(err);
@@ -918,10 +1207,10 @@ int launch_attn_bwd_tc(IndexPtrs idx, const void* q, const void* k, const void* 
                        void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (d == 64)
-    return launch_bwd_impl<64, 2, 3>(idx, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, L,
-                                     scale, ws, status, s);
-  return launch_bwd_impl<128, 1, 2>(idx, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, L, scale,
-                                    ws, status, s);
+    return launch_bwd_impl<64>(idx, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, L, scale, ws,
+                               status, s);
+  return launch_bwd_impl<128>(idx, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, L, scale, ws,
+                              status, s);
 }
 
 }  // namespace sep

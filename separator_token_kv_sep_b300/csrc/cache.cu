@@ -143,17 +143,6 @@ __device__ __forceinline__ float dsmem_ld(uint32_t addr) {
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
   return v;
 }
-// Global -> shared bulk copy (TMA, untiled); completion as transaction
-// bytes on `bar`.  Both addresses 16-byte aligned, bytes a multiple of 16.
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
-                                         uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
 // Packed fp32 pairs (f32x2): d = a * b + c and d = a * b, two lanes' worth
 // of arithmetic in one instruction.
 __device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b0,
