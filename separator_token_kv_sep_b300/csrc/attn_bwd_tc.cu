@@ -38,7 +38,8 @@ namespace sep {
 namespace {
 
 constexpr int kChunk = 128 * 128;  // bytes of a [128 rows x 64 cols] bf16 block
-constexpr int kThreads = 192;      // warp 0 TMA, warp 1 MMA, warps 2-5 elementwise
+constexpr int kThreads = 320;      // warp 0 TMA, warp 1 MMA, warps 2-9 elementwise
+constexpr int kEwThreads = 256;    // two elementwise warpgroups
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kKeepChunk = 4;      // query tiles per CTA of the keep-tile dK/dV kernel
 
@@ -237,7 +238,7 @@ __global__ void __launch_bounds__(kPrepThreads)
       for (int off = U / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
       const size_t row = row0 + it * RPI + sub;
       if (u == 0 && row < R)
-        stats[row] = live[it] ? make_float2(lse[src[it]] * kLog2e, acc) : make_float2(0.f, 0.f);
+        stats[row] = live[it] ? make_float2(-lse[src[it]] * kLog2e, -acc) : make_float2(0.f, 0.f);
     }
     return;
   }
@@ -309,7 +310,7 @@ struct KvCfg {
   static constexpr int OFF_DO = OFF_Q + NST * TILE;
   static constexpr int OFF_P = OFF_DO + NST * TILE;
   static constexpr int OFF_DS = OFF_P + 2 * kChunk;
-  static constexpr int OFF_STAT = OFF_DS + 2 * kChunk;  // [NST][128] (LSE log2, Delta)
+  static constexpr int OFF_STAT = OFF_DS + 2 * kChunk;  // [NST][128] (-LSE log2, -Delta)
   static constexpr int SMEM = OFF_STAT + NST * 128 * 8 + 1024;
   static constexpr int TM_S = 0, TM_DP = 128, TM_ACC = 256;  // acc b: dV at +2bD, dK at +2bD+D
   static constexpr int TM_COLS = 512;
@@ -367,11 +368,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < ACB; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 128);
+      mbar_init(&acc_empty[i], kEwThreads);
     }
     mbar_init(&sd_full, 1);
-    mbar_init(&sd_free, 128);
-    mbar_init(&ps_full, 128);
+    mbar_init(&sd_free, kEwThreads);
+    mbar_init(&ps_full, kEwThreads);
     mbar_init(&pd_done, 1);
     mbar_init(&mma_final, 1);
     fence_mbar_init();
@@ -556,9 +557,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ---------------------------------------------------------- elementwise
+    // Two warpgroups share every tile: warps 2-5 take query columns 0-63 and
+    // warps 6-9 columns 64-127 of the same 128 key rows (warp w reads TMEM
+    // lanes 32*(w%4)..).  In the epilogue the first writes dV, the second dK.
     const int quad = warp & 3;
-    const int r = quad * 32 + lane;   // key row of the tile
-    const int ew = threadIdx.x - 64;  // 0..127
+    const int half = (warp - 2) >> 2;
+    const int r = quad * 32 + lane;  // key row of the tile
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
     uint8_t* sP = smem + C::OFF_P;
     uint8_t* sDS = smem + C::OFF_DS;
@@ -577,54 +581,61 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nU = G * it.nt;
       for (int u = 0; u < nU; ++u) {
         const int ugl = ug + u;
-        const int h = it.g * G + u / it.nt, t = it.t0 + u % it.nt;
+        const int t = it.t0 + u % it.nt;
         const int i0 = t * 128;
-        (void)h;
-        uint32_t vm[4];
-        const int4 blk = *reinterpret_cast<const int4*>(blocks + 4 * t);
-        const int c_end = min(128, L - i0);  // query rows past L are padding
-        if (keep) {
-          const bool row_ok = j < blk.x && j < count;  // gathered by this query tile
-#pragma unroll
-          for (int w = 0; w < 4; ++w) vm[w] = row_ok ? range_bits(0, c_end, w) : 0u;
-        } else {
-          const bool in_band = j >= blk.y && j < blk.z && j < L;
-          const int c_lo = j - i0;
-          const int c_hi = keep_j ? c_end : min(c_end, j + n_win - i0);
-#pragma unroll
-          for (int w = 0; w < 4; ++w) vm[w] = in_band ? range_bits(c_lo, c_hi, w) : 0u;
+        // visible query columns of this row among the half's 64, as 2 words
+        uint32_t vm[2];
+        {
+          const int4 blk = *reinterpret_cast<const int4*>(blocks + 4 * t);
+          const int c_end = min(128, L - i0);  // query rows past L are padding
+          int c_lo = 0, c_hi = 0;
+          if (keep) {
+            if (j < blk.x && j < count) c_hi = c_end;  // gathered by this query tile
+          } else if (j >= blk.y && j < blk.z && j < L) {
+            c_lo = j - i0;
+            c_hi = keep_j ? c_end : min(c_end, j + n_win - i0);
+          }
+          vm[0] = range_bits(c_lo, c_hi, 2 * half);
+          vm[1] = range_bits(c_lo, c_hi, 2 * half + 1);
         }
         if (!mbar_wait(&sd_full, ugl & 1, status)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        // the query tile's (LSE log2, Delta) arrived with its Q / dO tiles
+        // the query tile's (-LSE log2, -Delta) arrived with its Q / dO tiles
         const int stg = ugl % NST;
         if (!mbar_wait(&qd_full[stg], (ugl / NST) & 1, status)) {
           ok = false;
           break;
         }
-        const float2* sst = reinterpret_cast<const float2*>(smem + C::OFF_STAT + stg * 1024);
-        uint32_t pk[64], dk2[64];
+        const float4* sst =
+            reinterpret_cast<const float4*>(smem + C::OFF_STAT + stg * 1024) + 32 * half;
+        uint32_t pk[32], dk2[32];
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < 2; ++cc) {
           uint32_t sr[32], dr[32];
-          tmem_ld32(tmem + lane_base + C::TM_S + 32 * cc, sr);
-          tmem_ld32(tmem + lane_base + C::TM_DP + 32 * cc, dr);
+          tmem_ld32(tmem + lane_base + C::TM_S + 64 * half + 32 * cc, sr);
+          tmem_ld32(tmem + lane_base + C::TM_DP + 64 * half + 32 * cc, dr);
           tmem_ld_wait();
+          const uint32_t w = vm[cc];
+          const bool full = __all_sync(0xffffffffu, w == 0xffffffffu);
 #pragma unroll
           for (int x = 0; x < 32; x += 2) {
-            const int c = 32 * cc + x;
-            const bool v0 = (vm[cc] >> x) & 1u, v1 = (vm[cc] >> (x + 1)) & 1u;
-            const float4 st2 = *reinterpret_cast<const float4*>(sst + c);  // columns c, c+1
-            const float p0 = v0 ? fast_exp2(__uint_as_float(sr[x]) * scale_log2 - st2.x) : 0.f;
-            const float p1 =
-                v1 ? fast_exp2(__uint_as_float(sr[x + 1]) * scale_log2 - st2.z) : 0.f;
-            const float d0 = p0 * (__uint_as_float(dr[x]) - st2.y);
-            const float d1 = p1 * (__uint_as_float(dr[x + 1]) - st2.w);
-            pk[c >> 1] = pack_bf16x2(p0, p1);
-            dk2[c >> 1] = pack_bf16x2(d0, d1);
+            const float4 st2 = sst[16 * cc + x / 2];  // columns (x, x+1): (-lse, -delta) pairs
+            float a0, a1, d0, d1;
+            ffma2(a0, a1, __uint_as_float(sr[x]), __uint_as_float(sr[x + 1]), scale_log2,
+                  scale_log2, st2.x, st2.z);
+            float p0 = fast_exp2(a0), p1 = fast_exp2(a1);
+            if (!full) {
+              p0 = ((w >> x) & 1u) ? p0 : 0.f;
+              p1 = ((w >> (x + 1)) & 1u) ? p1 : 0.f;
+            }
+            ffma2(d0, d1, __uint_as_float(dr[x]), __uint_as_float(dr[x + 1]), 1.f, 1.f, st2.y,
+                  st2.w);
+            fmul2(d0, d1, p0, p1, d0, d1);
+            pk[16 * cc + x / 2] = pack_bf16x2(p0, p1);
+            dk2[16 * cc + x / 2] = pack_bf16x2(d0, d1);
           }
         }
         tc_fence_before();
@@ -633,9 +644,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
+        // this half's 64 query columns are one 64-column block of the
+        // 128-byte-swizzle K-major P^T / dS^T tiles
 #pragma unroll
-        for (int un = 0; un < 16; ++un) {
-          const uint32_t off = (un >> 3) * kChunk + sw128_offset(r, (un & 7) * 8);
+        for (int un = 0; un < 8; ++un) {
+          const uint32_t off = half * kChunk + sw128_offset(r, un * 8);
           *reinterpret_cast<uint4*>(sP + off) =
               make_uint4(pk[4 * un], pk[4 * un + 1], pk[4 * un + 2], pk[4 * un + 3]);
           *reinterpret_cast<uint4*>(sDS + off) =
@@ -647,53 +660,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       ug += nU;
-      // ---- epilogue of the item: accumulators -> global
+      // ---- epilogue of the item: accumulators -> global (half 0 dV, half 1 dK)
       if (!mbar_wait(&acc_full[ab], (k / ACB) & 1, status)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t tm_dv = tmem + C::TM_ACC + ab * 2 * D, tm_dk = tm_dv + D;
+      const uint32_t tm_acc = tmem + C::TM_ACC + ab * 2 * D + half * D;
       // KEEP rows and DENSE keep tokens add into the fp32 keep accumulators
       // (written to dK/dV by the scatter kernel); other DENSE rows are final.
       const bool to_acc = keep ? (j < count) : (j < L && keep_j);
       const bool to_out = !keep && j < L && !keep_j;
       const int kidx = keep ? j : (keep_j ? idx.keep_prefix[(size_t)it.b * (L + 1) + j] : 0);
-      float* dkr = dk_keep + (((size_t)it.b * Hkv + it.g) * L + kidx) * D;
-      float* dvr = dv_keep + (((size_t)it.b * Hkv + it.g) * L + kidx) * D;
-      __nv_bfloat16* dko = dk + (((size_t)it.b * Hkv + it.g) * L + (to_out ? j : 0)) * D;
-      __nv_bfloat16* dvo = dv + (((size_t)it.b * Hkv + it.g) * L + (to_out ? j : 0)) * D;
+      float* accr = (half ? dk_keep : dv_keep) + (((size_t)it.b * Hkv + it.g) * L + kidx) * D;
+      __nv_bfloat16* outr =
+          (half ? dk : dv) + (((size_t)it.b * Hkv + it.g) * L + (to_out ? j : 0)) * D;
+      const float osc = half ? scale : 1.f;
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t vb[32], kb[32];
-        tmem_ld32(tm_dv + lane_base + c0, vb);
-        tmem_ld32(tm_dk + lane_base + c0, kb);
+        uint32_t vb[32];
+        tmem_ld32(tm_acc + lane_base + c0, vb);
         tmem_ld_wait();
         if (to_acc) {
 #pragma unroll
-          for (int x = 0; x < 32; x += 4) {
-            red_add_v4(dvr + c0 + x, __uint_as_float(vb[x]), __uint_as_float(vb[x + 1]),
+          for (int x = 0; x < 32; x += 4)
+            red_add_v4(accr + c0 + x, __uint_as_float(vb[x]), __uint_as_float(vb[x + 1]),
                        __uint_as_float(vb[x + 2]), __uint_as_float(vb[x + 3]));
-            red_add_v4(dkr + c0 + x, __uint_as_float(kb[x]), __uint_as_float(kb[x + 1]),
-                       __uint_as_float(kb[x + 2]), __uint_as_float(kb[x + 3]));
-          }
         } else if (to_out) {
 #pragma unroll
           for (int x = 0; x < 32; x += 8) {
-            uint4 ov, ok4;
-            ov.x = pack_bf16x2(__uint_as_float(vb[x]), __uint_as_float(vb[x + 1]));
-            ov.y = pack_bf16x2(__uint_as_float(vb[x + 2]), __uint_as_float(vb[x + 3]));
-            ov.z = pack_bf16x2(__uint_as_float(vb[x + 4]), __uint_as_float(vb[x + 5]));
-            ov.w = pack_bf16x2(__uint_as_float(vb[x + 6]), __uint_as_float(vb[x + 7]));
-            ok4.x = pack_bf16x2(__uint_as_float(kb[x]) * scale, __uint_as_float(kb[x + 1]) * scale);
-            ok4.y = pack_bf16x2(__uint_as_float(kb[x + 2]) * scale,
-                                __uint_as_float(kb[x + 3]) * scale);
-            ok4.z = pack_bf16x2(__uint_as_float(kb[x + 4]) * scale,
-                                __uint_as_float(kb[x + 5]) * scale);
-            ok4.w = pack_bf16x2(__uint_as_float(kb[x + 6]) * scale,
-                                __uint_as_float(kb[x + 7]) * scale);
-            *reinterpret_cast<uint4*>(dvo + c0 + x) = ov;
-            *reinterpret_cast<uint4*>(dko + c0 + x) = ok4;
+            uint4 ov;
+            ov.x = pack_bf16x2(__uint_as_float(vb[x]) * osc, __uint_as_float(vb[x + 1]) * osc);
+            ov.y = pack_bf16x2(__uint_as_float(vb[x + 2]) * osc, __uint_as_float(vb[x + 3]) * osc);
+            ov.z = pack_bf16x2(__uint_as_float(vb[x + 4]) * osc, __uint_as_float(vb[x + 5]) * osc);
+            ov.w = pack_bf16x2(__uint_as_float(vb[x + 6]) * osc, __uint_as_float(vb[x + 7]) * osc);
+            *reinterpret_cast<uint4*>(outr + c0 + x) = ov;
           }
         }
       }
@@ -801,11 +802,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 128);
+      mbar_init(&acc_empty[i], kEwThreads);
     }
     mbar_init(&sd_full, 1);
-    mbar_init(&sd_free, 128);
-    mbar_init(&ds_full, 128);
+    mbar_init(&sd_free, kEwThreads);
+    mbar_init(&ds_full, kEwThreads);
     mbar_init(&dq_done, 1);
     mbar_init(&mma_final, 1);
     fence_mbar_init();
@@ -979,7 +980,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ---------------------------------------------------------- elementwise
+    // Two warpgroups share every tile: warps 2-5 take key columns 0-63 and
+    // warps 6-9 columns 64-127 of the same 128 query rows; in the epilogue
+    // each writes half of the dQ columns.
     const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int r = quad * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t* kb_all = idx.keep_bits;
@@ -993,30 +998,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ab = k & 1;
       const int i_row = it.t * 128 + r;
       const bool row_live = i_row < L;
+      // (-LSE log2, -Delta) of this row (zero for padding rows)
       const float2 st2 = stats[((size_t)it.b * Hq + it.h) * T * 128 + it.t * 128 + r];
-      const float lse2 = st2.x, dlt = st2.y;
       const uint32_t* kbits = kb_all + (size_t)it.b * nwords;
       for (int u = 0; u < it.nT; ++u) {
         const int ugl = ug + u;
-        uint32_t vm[4];
+        uint32_t vm[2];
         if (!row_live) {
-          vm[0] = vm[1] = vm[2] = vm[3] = 0u;
+          vm[0] = vm[1] = 0u;
         } else if (u < it.nG) {
           const int nv = min(128, it.n_gather - 128 * u);
-#pragma unroll
-          for (int w = 0; w < 4; ++w) vm[w] = range_bits(0, nv, w);
+          vm[0] = range_bits(0, nv, 2 * half);
+          vm[1] = range_bits(0, nv, 2 * half + 1);
         } else {
-          const int jt = it.lo + 128 * (u - it.nG);
-          const int n_causal = min(128, max(0, i_row - jt + 1));
+          const int jt = it.lo + 128 * (u - it.nG) + 64 * half;  // first key of this half
+          const int n_causal = min(64, max(0, i_row - jt + 1));
           const int c_win = i_row - n_win + 1 - jt;
           const int wj = jt >> 5, sh = jt & 31;
-          uint32_t kw[5];
+          uint32_t kw[3];
 #pragma unroll
-          for (int x = 0; x < 5; ++x) kw[x] = (wj + x < nwords) ? __ldg(kbits + wj + x) : 0u;
+          for (int x = 0; x < 3; ++x) kw[x] = (wj + x < nwords) ? __ldg(kbits + wj + x) : 0u;
 #pragma unroll
-          for (int w = 0; w < 4; ++w) {
+          for (int w = 0; w < 2; ++w) {
             const uint32_t keepw = sh ? ((kw[w] >> sh) | (kw[w + 1] << (32 - sh))) : kw[w];
-            vm[w] = range_bits(0, n_causal, w) & (range_bits(c_win, 128, w) | keepw);
+            vm[w] = range_bits(0, n_causal, w) & (range_bits(c_win, 64, w) | keepw);
           }
         }
         if (!mbar_wait(&sd_full, ugl & 1, status)) {
@@ -1024,21 +1029,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        uint32_t dsk[64];
+        uint32_t dsk[32];
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < 2; ++cc) {
           uint32_t sr[32], dr[32];
-          tmem_ld32(tmem + lane_base + C::TM_S + 32 * cc, sr);
-          tmem_ld32(tmem + lane_base + C::TM_DP + 32 * cc, dr);
+          tmem_ld32(tmem + lane_base + C::TM_S + 64 * half + 32 * cc, sr);
+          tmem_ld32(tmem + lane_base + C::TM_DP + 64 * half + 32 * cc, dr);
           tmem_ld_wait();
+          const uint32_t w = vm[cc];
+          const bool full = __all_sync(0xffffffffu, w == 0xffffffffu);
 #pragma unroll
           for (int x = 0; x < 32; x += 2) {
-            const bool v0 = (vm[cc] >> x) & 1u, v1 = (vm[cc] >> (x + 1)) & 1u;
-            const float p0 = v0 ? fast_exp2(__uint_as_float(sr[x]) * scale_log2 - lse2) : 0.f;
-            const float p1 =
-                v1 ? fast_exp2(__uint_as_float(sr[x + 1]) * scale_log2 - lse2) : 0.f;
-            dsk[(32 * cc + x) >> 1] = pack_bf16x2(p0 * (__uint_as_float(dr[x]) - dlt),
-                                                  p1 * (__uint_as_float(dr[x + 1]) - dlt));
+            float a0, a1, d0, d1;
+            ffma2(a0, a1, __uint_as_float(sr[x]), __uint_as_float(sr[x + 1]), scale_log2,
+                  scale_log2, st2.x, st2.x);
+            float p0 = fast_exp2(a0), p1 = fast_exp2(a1);
+            if (!full) {
+              p0 = ((w >> x) & 1u) ? p0 : 0.f;
+              p1 = ((w >> (x + 1)) & 1u) ? p1 : 0.f;
+            }
+            ffma2(d0, d1, __uint_as_float(dr[x]), __uint_as_float(dr[x + 1]), 1.f, 1.f, st2.y,
+                  st2.y);
+            fmul2(d0, d1, p0, p1, d0, d1);
+            dsk[16 * cc + x / 2] = pack_bf16x2(d0, d1);
           }
         }
         tc_fence_before();
@@ -1048,8 +1061,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
 #pragma unroll
-        for (int un = 0; un < 16; ++un) {
-          const uint32_t off = (un >> 3) * kChunk + sw128_offset(r, (un & 7) * 8);
+        for (int un = 0; un < 8; ++un) {
+          const uint32_t off = half * kChunk + sw128_offset(r, un * 8);
           *reinterpret_cast<uint4*>(sDS + off) =
               make_uint4(dsk[4 * un], dsk[4 * un + 1], dsk[4 * un + 2], dsk[4 * un + 3]);
         }
@@ -1067,7 +1080,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tm_dq = tmem + C::TM_DQ + ab * D;
       __nv_bfloat16* qrow = dq + (((size_t)it.b * Hq + it.h) * L + (row_live ? i_row : 0)) * D;
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
+      for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
         uint32_t qb2[32];
         tmem_ld32(tm_dq + lane_base + c0, qb2);
         tmem_ld_wait();
@@ -1100,7 +1113,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 struct BwdWs {
   uint8_t *kk, *vk;
   float *dk_keep, *dv_keep;
-  float2* stats;  // [B*Hq][ceil(L/128)*128] (LSE in log2 units, Delta)
+  float2* stats;  // [B*Hq][ceil(L/128)*128] (-LSE in log2 units, -Delta)
   BwdSchedule* sched;
   int4* items;
   size_t total;
