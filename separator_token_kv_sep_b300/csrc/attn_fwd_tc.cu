@@ -33,24 +33,6 @@ namespace {
 
 constexpr int kChunk = 128 * 128;  // bytes of a [128 rows x 64 cols] bf16 block
 
-template <int D, int NS, int NST>
-struct FwdCfg {
-  static constexpr int DCH = D / 64;
-  static constexpr int TILE = DCH * kChunk;  // one [128 x D] bf16 tile
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + TILE;
-  static constexpr int OFF_V = OFF_K + NST * TILE;
-  static constexpr int OFF_P = OFF_V + NST * TILE;
-  static constexpr int SMEM = OFF_P + 2 * kChunk + 1024;
-  static constexpr int TM_O = NS * 128;
-  static constexpr int TM_USED = NS * 128 + D;
-  static constexpr int TM_COLS = TM_USED <= 256 ? 256 : 512;
-  static_assert(SMEM <= 227 * 1024, "shared memory");
-};
-
-constexpr int kThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
-constexpr float kRescaleLog2 = 8.0f;
-
 template <int D>
 __global__ void __launch_bounds__(256)
     gather_keep_kernel(IndexPtrs idx, const uint4* __restrict__ k, const uint4* __restrict__ v,
@@ -83,7 +65,43 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-template <int D, int NS, int NST>
+template <int D, int NST>
+struct FwdCfg {
+  static constexpr int DCH = D / 64;
+  static constexpr int TILE = DCH * kChunk;  // one [128 x D] bf16 tile
+  static constexpr int OFF_Q = 0;            // [2] query tiles A, B
+  static constexpr int OFF_K = OFF_Q + 2 * TILE;
+  static constexpr int OFF_V = OFF_K + NST * TILE;
+  static constexpr int SMEM = OFF_V + NST * TILE + 1024;
+  // tensor memory: per query tile X, S (fp32, 128 columns; P overwrites its
+  // first 64 columns as packed bf16) and the O accumulator (D columns)
+  static constexpr int TM_S0 = 0, TM_O0 = 128, TM_S1 = 256, TM_O1 = 384;
+  static constexpr int TM_COLS = 512;
+  static_assert(SMEM <= 227 * 1024, "shared memory");
+};
+
+constexpr int kThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-5 softmax A, 6-9 softmax B
+constexpr float kRescaleLog2 = 8.0f;
+
+// The key tiles one CTA visits for its query tiles A = 2p and B = 2p + 1, in
+// order: the gathered keep tiles of the longer gathered list, then the dense
+// band from A's window start to B's last row.  Tile u is active for X when it
+// holds keys X can see: gathered tile u when 128u < n_gather(X); a band tile
+// for A below A's last row, for B when it reaches past B's window start.
+struct PairPlan {
+  int nA, loA, hiA, nB, loB, hiB;  // block records of A and B
+  bool hasB;
+  int nG, nT;  // gathered tiles, total tiles
+  __device__ bool active(int u, int x) const {
+    if (x == 1 && !hasB) return false;
+    if (u < nG) return 128 * u < (x == 0 ? nA : nB);
+    const int jt = loA + 128 * (u - nG);
+    return x == 0 ? jt < hiA : (jt + 128 > loB && jt < hiB);
+  }
+  __device__ bool any(int u) const { return active(u, 0) || active(u, 1); }
+};
+
+template <int D, int NST>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
@@ -92,52 +110,59 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tm_vk, IndexPtrs idx,
                        __nv_bfloat16* __restrict__ o, float* __restrict__ lse, int B, int Hq,
                        int Hkv, int L, float scale_log2, int* status) {
-  using C = FwdCfg<D, NS, NST>;
+  using C = FwdCfg<D, NST>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  __shared__ __align__(8) uint64_t q_full, p_full, pv_done, mma_final;
-  __shared__ __align__(8) uint64_t k_full[NST], v_full[NST], kv_empty[NST], s_full[NS];
+  __shared__ __align__(8) uint64_t q_full, kv_full[NST], kv_empty[NST], s_full[2], p_full[2],
+      o_done[2], mma_final;
   __shared__ uint32_t tmem_slot;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = (L + 127) >> 7;
-  const int t = T - 1 - static_cast<int>(blockIdx.x);  // longest tiles first
+  const int P = (T + 1) >> 1;
+  const int pair = P - 1 - static_cast<int>(blockIdx.x);  // longest first
   const int h = blockIdx.y, b = blockIdx.z;
   const int g = h / (Hq / Hkv);
-  const int q0 = t * 128;
+  const int tA = 2 * pair;
 
   const IndexHeader hdr = *idx.header;
   if (hdr.magic != kIndexMagic || hdr.B != B || hdr.L != L || hdr.block_m != 128) {
     if (threadIdx.x == 0) report(status, SEP_ERR_DEVICE_BOUNDS);
     return;
   }
-  const int4 blk = *reinterpret_cast<const int4*>(idx.blocks + ((size_t)b * T + t) * 4);
-  const int n_gather = blk.x, lo = blk.y, hi = blk.z;
-  if (n_gather < 0 || n_gather > lo || lo < 0 || lo > q0 || hi <= q0 || hi > L) {
-    if (threadIdx.x == 0) report(status, SEP_ERR_DEVICE_BOUNDS);
-    return;
+  PairPlan pl;
+  pl.hasB = tA + 1 < T;
+  {
+    const int4 ba = *reinterpret_cast<const int4*>(idx.blocks + ((size_t)b * T + tA) * 4);
+    const int4 bb = pl.hasB ? *reinterpret_cast<const int4*>(idx.blocks + ((size_t)b * T + tA + 1) * 4)
+                            : ba;
+    pl.nA = ba.x; pl.loA = ba.y; pl.hiA = ba.z;
+    pl.nB = bb.x; pl.loB = bb.y; pl.hiB = bb.z;
+    auto bad = [&](int4 r, int q0) {
+      return r.x < 0 || r.x > r.y || r.y < 0 || r.y > q0 || r.z <= q0 || r.z > L;
+    };
+    if (bad(ba, tA * 128) || (pl.hasB && (bad(bb, tA * 128 + 128) || bb.x < ba.x || bb.y < ba.y))) {
+      if (threadIdx.x == 0) report(status, SEP_ERR_DEVICE_BOUNDS);
+      return;
+    }
+    pl.nG = ((pl.hasB ? pl.nB : pl.nA) + 127) >> 7;
+    pl.nT = pl.nG + (((pl.hasB ? pl.hiB : pl.hiA) - pl.loA + 127) >> 7);
   }
-  const int nG = (n_gather + 127) >> 7;
-  const int nT = nG + ((hi - lo + 127) >> 7);
   const int n_win = hdr.n;
-
-  uint8_t* sQ = smem + C::OFF_Q;
-  uint8_t* sK = smem + C::OFF_K;
-  uint8_t* sV = smem + C::OFF_V;
-  uint8_t* sP = smem + C::OFF_P;
 
   if (threadIdx.x == 0) {
     mbar_init(&q_full, 1);
-    mbar_init(&p_full, 128);
-    mbar_init(&pv_done, 1);
-    mbar_init(&mma_final, 1);
     for (int s = 0; s < NST; ++s) {
-      mbar_init(&k_full[s], 1);
-      mbar_init(&v_full[s], 1);
+      mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
-    for (int s = 0; s < NS; ++s) mbar_init(&s_full[s], 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&s_full[x], 1);
+      mbar_init(&p_full[x], 128);
+      mbar_init(&o_done[x], 1);
+    }
+    mbar_init(&mma_final, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -156,36 +181,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       const int plane_q = b * Hq + h, plane_kv = b * Hkv + g;
-      mbar_arrive_expect_tx(&q_full, C::TILE);
-      for (int c = 0; c < C::DCH; ++c)
-        tma_load_3d(sQ + c * kChunk, &tm_q, &q_full, 64 * c, q0, plane_q);
-      int issued = 0;
+      mbar_arrive_expect_tx(&q_full, (pl.hasB ? 2 : 1) * C::TILE);
+      for (int x = 0; x < (pl.hasB ? 2 : 1); ++x)
+        for (int c = 0; c < C::DCH; ++c)
+          tma_load_3d(smem + C::OFF_Q + x * C::TILE + c * kChunk, &tm_q, &q_full, 64 * c,
+                      (tA + x) * 128, plane_q);
+      int n = 0;
       bool ok = true;
-      for (int u = 0; u < nT; ++u) {
-        const int st = u % NST;
-        if (u >= NST && !mbar_wait(&kv_empty[st], ((u / NST) - 1) & 1, status)) {
+      for (int u = 0; u < pl.nT; ++u) {
+        if (!pl.any(u)) continue;
+        const int st = n % NST;
+        if (n >= NST && !mbar_wait(&kv_empty[st], ((n / NST) - 1) & 1, status)) {
           ok = false;
           break;
         }
-        const bool gat = u < nG;
+        const bool gat = u < pl.nG;
         const CUtensorMap* mk = gat ? &tm_kk : &tm_k;
         const CUtensorMap* mv = gat ? &tm_vk : &tm_v;
-        const int row = gat ? 128 * u : lo + 128 * (u - nG);
-        mbar_arrive_expect_tx(&k_full[st], C::TILE);
-        for (int c = 0; c < C::DCH; ++c)
-          tma_load_3d(sK + st * C::TILE + c * kChunk, mk, &k_full[st], 64 * c, row, plane_kv);
-        mbar_arrive_expect_tx(&v_full[st], C::TILE);
-        for (int c = 0; c < C::DCH; ++c)
-          tma_load_3d(sV + st * C::TILE + c * kChunk, mv, &v_full[st], 64 * c, row, plane_kv);
-        issued = u + 1;
+        const int row = gat ? 128 * u : pl.loA + 128 * (u - pl.nG);
+        mbar_arrive_expect_tx(&kv_full[st], 2 * C::TILE);
+        for (int c = 0; c < C::DCH; ++c) {
+          tma_load_3d(smem + C::OFF_K + st * C::TILE + c * kChunk, mk, &kv_full[st], 64 * c, row,
+                      plane_kv);
+          tma_load_3d(smem + C::OFF_V + st * C::TILE + c * kChunk, mv, &kv_full[st], 64 * c, row,
+                      plane_kv);
+        }
+        ++n;
       }
       if (!ok) {
-        // drain the copies still in flight before the CTA's smem goes away
-        for (int u = issued - NST; u < issued; ++u) {
-          if (u < 0) continue;
-          mbar_wait(&k_full[u % NST], (u / NST) & 1, status);
-          mbar_wait(&v_full[u % NST], (u / NST) & 1, status);
-        }
+        // let the copies still in flight land before the CTA's smem goes away
+        for (int x = n - NST; x < n; ++x)
+          if (x >= 0) mbar_wait(&kv_full[x % NST], (x / NST) & 1, status);
         mbar_wait(&q_full, 0, status);
       }
     }
@@ -194,46 +220,68 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
-      const uint32_t q_base = smem_u32(sQ), k_base = smem_u32(sK), v_base = smem_u32(sV),
-                     p_base = smem_u32(sP);
+      const uint32_t k_base = smem_u32(smem + C::OFF_K), v_base = smem_u32(smem + C::OFF_V);
+      int cnt0 = 0, cnt1 = 0;  // P.V products issued per query tile
       bool ok = mbar_wait(&q_full, 0, status);
       tc_fence_after();
-      auto issue_qk = [&](int u) -> bool {
-        const int st = u % NST;
-        if (!mbar_wait(&k_full[st], (u / NST) & 1, status)) return false;
-        tc_fence_after();
-        const uint32_t d_tm = tmem + 128 * (u % NS);
+      auto issue_qk = [&](int x, int st) {
+        const uint32_t q_base = smem_u32(smem + C::OFF_Q + x * C::TILE);
+        const uint32_t d_s = tmem + (x ? C::TM_S1 : C::TM_S0);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
-          umma_bf16_ss(d_tm, sdesc_sw128(q_base + off, 16, 1024),
+          umma_bf16_ss(d_s, sdesc_sw128(q_base + off, 16, 1024),
                        sdesc_sw128(k_base + st * C::TILE + off, 16, 1024), idesc_qk, kk > 0);
         }
-        umma_commit(&s_full[u % NS]);
-        return true;
+        umma_commit(&s_full[x]);
       };
-      auto issue_pv = [&](int u) -> bool {
-        const int st = u % NST;
-        if (!mbar_wait(&p_full, u & 1, status)) return false;
-        if (!mbar_wait(&v_full[st], (u / NST) & 1, status)) return false;
+      auto issue_pv = [&](int x, int st) -> bool {  // O_x (+)= P_x V, P_x from TMEM
+        int& cx = x ? cnt1 : cnt0;
+        if (!mbar_wait(&p_full[x], cx & 1, status)) return false;
         tc_fence_after();
+        const uint32_t a_p = tmem + (x ? C::TM_S1 : C::TM_S0);
+        const uint32_t d_o = tmem + (x ? C::TM_O1 : C::TM_O0);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t aoff = (kk >> 2) * kChunk + (kk & 3) * 32;
-          umma_bf16_ss(tmem + C::TM_O, sdesc_sw128(p_base + aoff, 16, 1024),
+        for (int kk = 0; kk < 8; ++kk)
+          umma_bf16_ts(d_o, a_p + 8 * kk,
                        sdesc_sw128(v_base + st * C::TILE + kk * 2048, kChunk, 1024), idesc_pv,
-                       (u > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(&pv_done);
-        umma_commit(&kv_empty[st]);
+                       (cx > 0 || kk > 0) ? 1u : 0u);
+        ++cx;
         return true;
       };
-      if (ok) ok = issue_qk(0);
-      for (int u = 0; ok && u < nT; ++u) {
-        if (NS == 2 && u + 1 < nT) ok = issue_qk(u + 1);
-        if (ok) ok = issue_pv(u);
-        if (ok && NS == 1 && u + 1 < nT) ok = issue_qk(u + 1);
+      // first active tile: both S products
+      int u = 0, n = 0;
+      while (u < pl.nT && !pl.any(u)) ++u;
+      if (ok && u < pl.nT) {
+        ok = mbar_wait(&kv_full[0], 0, status);
+        tc_fence_after();
+        if (ok) {
+          if (pl.active(u, 0)) issue_qk(0, 0);
+          if (pl.active(u, 1)) issue_qk(1, 0);
+        }
       }
+      while (ok && u < pl.nT) {
+        const int st = n % NST;
+        int un = u + 1;
+        while (un < pl.nT && !pl.any(un)) ++un;
+        const int stn = (n + 1) % NST;
+        const bool has_next = un < pl.nT;
+        // A: P.V of this tile, then S of the next (S_A / P_A share TMEM, and
+        // the tensor pipe runs these in issue order)
+        if (pl.active(u, 0) && !(ok = issue_pv(0, st))) break;
+        if (has_next) {
+          if (!(ok = mbar_wait(&kv_full[stn], ((n + 1) / NST) & 1, status))) break;
+          tc_fence_after();
+          if (pl.active(un, 0)) issue_qk(0, stn);
+        }
+        if (pl.active(u, 1) && !(ok = issue_pv(1, st))) break;
+        umma_commit(&kv_empty[st]);  // every MMA reading this K/V stage is issued
+        if (has_next && pl.active(un, 1)) issue_qk(1, stn);
+        u = un;
+        ++n;
+      }
+      umma_commit(&o_done[0]);
+      umma_commit(&o_done[1]);
       // every MMA issued by this thread completes before TMEM is released
       umma_commit(&mma_final);
       mbar_wait(&mma_final, 0, status);
@@ -241,135 +289,150 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
+    const int x = (warp - 2) >> 2;  // query tile: 0 = A, 1 = B
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
-    const int i = q0 + r;
+    const int i = (tA + x) * 128 + r;
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t tS = tmem + lane_base + (x ? C::TM_S1 : C::TM_S0);
+    const uint32_t tO = tmem + lane_base + (x ? C::TM_O1 : C::TM_O0);
     const uint32_t* kbits = idx.keep_bits + (size_t)b * hdr.nwords;
     const int nwords = hdr.nwords;
+    const int n_gath = x ? pl.nB : pl.nA;
+    const int lo_x = x ? pl.loB : pl.loA;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
-    uint32_t sr[128];
-    for (int u = 0; u < nT; ++u) {
-      const int sb = u % NS;
-      if (!mbar_wait(&s_full[sb], (u / NS) & 1, status)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
+    int cnt = 0;
+    if (x == 0 || pl.hasB) {
+      for (int u = 0; u < pl.nT; ++u) {
+        if (!pl.active(u, x)) continue;
+        // visibility of the 128 columns as 4 words
+        uint32_t vm[4];
+        if (u < pl.nG) {
+          const int nv = min(128, n_gath - 128 * u);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_base + 128 * sb + 32 * c, sr + 32 * c);
-      tmem_ld_wait();
-
-      // visibility of the 128 columns as 4 words
-      uint32_t vm[4];
-      if (u < nG) {
-        const int nv = min(128, n_gather - 128 * u);
+          for (int w = 0; w < 4; ++w) {
+            const int c = nv - 32 * w;
+            vm[w] = c >= 32 ? 0xffffffffu : (c <= 0 ? 0u : ((1u << c) - 1u));
+          }
+        } else {
+          const int jt = pl.loA + 128 * (u - pl.nG);
+          const int n_causal = min(128, max(0, i - jt + 1));  // columns c with jt+c <= i
+          const int c_win = i - n_win + 1 - jt;               // columns c >= c_win: window
+          const int c_lo = lo_x - jt;                         // columns below it: gathered
+          const int wj = jt >> 5, sh = jt & 31;
+          uint32_t kw[5];
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const int c = nv - 32 * w;
-          vm[w] = c >= 32 ? 0xffffffffu : (c <= 0 ? 0u : ((1u << c) - 1u));
+          for (int q = 0; q < 5; ++q) kw[q] = (wj + q < nwords) ? __ldg(kbits + wj + q) : 0u;
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const uint32_t keepw = sh ? ((kw[w] >> sh) | (kw[w + 1] << (32 - sh))) : kw[w];
+            const int cc = n_causal - 32 * w;
+            const uint32_t causal = cc >= 32 ? 0xffffffffu : (cc <= 0 ? 0u : ((1u << cc) - 1u));
+            const int cw = c_win - 32 * w;
+            const uint32_t win = cw <= 0 ? 0xffffffffu : (cw >= 32 ? 0u : ~((1u << cw) - 1u));
+            const int cl = c_lo - 32 * w;
+            const uint32_t above = cl <= 0 ? 0xffffffffu : (cl >= 32 ? 0u : ~((1u << cl) - 1u));
+            vm[w] = causal & above & (win | keepw);
+          }
         }
-      } else {
-        const int jt = lo + 128 * (u - nG);
-        const int n_causal = min(128, max(0, i - jt + 1));  // columns c with jt+c <= i
-        const int c_win = i - n_win + 1 - jt;               // columns c >= c_win are in the window
-        const int wj = jt >> 5, sh = jt & 31;
-        uint32_t kw[5];
-#pragma unroll
-        for (int x = 0; x < 5; ++x) kw[x] = (wj + x < nwords) ? __ldg(kbits + wj + x) : 0u;
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const uint32_t keepw = sh ? ((kw[w] >> sh) | (kw[w + 1] << (32 - sh))) : kw[w];
-          const int cc = n_causal - 32 * w;
-          const uint32_t causal = cc >= 32 ? 0xffffffffu : (cc <= 0 ? 0u : ((1u << cc) - 1u));
-          const int cw = c_win - 32 * w;  // bits >= cw
-          const uint32_t win = cw <= 0 ? 0xffffffffu : (cw >= 32 ? 0u : ~((1u << cw) - 1u));
-          vm[w] = causal & (win | keepw);
-        }
-      }
-      float mt = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        const float x = ((vm[c >> 5] >> (c & 31)) & 1u) ? __uint_as_float(sr[c]) * scale_log2
-                                                         : -INFINITY;
-        sr[c] = __float_as_uint(x);
-        mt = fmaxf(mt, x);
-      }
-      const float m_new = fmaxf(m_used, mt);
-      const bool rescale = m_new > m_used + kRescaleLog2;
-      float alpha = 1.f;
-      if (rescale) {
-        alpha = fast_exp2(m_used - m_new);
-        m_used = m_new;
-      }
-      const float msub = (m_used == -INFINITY) ? 0.f : m_used;
-      float rs = 0.f;
-#pragma unroll
-      for (int c = 0; c < 128; c += 2) {
-        const float p0 = fast_exp2(__uint_as_float(sr[c]) - msub);
-        const float p1 = fast_exp2(__uint_as_float(sr[c + 1]) - msub);
-        rs += p0 + p1;
-        sr[c >> 1] = pack_bf16x2(p0, p1);
-      }
-      l = l * alpha + rs;
-
-      if (u > 0) {
-        if (!mbar_wait(&pv_done, (u - 1) & 1, status)) {
+        if (!mbar_wait(&s_full[x], cnt & 1, status)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, rescale)) {
+        // pass 1: the row maximum over the visible columns (S read in two
+        // halves to keep registers for the second pass)
+        float mt = -INFINITY;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t sr[64];
+          tmem_ld32(tS + 64 * hf, sr);
+          tmem_ld32(tS + 64 * hf + 32, sr + 32);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            const int cc = 64 * hf + c;
+            if ((vm[cc >> 5] >> (cc & 31)) & 1u) mt = fmaxf(mt, __uint_as_float(sr[c]));
+          }
+        }
+        mt *= scale_log2;  // scale_log2 > 0 keeps the maximum where it is
+        const float m_new = fmaxf(m_used, mt);
+        const bool rescale = m_new > m_used + kRescaleLog2;
+        float alpha = 1.f;
+        if (rescale) {
+          alpha = fast_exp2(m_used - m_new);
+          m_used = m_new;
+        }
+        const float msub = (m_used == -INFINITY) ? 0.f : m_used;
+        // O rescale: S of this tile being ready means the previous P.V of
+        // this query tile has completed (the tensor pipe runs in order)
+        if (cnt > 0 && __any_sync(0xffffffffu, rescale)) {
           uint32_t ob[32];
 #pragma unroll
           for (int c0 = 0; c0 < D; c0 += 32) {
-            tmem_ld32(tmem + lane_base + C::TM_O + c0, ob);
+            tmem_ld32(tO + c0, ob);
             tmem_ld_wait();
 #pragma unroll
-            for (int x = 0; x < 32; ++x) ob[x] = __float_as_uint(__uint_as_float(ob[x]) * alpha);
-            tmem_st32(tmem + lane_base + C::TM_O + c0, ob);
-          }
-          tmem_st_wait();
-        }
-      }
-      // P row -> shared memory, 128-byte swizzle, two 64-key blocks
-#pragma unroll
-      for (int un = 0; un < 16; ++un) {
-        const uint32_t off = (un >> 3) * kChunk + sw128_offset(r, (un & 7) * 8);
-        *reinterpret_cast<uint4*>(sP + off) =
-            make_uint4(sr[4 * un], sr[4 * un + 1], sr[4 * un + 2], sr[4 * un + 3]);
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&p_full);
-    }
-    if (ok && mbar_wait(&pv_done, (nT - 1) & 1, status)) {
-      tc_fence_after();
-      const float inv_l = 1.f / l;
-      uint32_t ob[32];
-      __nv_bfloat16* orow = o + (((size_t)b * Hq + h) * L + i) * D;
-#pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        tmem_ld32(tmem + lane_base + C::TM_O + c0, ob);
-        tmem_ld_wait();
-        if (i < L) {
-#pragma unroll
-          for (int x = 0; x < 32; x += 8) {
-            uint4 pk;
-            pk.x = pack_bf16x2(__uint_as_float(ob[x]) * inv_l, __uint_as_float(ob[x + 1]) * inv_l);
-            pk.y = pack_bf16x2(__uint_as_float(ob[x + 2]) * inv_l,
-                               __uint_as_float(ob[x + 3]) * inv_l);
-            pk.z = pack_bf16x2(__uint_as_float(ob[x + 4]) * inv_l,
-                               __uint_as_float(ob[x + 5]) * inv_l);
-            pk.w = pack_bf16x2(__uint_as_float(ob[x + 6]) * inv_l,
-                               __uint_as_float(ob[x + 7]) * inv_l);
-            *reinterpret_cast<uint4*>(orow + c0 + x) = pk;
+            for (int q = 0; q < 32; ++q) ob[q] = __float_as_uint(__uint_as_float(ob[q]) * alpha);
+            tmem_st32(tO + c0, ob);
           }
         }
+        // pass 2: P = exp2(S * scale - m) as packed bf16, written over the
+        // first 64 columns of S chunk by chunk (chunk c's P lands on S
+        // columns [16c, 16c+16), all of which have been read by then)
+        float rs = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t sr[32], pk[16];
+          tmem_ld32(tS + 32 * c, sr);
+          tmem_ld_wait();
+          const uint32_t w = c == 0 ? vm[0] : c == 1 ? vm[1] : c == 2 ? vm[2] : vm[3];
+#pragma unroll
+          for (int q = 0; q < 32; q += 2) {
+            float a0, a1;
+            ffma2(a0, a1, __uint_as_float(sr[q]), __uint_as_float(sr[q + 1]), scale_log2,
+                  scale_log2, -msub, -msub);
+            float p0 = fast_exp2(a0), p1 = fast_exp2(a1);
+            p0 = ((w >> q) & 1u) ? p0 : 0.f;
+            p1 = ((w >> (q + 1)) & 1u) ? p1 : 0.f;
+            rs += p0 + p1;
+            pk[q >> 1] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16(tS + 16 * c, pk);
+        }
+        l = l * alpha + rs;
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&p_full[x]);
+        ++cnt;
       }
-      if (i < L)
-        lse[((size_t)b * Hq + h) * L + i] = (m_used + __log2f(l)) * 0.69314718055994531f;
+      if (ok && mbar_wait(&o_done[x], 0, status)) {
+        tc_fence_after();
+        const float inv_l = 1.f / l;
+        uint32_t ob[32];
+        __nv_bfloat16* orow = o + (((size_t)b * Hq + h) * L + i) * D;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          tmem_ld32(tO + c0, ob);
+          tmem_ld_wait();
+          if (i < L) {
+#pragma unroll
+            for (int q = 0; q < 32; q += 8) {
+              uint4 pk;
+              pk.x = pack_bf16x2(__uint_as_float(ob[q]) * inv_l, __uint_as_float(ob[q + 1]) * inv_l);
+              pk.y = pack_bf16x2(__uint_as_float(ob[q + 2]) * inv_l,
+                                 __uint_as_float(ob[q + 3]) * inv_l);
+              pk.z = pack_bf16x2(__uint_as_float(ob[q + 4]) * inv_l,
+                                 __uint_as_float(ob[q + 5]) * inv_l);
+              pk.w = pack_bf16x2(__uint_as_float(ob[q + 6]) * inv_l,
+                                 __uint_as_float(ob[q + 7]) * inv_l);
+              *reinterpret_cast<uint4*>(orow + c0 + q) = pk;
+            }
+          }
+        }
+        if (i < L) lse[((size_t)b * Hq + h) * L + i] = (m_used + __log2f(l)) * 0.69314718055994531f;
+      }
     }
   }
 
@@ -379,11 +442,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, C::TM_COLS);
 }
 
-template <int D, int NS, int NST>
+template <int D, int NST>
 int launch_fwd_impl(IndexPtrs idx, const void* q, const void* k, const void* v, void* o, float* lse,
                     int B, int Hq, int Hkv, int L, float scale, void* ws, int* status,
                     cudaStream_t s) {
-  using C = FwdCfg<D, NS, NST>;
+  using C = FwdCfg<D, NST>;
   const size_t plane_elems = (size_t)L * D;
   uint8_t* kk = static_cast<uint8_t*>(ws);
   uint8_t* vk = kk + align_up((size_t)B * Hkv * plane_elems * 2, 256);
@@ -400,11 +463,12 @@ int launch_fwd_impl(IndexPtrs idx, const void* q, const void* k, const void* v, 
       !make_bf16_map(&mkk, kk, (uint64_t)B * Hkv, L, D, 128) ||
       !make_bf16_map(&mvk, vk, (uint64_t)B * Hkv, L, D, 128))
     return static_cast<int>(cudaErrorInvalidValue);
-  auto kern = attn_fwd_tc_kernel<D, NS, NST>;
+  auto kern = attn_fwd_tc_kernel<D, NST>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return static_cast<int>(e);
   const float scale_log2 = scale * 1.4426950408889634f;
-  dim3 grid((L + 127) / 128, Hq, B);
+  const int T = (L + 127) / 128;
+  dim3 grid((T + 1) / 2, Hq, B);  // one CTA per pair of query tiles
   profile_mark(1, s);
   kern<<<grid, kThreads, C::SMEM, s>>>(mq, mk, mv, mkk, mvk, idx,
                                        static_cast<__nv_bfloat16*>(o), lse, B, Hq, Hkv, L,
@@ -424,9 +488,9 @@ int launch_attn_fwd_tc(IndexPtrs idx, const void* q, const void* k, const void* 
                        float* lse, int B, int Hq, int Hkv, int L, int d, float scale, void* ws,
                        int* status, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (d == 64) return launch_fwd_impl<64, 2, 3>(idx, q, k, v, o, lse, B, Hq, Hkv, L, scale, ws,
-                                                status, s);
-  return launch_fwd_impl<128, 2, 2>(idx, q, k, v, o, lse, B, Hq, Hkv, L, scale, ws, status, s);
+  if (d == 64) return launch_fwd_impl<64, 4>(idx, q, k, v, o, lse, B, Hq, Hkv, L, scale, ws,
+                                             status, s);
+  return launch_fwd_impl<128, 2>(idx, q, k, v, o, lse, B, Hq, Hkv, L, scale, ws, status, s);
 }
 
 }  // namespace sep
