@@ -303,16 +303,16 @@ struct KvCfg {
   static constexpr int DCH = D / 64;
   static constexpr int TILE = DCH * kChunk;
   static constexpr int KVB = D == 64 ? 2 : 1;   // K/V tile buffers
-  static constexpr int NST = D == 64 ? 2 : 1;   // Q/dO ring stages
+  static constexpr int NST = D == 64 ? 3 : 2;   // Q/dO ring stages
   static constexpr int ACB = D == 64 ? 2 : 1;   // dK/dV accumulator buffers in TMEM
   static constexpr int OFF_KV = 0;              // [KVB][K, V]
   static constexpr int OFF_Q = OFF_KV + KVB * 2 * TILE;
   static constexpr int OFF_DO = OFF_Q + NST * TILE;
-  static constexpr int OFF_P = OFF_DO + NST * TILE;
-  static constexpr int OFF_DS = OFF_P + 2 * kChunk;
-  static constexpr int OFF_STAT = OFF_DS + 2 * kChunk;  // [NST][128] (-LSE log2, -Delta)
+  static constexpr int OFF_STAT = OFF_DO + NST * TILE;  // [NST][128] (-LSE log2, -Delta)
   static constexpr int SMEM = OFF_STAT + NST * 128 * 8 + 1024;
-  static constexpr int TM_S = 0, TM_DP = 128, TM_ACC = 256;  // acc b: dV at +2bD, dK at +2bD+D
+  // TMEM: half-tile buffers h = 0, 1 at 128h (S^T / P^T, then dP^T / dS^T at
+  // +64); accumulator buffer b: dV at TM_ACC + 2bD, dK at TM_ACC + 2bD + D
+  static constexpr int TM_ACC = 256;
   static constexpr int TM_COLS = 512;
   static_assert(SMEM <= 227 * 1024, "shared memory");
   static_assert(TM_ACC + ACB * 2 * D <= TM_COLS, "tensor memory");
@@ -337,8 +337,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   __shared__ __align__(8) uint64_t kv_full[KVB], kv_empty[KVB], qd_full[NST], qd_empty[NST];
-  __shared__ __align__(8) uint64_t sd_full, sd_free, ps_full, pd_done, acc_full[ACB],
-      acc_empty[ACB], mma_final;
+  __shared__ __align__(8) uint64_t sd_full[2], ps_full[2], acc_full[ACB], acc_empty[ACB],
+      mma_final;
   __shared__ uint32_t tmem_slot;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -370,10 +370,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], kEwThreads);
     }
-    mbar_init(&sd_full, 1);
-    mbar_init(&sd_free, kEwThreads);
-    mbar_init(&ps_full, kEwThreads);
-    mbar_init(&pd_done, 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&sd_full[x], 1);
+      mbar_init(&ps_full[x], 128);
+    }
     mbar_init(&mma_final, 1);
     fence_mbar_init();
   }
@@ -459,96 +459,115 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // The unit of work is a half-tile: the 64 query columns h of one query
+    // tile u against the item's 128 keys.  Half h lives in TMEM buffer h:
+    // S^T at columns [128h, 128h+64), dP^T at [128h+64, 128h+128); the
+    // elementwise warpgroup h overwrites them with P^T and dS^T (packed
+    // bf16), which the dV / dK products then read from TMEM.  Order:
+    // S/dP(u,0), S/dP(u,1), then per half-tile j: dV/dK(j), S/dP(j+2) --
+    // the two warpgroups' chains interleave on the tensor pipe.
     if (lane == 0) {
-      constexpr uint32_t idesc_ss = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idesc_sd = idesc_bf16_f32(128, 64, false, false);
       constexpr uint32_t idesc_acc = idesc_bf16_f32(128, D, false, true);
-      const uint32_t q_base = smem_u32(smem + C::OFF_Q), do_base = smem_u32(smem + C::OFF_DO),
-                     p_base = smem_u32(smem + C::OFF_P), ds_base = smem_u32(smem + C::OFF_DS);
-      int k = 0, ug = 0;
+      const uint32_t q_base = smem_u32(smem + C::OFF_Q), do_base = smem_u32(smem + C::OFF_DO);
+      // a cursor over the CTA's half-tiles: item i (k-th of this CTA), query
+      // iteration u (global count ug), half h
+      struct Cur {
+        int i, k, u, ug, h, nU;
+        Item it;
+      };
+      auto cur_load = [&](Cur& c) {
+        if (c.i < n_items) {
+          c.it = item_at(c.i);
+          c.nU = G * c.it.nt;
+        }
+      };
+      auto cur_next = [&](Cur& c) {
+        if (++c.h < 2) return;
+        c.h = 0;
+        ++c.ug;
+        if (++c.u < c.nU) return;
+        c.u = 0;
+        c.i += gridDim.x;
+        ++c.k;
+        cur_load(c);
+      };
+      // descriptors of the operand bases, advanced by constant offsets
+      const uint64_t dsc_kv = sdesc_sw128(smem_u32(smem + C::OFF_KV), 16, 1024);
+      const uint64_t dsc_q = sdesc_sw128(q_base, 16, 1024);
+      const uint64_t dsc_do = sdesc_sw128(do_base, 16, 1024);
+      const uint64_t dsc_q_mn = sdesc_sw128(q_base, kChunk, 1024);
+      const uint64_t dsc_do_mn = sdesc_sw128(do_base, kChunk, 1024);
+      auto issue_sd = [&](const Cur& c) -> bool {  // S^T / dP^T of half-tile c
+        const int kb = c.k % KVB, st = c.ug % NST;
+        if (c.u == 0 && c.h == 0) {
+          if (!mbar_wait(&kv_full[kb], (c.k / KVB) & 1, status)) return false;
+        }
+        if (c.h == 0) {
+          if (!mbar_wait(&qd_full[st], (c.ug / NST) & 1, status)) return false;
+        }
+        tc_fence_after();
+        const uint64_t dk = dsc_kv + ((kb * 2 * C::TILE) >> 4), dv = dk + (C::TILE >> 4);
+        const uint64_t qo = (st * C::TILE + 8192 * c.h) >> 4;  // query rows 64h .. 64h+63
+        const uint64_t dq = dsc_q + qo, ddo = dsc_do + qo;
+        const uint32_t tb = tmem + 128 * c.h;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * kChunk + (kk & 3) * 32) >> 4;
+          umma_bf16_ss(tb, dk + off, dq + off, idesc_sd, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * kChunk + (kk & 3) * 32) >> 4;
+          umma_bf16_ss(tb + 64, dv + off, ddo + off, idesc_sd, kk > 0);
+        }
+        umma_commit(&sd_full[c.h]);
+        return true;
+      };
+      Cur cs{static_cast<int>(blockIdx.x), 0, 0, 0, 0, 0, Item{}};  // next S/dP to issue
+      cur_load(cs);
+      Cur ca = cs;  // next dV/dK to issue
       bool ok = true;
-      for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x, ++k) {
-        const Item it = item_at(i);
-        const int kb = k % KVB, ab = k % ACB;
-        const uint32_t k_base = smem_u32(smem + C::OFF_KV + kb * 2 * C::TILE);
-        const uint32_t v_base = k_base + C::TILE;
+      // S/dP run up to two half-tiles ahead of dV/dK, but not into an item
+      // whose K/V buffer the current item still holds
+      int ahead = 0;
+      auto top_up = [&]() -> bool {
+        while (ahead < 2 && cs.i < n_items && cs.k < ca.k + KVB) {
+          if (!issue_sd(cs)) return false;
+          cur_next(cs);
+          ++ahead;
+        }
+        return true;
+      };
+      ok = top_up();
+      while (ok && ca.i < n_items) {
+        const int ab = ca.k % ACB, st = ca.ug % NST, kb = ca.k % KVB;
+        if (ca.u == 0 && ca.h == 0 && ca.k >= ACB) {
+          // the epilogue has drained this accumulator buffer
+          if (!(ok = mbar_wait(&acc_empty[ab], ((ca.k / ACB) - 1) & 1, status))) break;
+        }
+        if (!(ok = mbar_wait(&ps_full[ca.h], ca.ug & 1, status))) break;
+        tc_fence_after();
+        const uint32_t tb = tmem + 128 * ca.h;
         const uint32_t tm_dv = tmem + C::TM_ACC + ab * 2 * D, tm_dk = tm_dv + D;
-        if (!mbar_wait(&kv_full[kb], (k / KVB) & 1, status)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const int nU = G * it.nt;
-        auto issue_sdp = [&](int ugl) -> bool {  // S^T and dP^T of global iteration ugl
-          const int st = ugl % NST;
-          if (!mbar_wait(&qd_full[st], (ugl / NST) & 1, status)) return false;
-          tc_fence_after();
+        const uint64_t qo = (st * C::TILE + 8192 * ca.h) >> 4;
+        const uint64_t ddo = dsc_do_mn + qo, dq = dsc_q_mn + qo;
+        const uint32_t first = (ca.u > 0 || ca.h > 0) ? 1u : 0u;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
-            umma_bf16_ss(tmem + C::TM_S, sdesc_sw128(k_base + off, 16, 1024),
-                         sdesc_sw128(q_base + st * C::TILE + off, 16, 1024), idesc_ss, kk > 0);
-          }
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
-            umma_bf16_ss(tmem + C::TM_DP, sdesc_sw128(v_base + off, 16, 1024),
-                         sdesc_sw128(do_base + st * C::TILE + off, 16, 1024), idesc_ss, kk > 0);
-          }
-          umma_commit(&sd_full);
-          return true;
-        };
-        // S^T / dP^T of the item's first iteration (TMEM S/dP freed by the
-        // elementwise warps of the previous iteration)
-        if (ug > 0 && !mbar_wait(&sd_free, (ug - 1) & 1, status)) {
-          ok = false;
-          break;
+        for (int kk = 0; kk < 4; ++kk) {  // 16 queries per step
+          const uint32_t acc = kk > 0 ? 1u : first;
+          umma_bf16_ts(tm_dv, tb + 8 * kk, ddo + ((kk * 2048) >> 4), idesc_acc, acc);
+          umma_bf16_ts(tm_dk, tb + 64 + 8 * kk, dq + ((kk * 2048) >> 4), idesc_acc, acc);
         }
-        if (!issue_sdp(ug)) {
-          ok = false;
-          break;
+        const bool last_h = ca.h == 1, last_u = ca.u + 1 == ca.nU;
+        if (last_h) umma_commit(&qd_empty[st]);  // Q / dO / stats of this tile are done
+        if (last_h && last_u) {
+          umma_commit(&kv_empty[kb]);  // every MMA reading this item's K and V is issued
+          umma_commit(&acc_full[ab]);
         }
-        // the accumulators of buffer ab must have been drained by the epilogue
-        if (k >= ACB && !mbar_wait(&acc_empty[ab], ((k / ACB) - 1) & 1, status)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        for (int u = 0; ok && u < nU; ++u) {
-          const int ugl = ug + u;
-          // S^T / dP^T of the next iteration go ahead of this iteration's
-          // dV / dK when the Q/dO ring has a second stage; with one stage the
-          // next tile only arrives once this iteration's MMAs release it.
-          if (NST > 1 && u + 1 < nU) {
-            ok = mbar_wait(&sd_free, ugl & 1, status) && issue_sdp(ugl + 1);
-            if (!ok) break;
-          }
-          if (!mbar_wait(&ps_full, ugl & 1, status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const int st = ugl % NST;
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t aoff = (kk >> 2) * kChunk + (kk & 3) * 32;
-            const uint32_t boff = st * C::TILE + kk * 2048;
-            const uint32_t acc = (u > 0 || kk > 0) ? 1u : 0u;
-            umma_bf16_ss(tm_dv, sdesc_sw128(p_base + aoff, 16, 1024),
-                         sdesc_sw128(do_base + boff, kChunk, 1024), idesc_acc, acc);
-            umma_bf16_ss(tm_dk, sdesc_sw128(ds_base + aoff, 16, 1024),
-                         sdesc_sw128(q_base + boff, kChunk, 1024), idesc_acc, acc);
-          }
-          umma_commit(&pd_done);
-          umma_commit(&qd_empty[st]);
-          if (NST == 1 && u + 1 < nU) {
-            ok = mbar_wait(&sd_free, ugl & 1, status) && issue_sdp(ugl + 1);
-            if (!ok) break;
-          }
-        }
-        if (!ok) break;
-        umma_commit(&kv_empty[kb]);  // every MMA reading this item's K and V is issued
-        umma_commit(&acc_full[ab]);
-        ug += nU;
+        cur_next(ca);
+        --ahead;
+        if (!(ok = top_up())) break;
       }
       // every MMA issued by this thread completes before TMEM is released
       umma_commit(&mma_final);
@@ -557,15 +576,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ---------------------------------------------------------- elementwise
-    // Two warpgroups share every tile: warps 2-5 take query columns 0-63 and
-    // warps 6-9 columns 64-127 of the same 128 key rows (warp w reads TMEM
+    // Warpgroup `half` owns query columns [64 half, 64 half + 64) of every
+    // query tile: warps 2-5 half 0, warps 6-9 half 1 (warp w reads TMEM
     // lanes 32*(w%4)..).  In the epilogue the first writes dV, the second dK.
     const int quad = warp & 3;
     const int half = (warp - 2) >> 2;
     const int r = quad * 32 + lane;  // key row of the tile
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-    uint8_t* sP = smem + C::OFF_P;
-    uint8_t* sDS = smem + C::OFF_DS;
+    const uint32_t tb = tmem + lane_base + 128 * half;
     int k = 0, ug = 0;
     bool ok = true;
     for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x, ++k) {
@@ -579,14 +597,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!keep && j < L)
         keep_j = (idx.keep_bits[(size_t)it.b * hdr.nwords + (j >> 5)] >> (j & 31)) & 1u;
       const int nU = G * it.nt;
+      int4 blk_next = *reinterpret_cast<const int4*>(blocks + 4 * it.t0);
       for (int u = 0; u < nU; ++u) {
         const int ugl = ug + u;
         const int t = it.t0 + u % it.nt;
         const int i0 = t * 128;
+        const int4 blk = blk_next;  // loaded one iteration ahead
+        if (u + 1 < nU)
+          blk_next = *reinterpret_cast<const int4*>(blocks + 4 * (it.t0 + (u + 1) % it.nt));
         // visible query columns of this row among the half's 64, as 2 words
         uint32_t vm[2];
         {
-          const int4 blk = *reinterpret_cast<const int4*>(blocks + 4 * t);
           const int c_end = min(128, L - i0);  // query rows past L are padding
           int c_lo = 0, c_hi = 0;
           if (keep) {
@@ -598,7 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           vm[0] = range_bits(c_lo, c_hi, 2 * half);
           vm[1] = range_bits(c_lo, c_hi, 2 * half + 1);
         }
-        if (!mbar_wait(&sd_full, ugl & 1, status)) {
+        if (!mbar_wait(&sd_full[half], ugl & 1, status)) {
           ok = false;
           break;
         }
@@ -611,18 +632,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float4* sst =
             reinterpret_cast<const float4*>(smem + C::OFF_STAT + stg * 1024) + 32 * half;
-        uint32_t pk[32], dk2[32];
-#pragma unroll
+#pragma unroll 1
         for (int cc = 0; cc < 2; ++cc) {
-          uint32_t sr[32], dr[32];
-          tmem_ld32(tmem + lane_base + C::TM_S + 64 * half + 32 * cc, sr);
-          tmem_ld32(tmem + lane_base + C::TM_DP + 64 * half + 32 * cc, dr);
+          uint32_t sr[32], dr[32], pk[16], dk2[16];
+          tmem_ld32(tb + 32 * cc, sr);
+          tmem_ld32(tb + 64 + 32 * cc, dr);
           tmem_ld_wait();
-          const uint32_t w = vm[cc];
+          const uint32_t w = cc ? vm[1] : vm[0];
           const bool full = __all_sync(0xffffffffu, w == 0xffffffffu);
 #pragma unroll
           for (int x = 0; x < 32; x += 2) {
-            const float4 st2 = sst[16 * cc + x / 2];  // columns (x, x+1): (-lse, -delta) pairs
+            const float4 st2 = sst[16 * cc + x / 2];  // columns (x, x+1): (-lse, -delta)
             float a0, a1, d0, d1;
             ffma2(a0, a1, __uint_as_float(sr[x]), __uint_as_float(sr[x + 1]), scale_log2,
                   scale_log2, st2.x, st2.z);
@@ -634,29 +654,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             ffma2(d0, d1, __uint_as_float(dr[x]), __uint_as_float(dr[x + 1]), 1.f, 1.f, st2.y,
                   st2.w);
             fmul2(d0, d1, p0, p1, d0, d1);
-            pk[16 * cc + x / 2] = pack_bf16x2(p0, p1);
-            dk2[16 * cc + x / 2] = pack_bf16x2(d0, d1);
+            pk[x / 2] = pack_bf16x2(p0, p1);
+            dk2[x / 2] = pack_bf16x2(d0, d1);
           }
+          // P^T over S^T, dS^T over dP^T: chunk cc lands on columns
+          // [16cc, 16cc+16) of each, which chunk 0's loads already read
+          tmem_st16(tb + 16 * cc, pk);
+          tmem_st16(tb + 64 + 16 * cc, dk2);
         }
+        tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&sd_free);
-        if (ugl > 0 && !mbar_wait(&pd_done, (ugl - 1) & 1, status)) {
-          ok = false;
-          break;
-        }
-        // this half's 64 query columns are one 64-column block of the
-        // 128-byte-swizzle K-major P^T / dS^T tiles
-#pragma unroll
-        for (int un = 0; un < 8; ++un) {
-          const uint32_t off = half * kChunk + sw128_offset(r, un * 8);
-          *reinterpret_cast<uint4*>(sP + off) =
-              make_uint4(pk[4 * un], pk[4 * un + 1], pk[4 * un + 2], pk[4 * un + 3]);
-          *reinterpret_cast<uint4*>(sDS + off) =
-              make_uint4(dk2[4 * un], dk2[4 * un + 1], dk2[4 * un + 2], dk2[4 * un + 3]);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        mbar_arrive(&ps_full);
+        mbar_arrive(&ps_full[half]);
       }
       if (!ok) break;
       ug += nU;
