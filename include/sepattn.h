@@ -107,6 +107,18 @@ sep_status sep_build_index(const int32_t* ids, int B, int L,
                            int a, int n, int block_m,
                            void* index_buf, size_t index_bytes, void* stream);
 
+/* sep_build_index_fixed -- the index of the FixLLM control: the same
+ * fields and block lists as sep_build_index, with the separators replaced
+ * by one kept token per interval of `delta` positions (anthology record
+ * lit-748, Key takeaways, "What is ablated": FixLLM keeps one token at fixed
+ * intervals instead of separators).  keep[j] = (j < a) or ((j + 1) % delta
+ * == 0); no token ids are read.  sep_attn_fwd / sep_attn_bwd consume the
+ * result unchanged.  delta = 1 keeps every token (full causal attention).
+ * Errors: SEP_ERR_INVALID_ARG (B, L < 1, a < 0, n < 1, delta < 1, null or
+ * misaligned index_buf), SEP_ERR_UNSUPPORTED, SEP_ERR_WORKSPACE, SEP_ERR_CUDA. */
+sep_status sep_build_index_fixed(int B, int L, int a, int n, int delta, int block_m,
+                                 void* index_buf, size_t index_bytes, void* stream);
+
 /* Device pointers to the fields of an index buffer (pure pointer arithmetic,
  * no device access).  Any output pointer may be NULL. */
 sep_status sep_index_views(void* index_buf, int B, int L, int block_m,
@@ -263,6 +275,32 @@ sep_status sep_cache_step(const sep_cache_params* p, void* cache_buf,
                           const int32_t* ids_new, const int32_t* sep_ids,
                           int n_sep_ids, void* out, int Hq, float scale,
                           void* stream);
+
+/* Bytes of the workspace sep_cache_prefill needs for a prompt of T tokens
+ * (0 if the shape is invalid). */
+size_t sep_cache_prefill_workspace_bytes(const sep_cache_params* p, int T);
+
+/* sep_cache_prefill -- append a whole prompt of T tokens to EMPTY caches in
+ * one launch.  The result is the state T update-only sep_cache_step calls
+ * (q = out = NULL) would leave: the same export image, and every later step
+ * gives the same outputs.  Under the update rule of sep_cache_step the
+ * cache holds, in text order, the first a tokens, the newest <= s
+ * separators among the tokens the window has left and the window itself
+ * (pith.science review, key_machinery), so only the window start depends on
+ * the step-by-step history; it is replayed from a separator prefix count.
+ *
+ *   k_prompt, v_prompt [T, S, Hkv, d] bf16 (the T step inputs stacked).
+ *   ids      int32 [T, S] token ids.
+ *   sep_ids  HOST int32 [n_sep_ids].
+ *   ws       device workspace >= sep_cache_prefill_workspace_bytes(p, T),
+ *            256-byte aligned.
+ * Errors: SEP_ERR_INVALID_ARG, SEP_ERR_UNSUPPORTED, SEP_ERR_CAPACITY,
+ * SEP_ERR_WORKSPACE, SEP_ERR_CUDA; device: SEP_ERR_DEVICE_BOUNDS if a cache
+ * is not empty (its counters are left untouched). */
+sep_status sep_cache_prefill(const sep_cache_params* p, void* cache_buf, const void* k_prompt,
+                             const void* v_prompt, const int32_t* ids, int T,
+                             const int32_t* sep_ids, int n_sep_ids, void* ws, size_t ws_bytes,
+                             void* stream);
 
 /* Bytes of the host image written by sep_cache_export. */
 size_t sep_cache_export_bytes(const sep_cache_params* p);

@@ -15,6 +15,8 @@ Modules
 ``sepllm``     separator detection, the SepLLM mask, keep-token compaction,
                per-query-tile block lists, masked softmax attention forward
                and its textbook backward.
+``fixllm``     the FixLLM control (one kept token per fixed interval instead
+               of the separators) on the same mask machinery.
 ``streaming``  the four-block streaming KV cache (initial, separator, past
                window, local window) with eviction into the separator cache,
                position shifting inside the cache, RoPE and decode attention.
@@ -28,4 +30,4 @@ the block-list record format).  Those are marked "parity unpinned" where
 they are defined.
 """
 
-from . import sepllm, streaming  # noqa: F401
+from . import fixllm, sepllm, streaming  # noqa: F401

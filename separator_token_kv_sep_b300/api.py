@@ -32,7 +32,8 @@ EXPORTED = ["sep_index_bytes", "sep_build_index", "sep_index_views",
             "sep_cache_bytes", "sep_cache_init", "sep_cache_step",
             "sep_cache_export_bytes", "sep_cache_export", "sep_cache_import",
             "sep_get_device_status", "sep_status_string", "sep_attn_fwd_static",
-            "sep_profile_events", "sep_selftest_wait_timeout"]
+            "sep_profile_events", "sep_selftest_wait_timeout", "sep_build_index_fixed",
+            "sep_cache_prefill_workspace_bytes", "sep_cache_prefill"]
 
 
 class SepError(RuntimeError):
@@ -73,6 +74,9 @@ def _load() -> ctypes.CDLL:
         "sep_attn_fwd_static": (I, [P, P, P, P, P, P, I, I, I, I, I, F, P]),
         "sep_profile_events": (I, [ctypes.POINTER(ctypes.c_void_p), I]),
         "sep_selftest_wait_timeout": (I, [I, P]),
+        "sep_build_index_fixed": (I, [I, I, I, I, I, I, P, Z, P]),
+        "sep_cache_prefill_workspace_bytes": (Z, [CP, I]),
+        "sep_cache_prefill": (I, [CP, P, P, P, P, I, P, I, P, Z, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -142,6 +146,20 @@ def sep_build_index(ids: torch.Tensor, sep_ids: Sequence[int], a: int, n: int,
     _check(_lib.sep_build_index(_ptr(ids), B, L, arr, n_ids, a, n, block_m,
                                 _ptr(index_buf), index_buf.numel(), _stream(stream)),
            "sep_build_index")
+    return index_buf
+
+
+def sep_build_index_fixed(B: int, L: int, a: int, n: int, delta: int,
+                          block_m: int = SEP_BLOCK_M, index_buf: torch.Tensor | None = None,
+                          device="cuda", stream=None) -> torch.Tensor:
+    """Index of the FixLLM control: keep = first a tokens and every
+    position j with (j + 1) % delta == 0.  Returns the index buffer."""
+    nbytes = sep_index_bytes(B, L, block_m)
+    if index_buf is None:
+        index_buf = _empty_bytes(nbytes, device)
+    _check(_lib.sep_build_index_fixed(B, L, a, n, delta, block_m, _ptr(index_buf),
+                                      index_buf.numel(), _stream(stream)),
+           "sep_build_index_fixed")
     return index_buf
 
 
@@ -269,6 +287,20 @@ def sep_cache_step(p: CacheParams, cache_buf, q, k_new, v_new, ids_new,
                                _ptr(v_new), _ptr(ids_new), arr, n_ids, _ptr(out), hq,
                                float(scale), _stream(stream)), "sep_cache_step")
     return out
+
+
+def sep_cache_prefill(p: CacheParams, cache_buf, k_prompt, v_prompt, ids,
+                      sep_ids: Sequence[int], ws=None, stream=None) -> None:
+    """Append a prompt to empty caches in one launch.  k_prompt / v_prompt
+    [T, S, Hkv, d] bf16, ids int32 [T, S]."""
+    T = k_prompt.shape[0]
+    arr, n_ids = _sep_array(sep_ids)
+    nws = int(_lib.sep_cache_prefill_workspace_bytes(ctypes.byref(p), T))
+    if ws is None:
+        ws = _empty_bytes(nws, k_prompt.device)
+    _check(_lib.sep_cache_prefill(ctypes.byref(p), _ptr(cache_buf), _ptr(k_prompt),
+                                  _ptr(v_prompt), _ptr(ids), T, arr, n_ids, _ptr(ws),
+                                  ws.numel(), _stream(stream)), "sep_cache_prefill")
 
 
 def sep_cache_export_bytes(p: CacheParams) -> int:

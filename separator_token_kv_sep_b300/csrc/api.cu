@@ -97,7 +97,22 @@ SEP_API sep_status sep_build_index(const int32_t* ids, int B, int L, const int32
   if (index_bytes < lay.total) return SEP_ERR_WORKSPACE;
   int* st = device_status_ptr();
   if (!st) return SEP_ERR_CUDA;
-  return from_cuda(launch_build_index(ids, B, L, sids, a, n, block_m,
+  return from_cuda(launch_build_index(ids, B, L, sids, a, n, block_m, 0,
+                                      index_ptrs(index_buf, lay), st, stream));
+}
+
+SEP_API sep_status sep_build_index_fixed(int B, int L, int a, int n, int delta, int block_m,
+                                         void* index_buf, size_t index_bytes, void* stream) {
+  if (B < 1 || L < 1 || a < 0 || n < 1 || delta < 1 || !index_buf) return SEP_ERR_INVALID_ARG;
+  if (!aligned(index_buf, 256)) return SEP_ERR_INVALID_ARG;
+  if (block_m != SEP_BLOCK_M) return SEP_ERR_UNSUPPORTED;
+  const IndexLayout lay = index_layout(B, L, block_m);
+  if (index_bytes < lay.total) return SEP_ERR_WORKSPACE;
+  int* st = device_status_ptr();
+  if (!st) return SEP_ERR_CUDA;
+  SepIdList none;
+  memset(&none, 0, sizeof(none));
+  return from_cuda(launch_build_index(nullptr, B, L, none, a, n, block_m, delta,
                                       index_ptrs(index_buf, lay), st, stream));
 }
 

@@ -761,6 +761,140 @@ cudaError_t launch_step(const CachePtrs& cp, const StepArgs& args, int d, int G,
   return cudaErrorNotSupported;
 }
 
+// ---------------------------------------------------------------------------
+// Bulk prefill: the state T update-only steps leave in an empty cache, in
+// one launch.  In text order the cache always holds the first a tokens, the
+// newest <= s separators among the tokens the window has left behind
+// ([a, cp) for the window start cp), and the window [max(a, cp), T).  Only
+// the window start depends on the step-by-step history (it moves when the
+// cache is full and the past window is compressed); each CTA replays that
+// with a separator prefix count (O(1) per token), then copies its kv head's
+// rows into canonical slots (ring heads at 0).  Attention reads the cache
+// in logical order, so later steps see exactly what T steps would leave.
+// One CTA per (kv head, sequence).
+// ---------------------------------------------------------------------------
+constexpr int kPrefillThreads = 256;
+
+__global__ void __launch_bounds__(kPrefillThreads)
+    cache_prefill_kernel(CachePtrs cp, StepArgs args, int D, const uint16_t* __restrict__ k_in,
+                         const uint16_t* __restrict__ v_in, const int32_t* __restrict__ ids,
+                         int T, int* __restrict__ sep_prefix_all, int* status) {
+  const int g = blockIdx.x, sq = blockIdx.y, tid = threadIdx.x;
+  const int S = args.S, Hkv = args.Hkv, a = args.a, s = args.s, w = args.w, c = args.c,
+            NSL = args.NSL;
+  const int ring = c - a;
+  const size_t mh = (size_t)sq * Hkv + g;
+  __shared__ int warp_sums[kPrefillThreads / 32];
+  __shared__ int carry_sh, bad;
+  __shared__ Meta fin;
+  __shared__ int cp_fin;
+  // separator prefix: sp[t] = #separators among tokens [0, t) (this CTA's
+  // own copy in global scratch of T+1 ints per CTA)
+  int* sp = sep_prefix_all + mh * (size_t)(T + 1);
+  if (tid == 0) {
+    const Meta m = cp.meta[mh];
+    bad = (m.n_init | m.n_sep | m.n_pw | m.t) != 0;  // only an empty cache is filled
+    carry_sh = 0;
+  }
+  __syncthreads();
+  if (bad) {
+    if (tid == 0) report(status, SEP_ERR_DEVICE_BOUNDS);
+    return;
+  }
+  for (int base = 0; base < T; base += kPrefillThreads) {
+    const int t = base + tid;
+    bool is_s = false;
+    if (t < T) {
+      const int id = ids[(size_t)t * S + sq];
+      for (int x = 0; x < args.sids.n; ++x) is_s |= (id == args.sids.ids[x]);
+    }
+    const uint32_t bal = __ballot_sync(0xffffffffu, is_s);
+    const int lane = tid & 31, warp = tid >> 5;
+    if (lane == 0) warp_sums[warp] = __popc(bal);
+    __syncthreads();
+    int before = carry_sh;
+    for (int x = 0; x < warp; ++x) before += warp_sums[x];
+    before += __popc(bal & ((1u << lane) - 1u));
+    if (t < T) sp[t] = before;
+    __syncthreads();
+    if (tid == 0) {
+      int tot = 0;
+      for (int x = 0; x < kPrefillThreads / 32; ++x) tot += warp_sums[x];
+      carry_sh += tot;
+    }
+    __syncthreads();
+  }
+  if (tid == 0) sp[T] = carry_sh;
+  __syncthreads();
+  // replay the counters (thread 0): the step rule with the window start cp
+  if (tid == 0) {
+    int n_init = 0, n_sep = 0, n_pw = 0, cpos = a;  // window = [cpos, cpos + n_pw)
+    for (int t = 0; t < T; ++t) {
+      if (n_init + n_sep + n_pw == c) {
+        const int n_win = min(w, n_pw), n_past = n_pw - n_win;
+        const int ms = sp[cpos + n_past] - sp[cpos];  // separators leaving the window
+        n_sep = min(s, n_sep + ms);
+        cpos += n_past;
+        n_pw = n_win;
+      }
+      if (n_init < a) ++n_init; else ++n_pw;
+    }
+    Meta nm;
+    memset(&nm, 0, sizeof(nm));
+    nm.n_init = n_init;
+    nm.n_sep = n_sep;
+    nm.sep_head = 0;
+    nm.n_pw = n_pw;
+    nm.pw_head = 0;
+    nm.t = T;
+    fin = nm;
+    cp_fin = cpos;
+  }
+  __syncthreads();
+  const Meta nm = fin;
+  const int cpos = cp_fin;  // window start (>= a once the initial block is full)
+  const int D8 = D / 8;
+  uint16_t* kh = cp.k + mh * (size_t)NSL * D;
+  uint16_t* vh = cp.v + mh * (size_t)NSL * D;
+  uint8_t* sepw = cp.issep + mh * NSL;
+  int32_t* posw = cp.pos + (size_t)sq * NSL;
+  auto copy_row = [&](int t, int slot, int u) {
+    const size_t src = ((size_t)t * S + sq) * Hkv + g;
+    reinterpret_cast<uint4*>(kh + (size_t)slot * D)[u] = reinterpret_cast<const uint4*>(k_in + src * D)[u];
+    reinterpret_cast<uint4*>(vh + (size_t)slot * D)[u] = reinterpret_cast<const uint4*>(v_in + src * D)[u];
+  };
+  auto is_sep_at = [&](int t) { return sp[t + 1] != sp[t]; };
+  // initial block: tokens [0, n_init) in slots [0, n_init)
+  for (int e = tid; e < nm.n_init * D8; e += kPrefillThreads) copy_row(e / D8, e / D8, e % D8);
+  for (int t = tid; t < nm.n_init; t += kPrefillThreads) {
+    sepw[t] = is_sep_at(t) ? 1 : 0;
+    if (g == 0) posw[t] = t;
+  }
+  // separator block: the newest n_sep separators among [a, cpos), oldest
+  // first in slots a .. a + n_sep - 1
+  const int first = sp[cpos] - nm.n_sep;  // separator rank of the oldest kept one
+  for (int t = a + tid; t < cpos; t += kPrefillThreads) {
+    if (!is_sep_at(t) || sp[t] < first) continue;
+    const int slot = a + (sp[t] - first);
+    for (int u = 0; u < D8; ++u) copy_row(t, slot, u);
+    sepw[slot] = 1;
+    if (g == 0) posw[slot] = t;
+  }
+  // window: tokens [cpos, T) in ring slots a + s + 0 ..
+  const int w0 = nm.n_init < a ? T : cpos;  // no window until the initial block is full
+  for (int e = tid; e < nm.n_pw * D8; e += kPrefillThreads) {
+    const int x = e / D8;
+    copy_row(w0 + x, a + s + x, e % D8);
+  }
+  for (int x = tid; x < nm.n_pw; x += kPrefillThreads) {
+    sepw[a + s + x] = is_sep_at(w0 + x) ? 1 : 0;
+    if (g == 0) posw[a + s + x] = w0 + x;
+  }
+  (void)ring;
+  __syncthreads();
+  if (tid == 0) cp.meta[mh] = nm;
+}
+
 sep_status shape_check(const sep_cache_params* p) {
   if (!params_ok(p)) return SEP_ERR_INVALID_ARG;
   if (!(p->a + p->s + p->w < p->c)) return SEP_ERR_CAPACITY;
@@ -856,6 +990,40 @@ SEP_API sep_status sep_cache_step(const sep_cache_params* p, void* cache_buf, co
   const cudaError_t e = launch_step(cache_ptrs(cache_buf, l), args, p->d, G, q, k_new, v_new,
                                     ids_new, out, status, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SEP_OK : SEP_ERR_CUDA;
+}
+
+SEP_API size_t sep_cache_prefill_workspace_bytes(const sep_cache_params* p, int T) {
+  if (shape_check(p) != SEP_OK || T < 1) return 0;
+  return align_up(sizeof(int) * (size_t)p->S * p->Hkv * (T + 1), 256);
+}
+
+SEP_API sep_status sep_cache_prefill(const sep_cache_params* p, void* cache_buf,
+                                     const void* k_prompt, const void* v_prompt,
+                                     const int32_t* ids, int T, const int32_t* sep_ids,
+                                     int n_sep_ids, void* ws, size_t ws_bytes, void* stream) {
+  const sep_status st = shape_check(p);
+  if (st != SEP_OK) return st;
+  if (!cache_buf || !k_prompt || !v_prompt || !ids || !ws || T < 1) return SEP_ERR_INVALID_ARG;
+  auto al = [](const void* x, size_t n) { return reinterpret_cast<uintptr_t>(x) % n == 0; };
+  if (!al(cache_buf, 256) || !al(k_prompt, 16) || !al(v_prompt, 16) || !al(ids, 4) ||
+      !al(ws, 256))
+    return SEP_ERR_INVALID_ARG;
+  if (ws_bytes < sep_cache_prefill_workspace_bytes(p, T)) return SEP_ERR_WORKSPACE;
+  if (n_sep_ids < 0 || n_sep_ids > SEP_MAX_SEP_IDS || (n_sep_ids > 0 && !sep_ids))
+    return SEP_ERR_INVALID_ARG;
+  StepArgs args;
+  memset(&args, 0, sizeof(args));
+  args.sids.n = n_sep_ids;
+  for (int i = 0; i < n_sep_ids; ++i) args.sids.ids[i] = sep_ids[i];
+  args.S = p->S; args.Hkv = p->Hkv; args.a = p->a; args.s = p->s; args.w = p->w; args.c = p->c;
+  const CacheLayout l = cache_layout(p);
+  args.NSL = l.NSL;
+  int* status = device_status_ptr();
+  if (!status) return SEP_ERR_CUDA;
+  cache_prefill_kernel<<<dim3(p->Hkv, p->S), kPrefillThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      cache_ptrs(cache_buf, l), args, p->d, static_cast<const uint16_t*>(k_prompt),
+      static_cast<const uint16_t*>(v_prompt), ids, T, static_cast<int*>(ws), status);
+  return cudaGetLastError() == cudaSuccess ? SEP_OK : SEP_ERR_CUDA;
 }
 
 SEP_API size_t sep_cache_export_bytes(const sep_cache_params* p) {

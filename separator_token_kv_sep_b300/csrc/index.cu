@@ -4,7 +4,10 @@
 // keep[j] = (j < a) or ids[j] in the separator set -- the tokens a query
 // still sees after they leave its n-token window (SepLLM anthology record
 // lit-748, Key takeaways, "The mask"; separator set from the paperhub
-// rebuttal, reply A1 to the first reviewer).
+// rebuttal, reply A1 to the first reviewer).  The FixLLM control of the
+// same record ("What is ablated") replaces the separators by one token per
+// interval of fix_delta positions: keep[j] = (j < a) or (j + 1) % fix_delta
+// == 0, with no token ids read.
 //
 // One CTA of 1024 threads per sequence walks the row in chunks of 4096
 // tokens, 4 per thread: a warp shuffle scan and a one-warp scan of the 32
@@ -25,7 +28,7 @@ constexpr int kChunk = kThreads * kPerThread;
 
 __global__ void __launch_bounds__(kThreads)
     build_index_kernel(const int32_t* __restrict__ ids, int B, int L, SepIdList sids, int a, int n,
-                       int block_m, IndexPtrs ptrs, int* status) {
+                       int block_m, int fix_delta, IndexPtrs ptrs, int* status) {
   __shared__ int warp_sums[32];
   __shared__ int chunk_total;
   __shared__ int sep_ids[SEP_MAX_SEP_IDS];
@@ -41,7 +44,9 @@ __global__ void __launch_bounds__(kThreads)
   const int T = (L + block_m - 1) / block_m;
   const int nwords = (L + 31) / 32;
   uint32_t* bits_out = ptrs.keep_bits + (size_t)b * nwords;
-  const bool vec_ok = ((L & 3) == 0) && ((reinterpret_cast<uintptr_t>(row) & 15) == 0);
+  const bool by_ids = fix_delta <= 0;  // else keep is a function of the position alone
+  const bool vec_ok =
+      by_ids && ((L & 3) == 0) && ((reinterpret_cast<uintptr_t>(row) & 15) == 0);
 
   int carry = 0;
   for (int base = 0; base < L; base += kChunk) {
@@ -52,7 +57,7 @@ __global__ void __launch_bounds__(kThreads)
       v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
     } else {
 #pragma unroll
-      for (int e = 0; e < kPerThread; ++e) v[e] = (j0 + e < L) ? row[j0 + e] : 0;
+      for (int e = 0; e < kPerThread; ++e) v[e] = (by_ids && j0 + e < L) ? row[j0 + e] : 0;
     }
     uint32_t nib = 0;
 #pragma unroll
@@ -61,7 +66,11 @@ __global__ void __launch_bounds__(kThreads)
       bool keep = false;
       if (j < L) {
         keep = j < a;
-        for (int s = 0; s < n_sep; ++s) keep |= (v[e] == sep_ids[s]);
+        if (by_ids) {
+          for (int s = 0; s < n_sep; ++s) keep |= (v[e] == sep_ids[s]);
+        } else {
+          keep |= (j + 1) % fix_delta == 0;
+        }
       }
       nib |= (keep ? 1u : 0u) << e;
     }
@@ -135,9 +144,9 @@ __global__ void __launch_bounds__(kThreads)
 }  // namespace
 
 int launch_build_index(const int32_t* ids, int B, int L, const SepIdList& sids, int a, int n,
-                       int block_m, IndexPtrs ptrs, int* status, void* stream) {
+                       int block_m, int fix_delta, IndexPtrs ptrs, int* status, void* stream) {
   build_index_kernel<<<B, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-      ids, B, L, sids, a, n, block_m, ptrs, status);
+      ids, B, L, sids, a, n, block_m, fix_delta, ptrs, status);
   return static_cast<int>(cudaGetLastError());
 }
 

@@ -88,7 +88,7 @@ int* device_status_ptr();
 // ---------------------------------------------------------------------------
 // index.cu
 int launch_build_index(const int32_t* ids, int B, int L, const SepIdList& sids, int a, int n,
-                       int block_m, IndexPtrs ptrs, int* status, void* stream);
+                       int block_m, int fix_delta, IndexPtrs ptrs, int* status, void* stream);
 
 // attn_simt.cu -- fp32 CUDA-core forward
 int launch_attn_fwd_simt(IndexPtrs idx, const float* q, const float* k, const float* v, float* o,

@@ -167,3 +167,59 @@ def test_llama_stream_workload_sampled():
             else:
                 caches[sq].insert(kp[t % P, sq], vp[t % P, sq], sep[t, sq])
     check_state(img, caches, cfg.S, cfg.Hkv, cfg.d, cfg.c)
+
+
+@pytest.mark.parametrize("S,Hq,Hkv,d,a,s,w,c,p,T", [
+    (3, 4, 2, 64, 2, 4, 8, 20, 0.3, 150),
+    (2, 8, 2, 128, 4, 8, 16, 40, 0.2, 333),
+    (2, 4, 4, 64, 0, 3, 5, 12, 0.5, 97),
+    (2, 2, 1, 128, 3, 0, 4, 10, 0.4, 80),
+    (2, 32, 8, 128, 4, 32, 256, 324, 0.12, 2048),
+    (2, 4, 2, 64, 4, 4, 8, 20, 0.3, 3),
+])
+def test_prefill_matches_single_steps(S, Hq, Hkv, d, a, s, w, c, p, T):
+    """One sep_cache_prefill call leaves the export image T update-only steps
+    leave (and the oracle's four-block state); decoding on from either gives
+    identical outputs."""
+    rng = np.random.default_rng(T + c)
+    mk = lambda *sh: torch.from_numpy(
+        synth.round_to_bf16(rng.standard_normal(sh, dtype=np.float32))).to("cuda", torch.bfloat16)
+    n_more = 9
+    k, v = mk(T + n_more, S, Hkv, d), mk(T + n_more, S, Hkv, d)
+    q = mk(T + n_more, S, Hq, d)
+    ids_np = synth.token_ids(rng, (T + n_more, S), p)
+    ids = torch.from_numpy(ids_np).cuda()
+    stepped = GpuStream(S, Hkv, d, a, s, w, c)
+    for t in range(T):
+        stepped.api.sep_cache_step(stepped.p, stepped.buf, None, k[t], v[t], ids[t], synth.SEP_IDS,
+                                   Hq=Hq)
+    bulk = GpuStream(S, Hkv, d, a, s, w, c)
+    bulk.api.sep_cache_prefill(bulk.p, bulk.buf, k[:T].contiguous(), v[:T].contiguous(),
+                               ids[:T].contiguous(), synth.SEP_IDS)
+    img = bulk.export()
+    assert bytes(img) == bytes(stepped.export())
+    caches = [ST.FourBlockCache(a, s, w, c) for _ in range(S)]
+    sep = np.isin(ids_np, synth.SEP_IDS)
+    kn, vn = k.float().cpu().numpy(), v.float().cpu().numpy()
+    for t in range(T):
+        for sq in range(S):
+            caches[sq].insert(kn[t, sq], vn[t, sq], sep[t, sq])
+    check_state(img, caches, S, Hkv, d, c)
+    for t in range(T, T + n_more):
+        o1 = stepped.step(q[t], k[t], v[t], ids[t])
+        o2 = bulk.step(q[t], k[t], v[t], ids[t])
+        assert torch.equal(o1, o2), t
+    assert bulk.api.sep_get_device_status() == 0
+
+
+def test_prefill_rejects_a_cache_in_use():
+    from separator_token_kv_sep_b300 import api
+    S, Hkv, d = 2, 2, 64
+    gs = GpuStream(S, Hkv, d, 2, 4, 8, 20)
+    kk = torch.zeros((4, S, Hkv, d), dtype=torch.bfloat16, device="cuda")
+    ids = torch.zeros((4, S), dtype=torch.int32, device="cuda")
+    gs.api.sep_cache_step(gs.p, gs.buf, None, kk[0], kk[0], ids[0], synth.SEP_IDS, Hq=4)
+    before = bytes(gs.export())
+    api.sep_cache_prefill(gs.p, gs.buf, kk, kk, ids, synth.SEP_IDS)
+    assert api.sep_get_device_status() == 6  # SEP_ERR_DEVICE_BOUNDS
+    assert bytes(gs.export()) == before
