@@ -208,12 +208,12 @@ def run_ours(args, rank, world, device):
     lse = torch.empty((B, Hq, L), dtype=torch.float32, device=device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     # step boundaries, and the per-kernel marks the library records through
-    # sep_profile_events (fwd: gather | attention; bwd: gather | prep | keep
-    # dK/dV | dense dK/dV | dQ)
+    # sep_profile_events (fwd: gather | attention; bwd: prep | dK/dV | dQ |
+    # scatter)
     Ev = lambda: torch.cuda.Event(enable_timing=True, external=True)  # noqa: E731
     step_ev = [Ev(), Ev()]
     fwd_ev = [Ev() for _ in range(3)]
-    bwd_ev = [Ev() for _ in range(6)]
+    bwd_ev = [Ev() for _ in range(5)]
     for e in step_ev + fwd_ev + bwd_ev:  # create the CUDA events outside the capture
         e.record()
     torch.cuda.synchronize()
@@ -244,13 +244,13 @@ def run_ours(args, rank, world, device):
         graph.replay()
     torch.cuda.synchronize()
 
-    kern_names = ["index", "fwd_gather", "fwd_attn", "bwd_gather", "bwd_prep", "bwd_kv",
-                  "bwd_dq", "bwd_scatter"]
+    kern_names = ["index", "fwd_gather", "fwd_attn", "bwd_prep", "bwd_kv", "bwd_dq",
+                  "bwd_scatter"]
     marks = [step_ev[0], fwd_ev[0], fwd_ev[1], fwd_ev[2], bwd_ev[0], bwd_ev[1], bwd_ev[2],
-             bwd_ev[3], bwd_ev[4], bwd_ev[5]]
-    # index: step start -> fwd gather; fwd attn end -> bwd gather is launch glue
-    spans = {"index": (0, 1), "fwd_gather": (1, 2), "fwd_attn": (2, 3), "bwd_gather": (4, 5),
-             "bwd_prep": (5, 6), "bwd_kv": (6, 7), "bwd_dq": (7, 8), "bwd_scatter": (8, 9)}
+             bwd_ev[3], bwd_ev[4]]
+    # index: step start -> fwd gather; fwd attn end -> bwd prep is launch glue
+    spans = {"index": (0, 1), "fwd_gather": (1, 2), "fwd_attn": (2, 3), "bwd_prep": (4, 5),
+             "bwd_kv": (5, 6), "bwd_dq": (6, 7), "bwd_scatter": (7, 8)}
     sampler = ClockSampler(device.index if device.index is not None else 0)
     t_step = []
     t_kern = {n: [] for n in kern_names}
@@ -281,8 +281,7 @@ def run_ours(args, rank, world, device):
     mean = lambda xs: sum(xs) / len(xs)  # noqa: E731
     kern_ms = {n: mean(t_kern[n]) for n in kern_names}
     fwd_ms = kern_ms["fwd_gather"] + kern_ms["fwd_attn"]
-    bwd_ms = sum(kern_ms[n] for n in ("bwd_gather", "bwd_prep", "bwd_kv", "bwd_dq",
-                                      "bwd_scatter"))
+    bwd_ms = sum(kern_ms[n] for n in ("bwd_prep", "bwd_kv", "bwd_dq", "bwd_scatter"))
     fwd_tf = fwd_flops / (fwd_ms * 1e-3) / 1e12
     bwd_tf = bwd_flops / (bwd_ms * 1e-3) / 1e12
     # Algorithmic FLOPs of each tensor-core kernel over the visited pairs it

@@ -342,10 +342,10 @@ sep_status sep_get_device_status(void);
  * capture, where the records become graph nodes).  n_events = 0 clears.
  *   sep_attn_fwd (bf16): [0] before the keep gather, [1] before the
  *                        attention kernel, [2] after it.
- *   sep_attn_bwd:        [0] before the keep gather, [1] before the Delta
- *                        prep (which also writes the dK/dV work schedule),
- *                        [2] before the dK/dV kernel, [3] before the dQ
- *                        kernel, [4] before the keep-row scatter, [5] after.
+ *   sep_attn_bwd:        [0] before the prep kernel (keep gather, Delta and
+ *                        the dK/dV work schedule), [1] before the dK/dV
+ *                        kernel, [2] before the dQ kernel, [3] before the
+ *                        keep-row scatter, [4] after it.
  * Indices past n_events are skipped.  The handles stay owned by the caller
  * and must outlive their registration.
  * Errors: SEP_ERR_INVALID_ARG (n_events out of range, or events NULL with

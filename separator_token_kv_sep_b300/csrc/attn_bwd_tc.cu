@@ -30,6 +30,7 @@
 // All waits are bounded; on expiry a kernel records SEP_ERR_TIMEOUT, drains
 // its copies and MMAs, frees TMEM and returns.
 #include "common.cuh"
+#include "keep_rows.cuh"
 #include "layout.h"
 #include "tma_host.h"
 
@@ -172,126 +173,89 @@ __device__ void build_bwd_schedule(IndexPtrs idx, int B, int Hkv, int L, int T,
 }
 
 // ---------------------------------------------------------------------------
-// Prep: Delta = rowsum(dO o O) in fp32, and zeroed keep-token accumulators.
-// The first kPrepDeltaBlocks(..) CTAs compute Delta: U = D/8 lanes share a
-// row (16 bytes each, so a warp reads 32/U whole rows per instruction) and
-// each warp covers kPrepRows rows.  The remaining CTAs zero, per (batch, kv
-// head), the contiguous accumulator rows [0, ceil128(keep_count)).
+// Prep, one launch before the tensor-core passes:
+//   CTA 0      writes the dK/dV work schedule;
+//   the rest   stride, one warp per unit, over
+//              - the keep-row units: gathered K_keep / V_keep rows and zeroed
+//                fp32 keep accumulators dK_keep / dV_keep;
+//              - the stats units of kPrepRows rows of the padded
+//                [B*Hq][ceil128(L)] row space: (-LSE log2(e), -Delta) with
+//                Delta = rowsum(dO o O) in fp32; rows past L get (0, 0).
 // ---------------------------------------------------------------------------
 constexpr int kPrepThreads = 256;
-constexpr int kPrepRows = 16;  // rows per warp in the Delta part
+constexpr int kPrepRows = 16;  // rows per stats unit
 
 template <int D>
-__host__ __device__ constexpr int prep_rows_per_block() {
-  return (kPrepThreads / 32) * kPrepRows;
+__device__ __forceinline__ void prep_stats_unit(const uint4* __restrict__ o,
+                                                const uint4* __restrict__ dout,
+                                                const float* __restrict__ lse,
+                                                float2* __restrict__ stats, int B, int Hq, int L,
+                                                size_t unit, int lane) {
+  constexpr int U = D / 8;         // 16-byte units per row
+  constexpr int RPI = 32 / U;      // rows per warp instruction
+  constexpr int IT = kPrepRows / RPI;
+  const int LP = (L + 127) / 128 * 128;
+  const size_t R = (size_t)B * Hq * LP;
+  const size_t row0 = unit * kPrepRows;
+  const int sub = lane / U, u = lane % U;
+  uint4 xo[IT], xd[IT];
+  size_t src[IT];
+  bool live[IT];
+#pragma unroll
+  for (int it = 0; it < IT; ++it) {
+    const size_t row = row0 + it * RPI + sub;
+    const size_t plane = row / LP;
+    const int i = static_cast<int>(row % LP);
+    live[it] = row < R && i < L;
+    src[it] = plane * L + i;
+    xo[it] = live[it] ? o[src[it] * U + u] : make_uint4(0, 0, 0, 0);
+    xd[it] = live[it] ? dout[src[it] * U + u] : make_uint4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int it = 0; it < IT; ++it) {
+    const uint32_t xs[4] = {xo[it].x, xo[it].y, xo[it].z, xo[it].w};
+    const uint32_t ys[4] = {xd[it].x, xd[it].y, xd[it].z, xd[it].w};
+    float acc = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      acc = fmaf(__uint_as_float(xs[e] << 16), __uint_as_float(ys[e] << 16), acc);
+      acc = fmaf(__uint_as_float(xs[e] & 0xffff0000u), __uint_as_float(ys[e] & 0xffff0000u),
+                 acc);
+    }
+#pragma unroll
+    for (int off = U / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    const size_t row = row0 + it * RPI + sub;
+    if (u == 0 && row < R)
+      stats[row] = live[it] ? make_float2(-lse[src[it]] * kLog2e, -acc) : make_float2(0.f, 0.f);
+  }
 }
 
 template <int D>
 __global__ void __launch_bounds__(kPrepThreads)
-    bwd_prep_kernel(IndexPtrs idx, const uint4* __restrict__ o, const uint4* __restrict__ dout,
-                    const float* __restrict__ lse, float2* __restrict__ stats,
-                    float4* __restrict__ dk_keep,
+    bwd_prep_kernel(IndexPtrs idx, const uint4* __restrict__ k, const uint4* __restrict__ v,
+                    uint4* __restrict__ kk, uint4* __restrict__ vk, const uint4* __restrict__ o,
+                    const uint4* __restrict__ dout, const float* __restrict__ lse,
+                    float2* __restrict__ stats, float4* __restrict__ dk_keep,
                     float4* __restrict__ dv_keep, int B, int Hq, int Hkv, int L,
-                    int delta_blocks, BwdSchedule* __restrict__ sched,
-                    int4* __restrict__ items) {
-  constexpr int U = D / 8;         // 16-byte units per row
-  constexpr int RPI = 32 / U;      // rows per warp instruction
-  constexpr int IT = kPrepRows / RPI;
+                    BwdSchedule* __restrict__ sched, int4* __restrict__ items) {
   const IndexHeader hdr = *idx.header;
   if (hdr.magic != kIndexMagic || hdr.B != B || hdr.L != L) return;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (blockIdx.x == gridDim.x - 1) {  // the last block writes the dK/dV work schedule
+  if (blockIdx.x == 0) {
     build_bwd_schedule(idx, B, Hkv, L, (L + 127) / 128, sched, items);
     return;
   }
-  if (static_cast<int>(blockIdx.x) < delta_blocks) {
-    // rows of the padded [B*Hq][T*128] stats space; rows past L get (0, 0)
-    const int LP = (L + 127) / 128 * 128;
-    const size_t R = (size_t)B * Hq * LP;
-    const size_t row0 = ((size_t)blockIdx.x * (kPrepThreads / 32) + warp) * kPrepRows;
-    const int sub = lane / U, u = lane % U;
-    uint4 xo[IT], xd[IT];
-    size_t src[IT];
-    bool live[IT];
-#pragma unroll
-    for (int it = 0; it < IT; ++it) {
-      const size_t row = row0 + it * RPI + sub;
-      const size_t plane = row / LP;
-      const int i = static_cast<int>(row % LP);
-      live[it] = row < R && i < L;
-      src[it] = plane * L + i;
-      xo[it] = live[it] ? o[src[it] * U + u] : make_uint4(0, 0, 0, 0);
-      xd[it] = live[it] ? dout[src[it] * U + u] : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int it = 0; it < IT; ++it) {
-      const uint32_t xs[4] = {xo[it].x, xo[it].y, xo[it].z, xo[it].w};
-      const uint32_t ys[4] = {xd[it].x, xd[it].y, xd[it].z, xd[it].w};
-      float acc = 0.f;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        acc = fmaf(__uint_as_float(xs[e] << 16), __uint_as_float(ys[e] << 16), acc);
-        acc = fmaf(__uint_as_float(xs[e] & 0xffff0000u), __uint_as_float(ys[e] & 0xffff0000u),
-                   acc);
-      }
-#pragma unroll
-      for (int off = U / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-      const size_t row = row0 + it * RPI + sub;
-      if (u == 0 && row < R)
-        stats[row] = live[it] ? make_float2(-lse[src[it]] * kLog2e, -acc) : make_float2(0.f, 0.f);
-    }
-    return;
-  }
-  // zero the keep accumulators: per_plane consecutive blocks cover one plane
-  const int zb = static_cast<int>(blockIdx.x) - delta_blocks;
-  const int per_plane = (L * (D / 4) + kPrepThreads * 4 - 1) / (kPrepThreads * 4);
-  const int plane = zb / per_plane, part = zb % per_plane;
-  if (plane >= B * Hkv) return;
-  const int b = plane / Hkv;
-  const int count = min(max(idx.keep_count[b], 0), L);
-  const int end = min(L, (count + 127) / 128 * 128) * (D / 4);  // float4s in use
-  const size_t base = (size_t)plane * L * (D / 4);
-  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    const int e = (part * 4 + r) * kPrepThreads + threadIdx.x;
-    if (e < end) {
-      dk_keep[base + e] = z;
-      dv_keep[base + e] = z;
-    }
-  }
-}
-
-// Gathered keep-token K/V rows, zero-filled up to the next multiple of 128.
-template <int D>
-__global__ void __launch_bounds__(256)
-    bwd_gather_kernel(IndexPtrs idx, const uint4* __restrict__ k, const uint4* __restrict__ v,
-                      uint4* __restrict__ kk, uint4* __restrict__ vk, int Hkv, int L) {
-  constexpr int U = D / 8;
-  constexpr int ROWS = 64;
-  const int g = blockIdx.y, b = blockIdx.z;
-  // the header sits at offset 0 of any index buffer: check it before using
-  // the fields whose offsets depend on B and L
-  const IndexHeader hdr = *idx.header;
-  if (hdr.magic != kIndexMagic || hdr.B != static_cast<int>(gridDim.z) || hdr.L != L) return;
-  const int count = idx.keep_count[b];
-  if (count < 0 || count > L) return;
-  const int end = min(L, (count + 127) / 128 * 128);
-  const int r0 = blockIdx.x * ROWS;
-  if (r0 >= end) return;
-  const int32_t* kpos = idx.keep_pos + (size_t)b * L;
-  const size_t plane = ((size_t)b * Hkv + g) * (size_t)L * U;
-  for (int e = threadIdx.x; e < ROWS * U; e += blockDim.x) {
-    const int row = r0 + e / U, u = e % U;
-    if (row >= end) break;
-    const int src = row < count ? kpos[row] : -1;
-    uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
-    if (src >= 0 && src < L) {
-      kv = k[plane + (size_t)src * U + u];
-      vv = v[plane + (size_t)src * U + u];
-    }
-    kk[plane + (size_t)row * U + u] = kv;
-    vk[plane + (size_t)row * U + u] = vv;
+  constexpr int WPB = kPrepThreads / 32;
+  const int lane = threadIdx.x & 31;
+  const size_t w0 = (size_t)(blockIdx.x - 1) * WPB + (threadIdx.x >> 5);
+  const size_t nw = (size_t)(gridDim.x - 1) * WPB;
+  const size_t gunits = static_cast<size_t>(keep_units(B, Hkv, L));
+  const size_t sunits = ((size_t)B * Hq * ((L + 127) / 128 * 128)) / kPrepRows;
+  for (size_t u = w0; u < gunits + sunits; u += nw) {
+    if (u < gunits)
+      gather_keep_unit<D>(idx, k, v, kk, vk, dk_keep, dv_keep, B, Hkv, L, static_cast<int>(u),
+                          lane);
+    else
+      prep_stats_unit<D>(o, dout, lse, stats, B, Hq, L, u - gunits, lane);
   }
 }
 
@@ -723,27 +687,12 @@ __global__ void __launch_bounds__(256)
     bwd_keep_scatter_kernel(IndexPtrs idx, const float4* __restrict__ dk_keep,
                             const float4* __restrict__ dv_keep, __nv_bfloat16* __restrict__ dk,
                             __nv_bfloat16* __restrict__ dv, int B, int Hkv, int L, float scale) {
-  constexpr int U = D / 4;  // float4 per row
   const IndexHeader hdr = *idx.header;
   if (hdr.magic != kIndexMagic || hdr.B != B || hdr.L != L) return;
-  const int g = blockIdx.y, b = blockIdx.z;
-  const int count = min(max(idx.keep_count[b], 0), L);
-  const int32_t* kpos = idx.keep_pos + (size_t)b * L;
-  const size_t plane = (size_t)b * Hkv + g;
-  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < count * U; e += gridDim.x * blockDim.x) {
-    const int row = e / U, u = e % U;
-    const int j = kpos[row];
-    if (j < 0 || j >= L) continue;
-    const float4 a = dk_keep[(plane * L + row) * U + u];
-    const float4 c = dv_keep[(plane * L + row) * U + u];
-    uint2 ko, vo;
-    ko.x = pack_bf16x2(a.x * scale, a.y * scale);
-    ko.y = pack_bf16x2(a.z * scale, a.w * scale);
-    vo.x = pack_bf16x2(c.x, c.y);
-    vo.y = pack_bf16x2(c.z, c.w);
-    *reinterpret_cast<uint2*>(dk + (plane * L + j) * D + 4 * u) = ko;
-    *reinterpret_cast<uint2*>(dv + (plane * L + j) * D + 4 * u) = vo;
-  }
+  const int units = keep_units(B, Hkv, L);
+  const int lane = threadIdx.x & 31;
+  for (int u = blockIdx.x * 8 + (threadIdx.x >> 5); u < units; u += gridDim.x * 8)
+    scatter_keep_unit<D>(idx, dk_keep, dv_keep, dk, dv, B, Hkv, L, scale, u, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -1146,15 +1095,6 @@ BwdWs bwd_ws(void* base, int B, int Hq, int Hkv, int L, int d) {
   return w;
 }
 
-int num_sms() {
-  static int n[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (!n[dev] && cudaDeviceGetAttribute(&n[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    n[dev] = 148;
-  return n[dev];
-}
-
 template <int D>
 int launch_bwd_impl(IndexPtrs idx, const void* q, const void* k, const void* v, const void* o,
                     const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
@@ -1162,20 +1102,20 @@ int launch_bwd_impl(IndexPtrs idx, const void* q, const void* k, const void* v, 
                     cudaStream_t s) {
   const BwdWs w = bwd_ws(ws, B, Hq, Hkv, L, D);
   const int T = (L + 127) / 128;
+  const int sms = num_sms();
   profile_mark(0, s);
-  bwd_gather_kernel<D><<<dim3((L + 63) / 64, Hkv, B), 256, 0, s>>>(
-      idx, static_cast<const uint4*>(k), static_cast<const uint4*>(v),
-      reinterpret_cast<uint4*>(w.kk), reinterpret_cast<uint4*>(w.vk), Hkv, L);
-  profile_mark(1, s);
   {
-    const size_t rows = (size_t)B * Hq * T * 128;
-    const int delta_blocks =
-        static_cast<int>((rows + prep_rows_per_block<D>() - 1) / prep_rows_per_block<D>());
-    const int per_plane = (L * (D / 4) + kPrepThreads * 4 - 1) / (kPrepThreads * 4);
-    bwd_prep_kernel<D><<<delta_blocks + B * Hkv * per_plane + 1, kPrepThreads, 0, s>>>(
-        idx, static_cast<const uint4*>(o), static_cast<const uint4*>(dout), lse, w.stats,
+    // one CTA for the schedule, then a few CTAs per SM for the strided units
+    const size_t units = static_cast<size_t>(keep_units(B, Hkv, L)) +
+                         (size_t)B * Hq * T * 128 / kPrepRows;
+    const size_t want = (units + kPrepThreads / 32 - 1) / (kPrepThreads / 32);
+    const int ctas = static_cast<int>(want < (size_t)8 * sms ? want : (size_t)8 * sms);
+    bwd_prep_kernel<D><<<ctas + 1, kPrepThreads, 0, s>>>(
+        idx, static_cast<const uint4*>(k), static_cast<const uint4*>(v),
+        reinterpret_cast<uint4*>(w.kk), reinterpret_cast<uint4*>(w.vk),
+        static_cast<const uint4*>(o), static_cast<const uint4*>(dout), lse, w.stats,
         reinterpret_cast<float4*>(w.dk_keep), reinterpret_cast<float4*>(w.dv_keep), B, Hq, Hkv,
-        L, delta_blocks, w.sched, w.items);
+        L, w.sched, w.items);
   }
   CUtensorMap mq, mdo, mk, mv, mkk, mvk;
   if (!make_bf16_map(&mq, q, (uint64_t)B * Hq, L, D, 128) ||
@@ -1196,23 +1136,21 @@ int launch_bwd_impl(IndexPtrs idx, const void* q, const void* k, const void* v, 
     return static_cast<int>(e);
   __nv_bfloat16* dkb = static_cast<__nv_bfloat16*>(dk);
   __nv_bfloat16* dvb = static_cast<__nv_bfloat16*>(dv);
-  const int sms = num_sms();
-  profile_mark(2, s);
+  profile_mark(1, s);
   kv_k<<<sms, kThreads, KC::SMEM, s>>>(mkk, mvk, mk, mv, mq, mdo, idx, w.sched, w.items,
                                        w.stats, w.dk_keep, w.dv_keep, dkb, dvb, B, Hq, Hkv, L,
                                        scale, scale_log2, status);
-  profile_mark(3, s);
+  profile_mark(2, s);
   const int dq_items = B * Hq * T;
   dq_k<<<dq_items < sms ? dq_items : sms, kThreads, QC::SMEM, s>>>(
       mq, mdo, mk, mv, mkk, mvk, idx, w.stats, static_cast<__nv_bfloat16*>(dq), B, Hq, Hkv,
       L, scale, scale_log2, status);
-  profile_mark(4, s);
-  bwd_keep_scatter_kernel<D><<<dim3((L * (D / 4) + 255) / 256 < 64 ? (L * (D / 4) + 255) / 256 : 64,
-                                    Hkv, B), 256, 0, s>>>(
+  profile_mark(3, s);
+  bwd_keep_scatter_kernel<D><<<keep_pass_ctas(keep_units(B, Hkv, L), sms), 256, 0, s>>>(
       idx, reinterpret_cast<const float4*>(w.dk_keep), reinterpret_cast<const float4*>(w.dv_keep),
       dkb, dvb, B, Hkv, L, scale);
   const cudaError_t err = cudaGetLastError();
-  profile_mark(5, s);
+  profile_mark(4, s);
   return static_cast<int>(err);
 }
 

@@ -6,24 +6,29 @@
 // the n nearest tokens (SepLLM anthology record lit-748, Key takeaways,
 // "The mask"; pith.science review, key_machinery).
 //
-// How: one CTA per (128-row query tile, q head, batch).  The tile's keys come
+// How: a persistent kernel, one CTA per SM, walks work items of two adjacent
+// 128-row query tiles A and B of one (batch, q head).  A tile's keys come
 // from two sources, read from the index built by sep_build_index:
 //   gathered tiles  the keep tokens before the tile's first window start,
 //                   copied densely into K_keep / V_keep by gather_keep_kernel;
 //                   the last one is masked by k < n_gather;
 //   band tiles      the dense key range [dense_lo, dense_hi), masked per
 //                   element by j <= i and (keep[j] or j >= i-n+1).
-// Warp roles: warp 0 issues TMA loads (Q once, then K and V tiles through an
-// NST-stage ring), warp 1 issues tcgen05.mma (S = Q K^T into one of NS TMEM
-// buffers, O += P V into a TMEM accumulator), warps 2-5 run the softmax, one
-// thread per query row: they read S with tcgen05.ld, apply the mask, keep a
-// running max (rescaling O in TMEM only when the max grows by more than 2^8,
-// which keeps every P <= 256 and the final O / l exact), write P as bf16 into
-// shared memory in the 128-byte-swizzle K-major layout the MMA reads, and
-// finally normalise O and store it with the LSE.
+// A and B walk one K/V stream, the union of their key tiles.
+// Warp roles: warp 0 issues TMA loads (each item's two query tiles into one
+// of QB buffers, then K and V tiles through an NST-stage ring), warp 1
+// issues tcgen05.mma (S_X = Q_X K^T into TMEM, O_X += P_X V with P_X read
+// from TMEM), warps 2-5 and 6-9 run the softmax of A and of B, one thread
+// per query row: they read S with tcgen05.ld, apply the mask, keep a running
+// max (rescaling O in TMEM only when the max grows by more than 2^8, which
+// keeps every P <= 256 and the final O / l exact), write P as packed bf16
+// over the first half of S, and after the item's last tile normalise O and
+// store it with the LSE.  The next item's query tiles and first S products
+// are issued while the current item finishes, so its epilogue overlaps them.
 // Every mbarrier wait is bounded; on expiry the kernel records
 // SEP_ERR_TIMEOUT, lets its copies and MMAs drain, frees TMEM and returns.
 #include "common.cuh"
+#include "keep_rows.cuh"
 #include "layout.h"
 #include "tma_host.h"
 
@@ -36,41 +41,25 @@ constexpr int kChunk = 128 * 128;  // bytes of a [128 rows x 64 cols] bf16 block
 template <int D>
 __global__ void __launch_bounds__(256)
     gather_keep_kernel(IndexPtrs idx, const uint4* __restrict__ k, const uint4* __restrict__ v,
-                       uint4* __restrict__ kk, uint4* __restrict__ vk, int Hkv, int L) {
-  constexpr int U = D / 8;  // 16-byte units per row
-  constexpr int ROWS = 64;
-  const int g = blockIdx.y, b = blockIdx.z;
+                       uint4* __restrict__ kk, uint4* __restrict__ vk, int B, int Hkv, int L) {
   // the header sits at offset 0 of any index buffer: check it before using
   // the fields whose offsets depend on B and L
   const IndexHeader hdr = *idx.header;
-  if (hdr.magic != kIndexMagic || hdr.B != static_cast<int>(gridDim.z) || hdr.L != L) return;
-  const int count = idx.keep_count[b];
-  if (count < 0 || count > L) return;
-  const int end = min(L, (count + 127) / 128 * 128);
-  const int r0 = blockIdx.x * ROWS;
-  if (r0 >= end) return;
-  const int32_t* kpos = idx.keep_pos + (size_t)b * L;
-  const size_t plane = ((size_t)b * Hkv + g) * (size_t)L * U;
-  for (int e = threadIdx.x; e < ROWS * U; e += blockDim.x) {
-    const int row = r0 + e / U, u = e % U;
-    if (row >= end) break;
-    const int src = row < count ? kpos[row] : -1;
-    uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
-    if (src >= 0 && src < L) {
-      kv = k[plane + (size_t)src * U + u];
-      vv = v[plane + (size_t)src * U + u];
-    }
-    kk[plane + (size_t)row * U + u] = kv;
-    vk[plane + (size_t)row * U + u] = vv;
-  }
+  if (hdr.magic != kIndexMagic || hdr.B != B || hdr.L != L) return;
+  const int units = keep_units(B, Hkv, L);
+  const int lane = threadIdx.x & 31;
+  for (int u = blockIdx.x * 8 + (threadIdx.x >> 5); u < units; u += gridDim.x * 8)
+    gather_keep_unit<D>(idx, k, v, kk, vk, nullptr, nullptr, B, Hkv, L, u, lane);
 }
 
-template <int D, int NST>
+template <int D>
 struct FwdCfg {
   static constexpr int DCH = D / 64;
   static constexpr int TILE = DCH * kChunk;  // one [128 x D] bf16 tile
-  static constexpr int OFF_Q = 0;            // [2] query tiles A, B
-  static constexpr int OFF_K = OFF_Q + 2 * TILE;
+  static constexpr int QB = D == 64 ? 2 : 1;   // query-pair buffers
+  static constexpr int NST = D == 64 ? 4 : 2;  // K/V ring stages
+  static constexpr int OFF_Q = 0;              // [QB][query tiles A, B]
+  static constexpr int OFF_K = OFF_Q + QB * 2 * TILE;
   static constexpr int OFF_V = OFF_K + NST * TILE;
   static constexpr int SMEM = OFF_V + NST * TILE + 1024;
   // tensor memory: per query tile X, S (fp32, 128 columns; P overwrites its
@@ -83,14 +72,19 @@ struct FwdCfg {
 constexpr int kThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-5 softmax A, 6-9 softmax B
 constexpr float kRescaleLog2 = 8.0f;
 
-// The key tiles one CTA visits for its query tiles A = 2p and B = 2p + 1, in
-// order: the gathered keep tiles of the longer gathered list, then the dense
-// band from A's window start to B's last row.  Tile u is active for X when it
-// holds keys X can see: gathered tile u when 128u < n_gather(X); a band tile
-// for A below A's last row, for B when it reaches past B's window start.
+// One work item: query tiles A = 2p and B = 2p + 1 of one (batch, q head).
+// Items are numbered longest first (pair index descending, then batch and
+// head), and CTA c of a grid of G takes items c, c + G, c + 2G, ...
+//
+// The key tiles an item visits, in order: the gathered keep tiles of the
+// longer gathered list, then the dense band from A's window start to B's
+// last row.  Tile u is active for X when it holds keys X can see: gathered
+// tile u when 128u < n_gather(X); a band tile for A below A's last row, for
+// B when it reaches past B's window start.
 struct PairPlan {
   int nA, loA, hiA, nB, loB, hiB;  // block records of A and B
-  bool hasB;
+  int b, h, tA;
+  bool hasB, valid;
   int nG, nT;  // gathered tiles, total tiles
   __device__ bool active(int u, int x) const {
     if (x == 1 && !hasB) return false;
@@ -99,9 +93,45 @@ struct PairPlan {
     return x == 0 ? jt < hiA : (jt + 128 > loB && jt < hiB);
   }
   __device__ bool any(int u) const { return active(u, 0) || active(u, 1); }
+  // first active tile after u (nT if none)
+  __device__ int next(int u) const {
+    ++u;
+    while (u < nT && !any(u)) ++u;
+    return u;
+  }
 };
 
-template <int D, int NST>
+__device__ __forceinline__ PairPlan load_plan(IndexPtrs idx, int item, int n_items, int B, int Hq,
+                                              int L, int T) {
+  PairPlan pl;
+  pl.valid = false;
+  pl.nT = 0;
+  if (item >= n_items) return pl;
+  const int P = (T + 1) >> 1, BH = B * Hq;
+  const int pair = P - 1 - item / BH, bh = item % BH;
+  pl.b = bh / Hq;
+  pl.h = bh % Hq;
+  pl.tA = 2 * pair;
+  pl.hasB = pl.tA + 1 < T;
+  const int4 ba = *reinterpret_cast<const int4*>(idx.blocks + ((size_t)pl.b * T + pl.tA) * 4);
+  const int4 bb =
+      pl.hasB ? *reinterpret_cast<const int4*>(idx.blocks + ((size_t)pl.b * T + pl.tA + 1) * 4)
+              : ba;
+  pl.nA = ba.x; pl.loA = ba.y; pl.hiA = ba.z;
+  pl.nB = bb.x; pl.loB = bb.y; pl.hiB = bb.z;
+  auto bad = [&](int4 r, int q0) {
+    return r.x < 0 || r.x > r.y || r.y < 0 || r.y > q0 || r.z <= q0 || r.z > L;
+  };
+  pl.valid = !(bad(ba, pl.tA * 128) ||
+               (pl.hasB && (bad(bb, pl.tA * 128 + 128) || bb.x < ba.x || bb.y < ba.y)));
+  if (pl.valid) {
+    pl.nG = ((pl.hasB ? pl.nB : pl.nA) + 127) >> 7;
+    pl.nT = pl.nG + (((pl.hasB ? pl.hiB : pl.hiA) - pl.loA + 127) >> 7);
+  }
+  return pl;
+}
+
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
@@ -110,49 +140,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tm_vk, IndexPtrs idx,
                        __nv_bfloat16* __restrict__ o, float* __restrict__ lse, int B, int Hq,
                        int Hkv, int L, float scale_log2, int* status) {
-  using C = FwdCfg<D, NST>;
+  using C = FwdCfg<D>;
+  constexpr int QB = C::QB, NST = C::NST;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  __shared__ __align__(8) uint64_t q_full, kv_full[NST], kv_empty[NST], s_full[2], p_full[2],
-      o_done[2], mma_final;
+  __shared__ __align__(8) uint64_t q_full[QB], q_empty[QB], kv_full[NST], kv_empty[NST],
+      s_full[2], p_full[2], o_done[2], mma_final;
   __shared__ uint32_t tmem_slot;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = (L + 127) >> 7;
-  const int P = (T + 1) >> 1;
-  const int pair = P - 1 - static_cast<int>(blockIdx.x);  // longest first
-  const int h = blockIdx.y, b = blockIdx.z;
-  const int g = h / (Hq / Hkv);
-  const int tA = 2 * pair;
+  const int n_items = B * Hq * ((T + 1) >> 1);
+  const int G = gridDim.x;
+  const int grp = Hq / Hkv;
 
   const IndexHeader hdr = *idx.header;
   if (hdr.magic != kIndexMagic || hdr.B != B || hdr.L != L || hdr.block_m != 128) {
     if (threadIdx.x == 0) report(status, SEP_ERR_DEVICE_BOUNDS);
     return;
   }
-  PairPlan pl;
-  pl.hasB = tA + 1 < T;
-  {
-    const int4 ba = *reinterpret_cast<const int4*>(idx.blocks + ((size_t)b * T + tA) * 4);
-    const int4 bb = pl.hasB ? *reinterpret_cast<const int4*>(idx.blocks + ((size_t)b * T + tA + 1) * 4)
-                            : ba;
-    pl.nA = ba.x; pl.loA = ba.y; pl.hiA = ba.z;
-    pl.nB = bb.x; pl.loB = bb.y; pl.hiB = bb.z;
-    auto bad = [&](int4 r, int q0) {
-      return r.x < 0 || r.x > r.y || r.y < 0 || r.y > q0 || r.z <= q0 || r.z > L;
-    };
-    if (bad(ba, tA * 128) || (pl.hasB && (bad(bb, tA * 128 + 128) || bb.x < ba.x || bb.y < ba.y))) {
-      if (threadIdx.x == 0) report(status, SEP_ERR_DEVICE_BOUNDS);
-      return;
-    }
-    pl.nG = ((pl.hasB ? pl.nB : pl.nA) + 127) >> 7;
-    pl.nT = pl.nG + (((pl.hasB ? pl.hiB : pl.hiA) - pl.loA + 127) >> 7);
-  }
   const int n_win = hdr.n;
 
   if (threadIdx.x == 0) {
-    mbar_init(&q_full, 1);
+    for (int s = 0; s < QB; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_empty[s], 1);
+    }
     for (int s = 0; s < NST; ++s) {
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
@@ -180,52 +194,72 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      const int plane_q = b * Hq + h, plane_kv = b * Hkv + g;
-      mbar_arrive_expect_tx(&q_full, (pl.hasB ? 2 : 1) * C::TILE);
-      for (int x = 0; x < (pl.hasB ? 2 : 1); ++x)
-        for (int c = 0; c < C::DCH; ++c)
-          tma_load_3d(smem + C::OFF_Q + x * C::TILE + c * kChunk, &tm_q, &q_full, 64 * c,
-                      (tA + x) * 128, plane_q);
-      int n = 0;
+      tma_prefetch_desc(&tm_kk);
+      tma_prefetch_desc(&tm_vk);
+      int n = 0, kq = 0;  // K/V stages and query pairs loaded
       bool ok = true;
-      for (int u = 0; u < pl.nT; ++u) {
-        if (!pl.any(u)) continue;
-        const int st = n % NST;
-        if (n >= NST && !mbar_wait(&kv_empty[st], ((n / NST) - 1) & 1, status)) {
+      for (int it = blockIdx.x; ok && it < n_items; it += G) {
+        const PairPlan pl = load_plan(idx, it, n_items, B, Hq, L, T);
+        if (!pl.valid) {
+          report(status, SEP_ERR_DEVICE_BOUNDS);
+          continue;
+        }
+        const int qs = kq % QB;
+        if (kq >= QB && !mbar_wait(&q_empty[qs], ((kq / QB) - 1) & 1, status)) {
           ok = false;
           break;
         }
-        const bool gat = u < pl.nG;
-        const CUtensorMap* mk = gat ? &tm_kk : &tm_k;
-        const CUtensorMap* mv = gat ? &tm_vk : &tm_v;
-        const int row = gat ? 128 * u : pl.loA + 128 * (u - pl.nG);
-        mbar_arrive_expect_tx(&kv_full[st], 2 * C::TILE);
-        for (int c = 0; c < C::DCH; ++c) {
-          tma_load_3d(smem + C::OFF_K + st * C::TILE + c * kChunk, mk, &kv_full[st], 64 * c, row,
-                      plane_kv);
-          tma_load_3d(smem + C::OFF_V + st * C::TILE + c * kChunk, mv, &kv_full[st], 64 * c, row,
-                      plane_kv);
+        const int plane_q = pl.b * Hq + pl.h, plane_kv = pl.b * Hkv + pl.h / grp;
+        mbar_arrive_expect_tx(&q_full[qs], (pl.hasB ? 2 : 1) * C::TILE);
+        for (int x = 0; x < (pl.hasB ? 2 : 1); ++x)
+          for (int c = 0; c < C::DCH; ++c)
+            tma_load_3d(smem + C::OFF_Q + (qs * 2 + x) * C::TILE + c * kChunk, &tm_q, &q_full[qs],
+                        64 * c, (pl.tA + x) * 128, plane_q);
+        ++kq;
+        for (int u = 0; u < pl.nT; ++u) {
+          if (!pl.any(u)) continue;
+          const int st = n % NST;
+          if (n >= NST && !mbar_wait(&kv_empty[st], ((n / NST) - 1) & 1, status)) {
+            ok = false;
+            break;
+          }
+          const bool gat = u < pl.nG;
+          const CUtensorMap* mk = gat ? &tm_kk : &tm_k;
+          const CUtensorMap* mv = gat ? &tm_vk : &tm_v;
+          const int row = gat ? 128 * u : pl.loA + 128 * (u - pl.nG);
+          mbar_arrive_expect_tx(&kv_full[st], 2 * C::TILE);
+          for (int c = 0; c < C::DCH; ++c) {
+            tma_load_3d(smem + C::OFF_K + st * C::TILE + c * kChunk, mk, &kv_full[st], 64 * c,
+                        row, plane_kv);
+            tma_load_3d(smem + C::OFF_V + st * C::TILE + c * kChunk, mv, &kv_full[st], 64 * c,
+                        row, plane_kv);
+          }
+          ++n;
         }
-        ++n;
       }
       if (!ok) {
         // let the copies still in flight land before the CTA's smem goes away
         for (int x = n - NST; x < n; ++x)
           if (x >= 0) mbar_wait(&kv_full[x % NST], (x / NST) & 1, status);
-        mbar_wait(&q_full, 0, status);
+        for (int x = kq - QB; x < kq; ++x)
+          if (x >= 0) mbar_wait(&q_full[x % QB], (x / QB) & 1, status);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // The issuer walks one flat stream of (item, key tile) steps.  Per step
+    // it issues P.V of tile A, S of A's next step, P.V of B, then S of B's
+    // next step, so one tile's softmax runs while the other's products do;
+    // the next step may belong to the next item, whose S products then
+    // overlap this item's last P.V and the epilogue.
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
       const uint32_t k_base = smem_u32(smem + C::OFF_K), v_base = smem_u32(smem + C::OFF_V);
-      int cnt0 = 0, cnt1 = 0;  // P.V products issued per query tile
-      bool ok = mbar_wait(&q_full, 0, status);
-      tc_fence_after();
-      auto issue_qk = [&](int x, int st) {
-        const uint32_t q_base = smem_u32(smem + C::OFF_Q + x * C::TILE);
+      int cnt0 = 0, cnt1 = 0;  // P.V products issued per query tile (p_full parity)
+      int ci0 = 0, ci1 = 0;    // ... within the current item (accumulate flag)
+      auto issue_qk = [&](int x, int qs, int st) {
+        const uint32_t q_base = smem_u32(smem + C::OFF_Q + (qs * 2 + x) * C::TILE);
         const uint32_t d_s = tmem + (x ? C::TM_S1 : C::TM_S0);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -237,6 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto issue_pv = [&](int x, int st) -> bool {  // O_x (+)= P_x V, P_x from TMEM
         int& cx = x ? cnt1 : cnt0;
+        int& cix = x ? ci1 : ci0;
         if (!mbar_wait(&p_full[x], cx & 1, status)) return false;
         tc_fence_after();
         const uint32_t a_p = tmem + (x ? C::TM_S1 : C::TM_S0);
@@ -245,43 +280,73 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < 8; ++kk)
           umma_bf16_ts(d_o, a_p + 8 * kk,
                        sdesc_sw128(v_base + st * C::TILE + kk * 2048, kChunk, 1024), idesc_pv,
-                       (cx > 0 || kk > 0) ? 1u : 0u);
+                       (cix > 0 || kk > 0) ? 1u : 0u);
         ++cx;
+        ++cix;
         return true;
       };
-      // first active tile: both S products
-      int u = 0, n = 0;
-      while (u < pl.nT && !pl.any(u)) ++u;
-      if (ok && u < pl.nT) {
-        ok = mbar_wait(&kv_full[0], 0, status);
+      bool ok = true;
+      int it = blockIdx.x;
+      PairPlan pc = load_plan(idx, it, n_items, B, Hq, L, T);
+      while (it < n_items && !pc.valid) {
+        it += G;
+        pc = load_plan(idx, it, n_items, B, Hq, L, T);
+      }
+      if (it < n_items) {
+        int kq = 0, qs = 0, n = 0;  // current item's index and Q buffer; K/V stage count
+        int u = pc.next(-1);
+        int itn = it + G;
+        PairPlan pn = load_plan(idx, itn, n_items, B, Hq, L, T);  // prefetched
+        ok = mbar_wait(&q_full[0], 0, status) && mbar_wait(&kv_full[0], 0, status);
         tc_fence_after();
         if (ok) {
-          if (pl.active(u, 0)) issue_qk(0, 0);
-          if (pl.active(u, 1)) issue_qk(1, 0);
+          if (pc.active(u, 0)) issue_qk(0, 0, 0);
+          if (pc.active(u, 1)) issue_qk(1, 0, 0);
+          if (pc.next(u) >= pc.nT) umma_commit(&q_empty[0]);  // every S of the item issued
+        }
+        while (ok) {
+          const int st = n % NST, stn = (n + 1) % NST;
+          int un = pc.next(u);
+          const bool same = un < pc.nT;
+          if (!same) {
+            while (itn < n_items && !pn.valid) {
+              itn += G;
+              pn = load_plan(idx, itn, n_items, B, Hq, L, T);
+            }
+            if (itn < n_items) un = pn.next(-1);
+          }
+          const bool has_next = same || itn < n_items;
+          const int qsn = same ? qs : (kq + 1) % QB;
+          const PairPlan px = same ? pc : pn;
+          if (pc.active(u, 0) && !(ok = issue_pv(0, st))) break;
+          if (!same) umma_commit(&o_done[0]);
+          if (has_next) {
+            if (!same && !(ok = mbar_wait(&q_full[qsn], ((kq + 1) / QB) & 1, status))) break;
+            if (!(ok = mbar_wait(&kv_full[stn], ((n + 1) / NST) & 1, status))) break;
+            tc_fence_after();
+            if (px.active(un, 0)) issue_qk(0, qsn, stn);
+          }
+          if (pc.active(u, 1) && !(ok = issue_pv(1, st))) break;
+          umma_commit(&kv_empty[st]);  // every MMA reading this K/V stage is issued
+          if (!same && pc.hasB) umma_commit(&o_done[1]);
+          if (has_next) {
+            if (px.active(un, 1)) issue_qk(1, qsn, stn);
+            if (px.next(un) >= px.nT) umma_commit(&q_empty[qsn]);
+          }
+          ++n;
+          if (!has_next) break;
+          if (!same) {
+            pc = pn;
+            it = itn;
+            ++kq;
+            qs = qsn;
+            ci0 = ci1 = 0;
+            itn = it + G;
+            pn = load_plan(idx, itn, n_items, B, Hq, L, T);
+          }
+          u = un;
         }
       }
-      while (ok && u < pl.nT) {
-        const int st = n % NST;
-        int un = u + 1;
-        while (un < pl.nT && !pl.any(un)) ++un;
-        const int stn = (n + 1) % NST;
-        const bool has_next = un < pl.nT;
-        // A: P.V of this tile, then S of the next (S_A / P_A share TMEM, and
-        // the tensor pipe runs these in issue order)
-        if (pl.active(u, 0) && !(ok = issue_pv(0, st))) break;
-        if (has_next) {
-          if (!(ok = mbar_wait(&kv_full[stn], ((n + 1) / NST) & 1, status))) break;
-          tc_fence_after();
-          if (pl.active(un, 0)) issue_qk(0, stn);
-        }
-        if (pl.active(u, 1) && !(ok = issue_pv(1, st))) break;
-        umma_commit(&kv_empty[st]);  // every MMA reading this K/V stage is issued
-        if (has_next && pl.active(un, 1)) issue_qk(1, stn);
-        u = un;
-        ++n;
-      }
-      umma_commit(&o_done[0]);
-      umma_commit(&o_done[1]);
       // every MMA issued by this thread completes before TMEM is released
       umma_commit(&mma_final);
       mbar_wait(&mma_final, 0, status);
@@ -292,18 +357,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int x = (warp - 2) >> 2;  // query tile: 0 = A, 1 = B
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
-    const int i = (tA + x) * 128 + r;
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t tS = tmem + lane_base + (x ? C::TM_S1 : C::TM_S0);
     const uint32_t tO = tmem + lane_base + (x ? C::TM_O1 : C::TM_O0);
-    const uint32_t* kbits = idx.keep_bits + (size_t)b * hdr.nwords;
     const int nwords = hdr.nwords;
-    const int n_gath = x ? pl.nB : pl.nA;
-    const int lo_x = x ? pl.loB : pl.loA;
-    float m_used = -INFINITY, l = 0.f;
+    int cnt = 0, ko = 0;  // S tiles and items finished by this query tile
     bool ok = true;
-    int cnt = 0;
-    if (x == 0 || pl.hasB) {
+    PairPlan pn = load_plan(idx, blockIdx.x, n_items, B, Hq, L, T);
+    for (int it = blockIdx.x; ok && it < n_items; it += G) {
+      const PairPlan pl = pn;
+      pn = load_plan(idx, it + G, n_items, B, Hq, L, T);  // prefetch the next item
+      if (!pl.valid || (x == 1 && !pl.hasB)) continue;
+      const int b = pl.b, h = pl.h;
+      const int i = (pl.tA + x) * 128 + r;
+      const uint32_t* kbits = idx.keep_bits + (size_t)b * nwords;
+      const int n_gath = x ? pl.nB : pl.nA;
+      const int lo_x = x ? pl.loB : pl.loA;
+      float m_used = -INFINITY, l = 0.f;
+      int ci = 0;
       for (int u = 0; u < pl.nT; ++u) {
         if (!pl.active(u, x)) continue;
         // visibility of the 128 columns as 4 words
@@ -367,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float msub = (m_used == -INFINITY) ? 0.f : m_used;
         // O rescale: S of this tile being ready means the previous P.V of
         // this query tile has completed (the tensor pipe runs in order)
-        if (cnt > 0 && __any_sync(0xffffffffu, rescale)) {
+        if (ci > 0 && __any_sync(0xffffffffu, rescale)) {
           uint32_t ob[32];
 #pragma unroll
           for (int c0 = 0; c0 < D; c0 += 32) {
@@ -406,33 +477,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(&p_full[x]);
         ++cnt;
+        ++ci;
       }
-      if (ok && mbar_wait(&o_done[x], 0, status)) {
-        tc_fence_after();
-        const float inv_l = 1.f / l;
-        uint32_t ob[32];
-        __nv_bfloat16* orow = o + (((size_t)b * Hq + h) * L + i) * D;
+      if (!ok || !mbar_wait(&o_done[x], ko & 1, status)) {
+        ok = false;
+        break;
+      }
+      ++ko;
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+      uint32_t ob[32];
+      __nv_bfloat16* orow = o + (((size_t)b * Hq + h) * L + i) * D;
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          tmem_ld32(tO + c0, ob);
-          tmem_ld_wait();
-          if (i < L) {
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        tmem_ld32(tO + c0, ob);
+        tmem_ld_wait();
+        if (i < L) {
 #pragma unroll
-            for (int q = 0; q < 32; q += 8) {
-              uint4 pk;
-              pk.x = pack_bf16x2(__uint_as_float(ob[q]) * inv_l, __uint_as_float(ob[q + 1]) * inv_l);
-              pk.y = pack_bf16x2(__uint_as_float(ob[q + 2]) * inv_l,
-                                 __uint_as_float(ob[q + 3]) * inv_l);
-              pk.z = pack_bf16x2(__uint_as_float(ob[q + 4]) * inv_l,
-                                 __uint_as_float(ob[q + 5]) * inv_l);
-              pk.w = pack_bf16x2(__uint_as_float(ob[q + 6]) * inv_l,
-                                 __uint_as_float(ob[q + 7]) * inv_l);
-              *reinterpret_cast<uint4*>(orow + c0 + q) = pk;
-            }
+          for (int q = 0; q < 32; q += 8) {
+            uint4 pk;
+            pk.x = pack_bf16x2(__uint_as_float(ob[q]) * inv_l, __uint_as_float(ob[q + 1]) * inv_l);
+            pk.y = pack_bf16x2(__uint_as_float(ob[q + 2]) * inv_l,
+                               __uint_as_float(ob[q + 3]) * inv_l);
+            pk.z = pack_bf16x2(__uint_as_float(ob[q + 4]) * inv_l,
+                               __uint_as_float(ob[q + 5]) * inv_l);
+            pk.w = pack_bf16x2(__uint_as_float(ob[q + 6]) * inv_l,
+                               __uint_as_float(ob[q + 7]) * inv_l);
+            *reinterpret_cast<uint4*>(orow + c0 + q) = pk;
           }
         }
-        if (i < L) lse[((size_t)b * Hq + h) * L + i] = (m_used + __log2f(l)) * 0.69314718055994531f;
       }
+      if (i < L) lse[((size_t)b * Hq + h) * L + i] = (m_used + __log2f(l)) * 0.69314718055994531f;
+      tc_fence_before();
     }
   }
 
@@ -442,20 +518,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, C::TM_COLS);
 }
 
-template <int D, int NST>
+template <int D>
 int launch_fwd_impl(IndexPtrs idx, const void* q, const void* k, const void* v, void* o, float* lse,
                     int B, int Hq, int Hkv, int L, float scale, void* ws, int* status,
                     cudaStream_t s) {
-  using C = FwdCfg<D, NST>;
+  using C = FwdCfg<D>;
   const size_t plane_elems = (size_t)L * D;
   uint8_t* kk = static_cast<uint8_t*>(ws);
   uint8_t* vk = kk + align_up((size_t)B * Hkv * plane_elems * 2, 256);
-  dim3 ggrid((L + 63) / 64, Hkv, B);
+  const int sms = num_sms();
   profile_mark(0, s);
-  gather_keep_kernel<D><<<ggrid, 256, 0, s>>>(idx, static_cast<const uint4*>(k),
-                                               static_cast<const uint4*>(v),
-                                               reinterpret_cast<uint4*>(kk),
-                                               reinterpret_cast<uint4*>(vk), Hkv, L);
+  gather_keep_kernel<D><<<keep_pass_ctas(keep_units(B, Hkv, L), sms), 256, 0, s>>>(
+      idx, static_cast<const uint4*>(k), static_cast<const uint4*>(v),
+      reinterpret_cast<uint4*>(kk), reinterpret_cast<uint4*>(vk), B, Hkv, L);
   CUtensorMap mq, mk, mv, mkk, mvk;
   if (!make_bf16_map(&mq, q, (uint64_t)B * Hq, L, D, 128) ||
       !make_bf16_map(&mk, k, (uint64_t)B * Hkv, L, D, 128) ||
@@ -463,16 +538,16 @@ int launch_fwd_impl(IndexPtrs idx, const void* q, const void* k, const void* v, 
       !make_bf16_map(&mkk, kk, (uint64_t)B * Hkv, L, D, 128) ||
       !make_bf16_map(&mvk, vk, (uint64_t)B * Hkv, L, D, 128))
     return static_cast<int>(cudaErrorInvalidValue);
-  auto kern = attn_fwd_tc_kernel<D, NST>;
+  auto kern = attn_fwd_tc_kernel<D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return static_cast<int>(e);
   const float scale_log2 = scale * 1.4426950408889634f;
   const int T = (L + 127) / 128;
-  dim3 grid((T + 1) / 2, Hq, B);  // one CTA per pair of query tiles
+  const long long items = (long long)B * Hq * ((T + 1) / 2);
+  const int grid = static_cast<int>(items < sms ? items : sms);  // persistent: one CTA per SM
   profile_mark(1, s);
-  kern<<<grid, kThreads, C::SMEM, s>>>(mq, mk, mv, mkk, mvk, idx,
-                                       static_cast<__nv_bfloat16*>(o), lse, B, Hq, Hkv, L,
-                                       scale_log2, status);
+  kern<<<grid, kThreads, C::SMEM, s>>>(mq, mk, mv, mkk, mvk, idx, static_cast<__nv_bfloat16*>(o),
+                                       lse, B, Hq, Hkv, L, scale_log2, status);
   const cudaError_t err = cudaGetLastError();
   profile_mark(2, s);
   return static_cast<int>(err);
@@ -488,9 +563,8 @@ int launch_attn_fwd_tc(IndexPtrs idx, const void* q, const void* k, const void* 
                        float* lse, int B, int Hq, int Hkv, int L, int d, float scale, void* ws,
                        int* status, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (d == 64) return launch_fwd_impl<64, 4>(idx, q, k, v, o, lse, B, Hq, Hkv, L, scale, ws,
-                                             status, s);
-  return launch_fwd_impl<128, 2>(idx, q, k, v, o, lse, B, Hq, Hkv, L, scale, ws, status, s);
+  if (d == 64) return launch_fwd_impl<64>(idx, q, k, v, o, lse, B, Hq, Hkv, L, scale, ws, status, s);
+  return launch_fwd_impl<128>(idx, q, k, v, o, lse, B, Hq, Hkv, L, scale, ws, status, s);
 }
 
 }  // namespace sep

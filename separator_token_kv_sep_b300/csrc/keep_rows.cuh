@@ -1,0 +1,150 @@
+// Keep-token rows of K and V copied into dense tiles, and their gradients
+// copied back.
+//
+// The tokens every query sees before its window (the first a tokens and the
+// separators: anthology record lit-748, Key takeaways, "The mask") are read by
+// every query tile.  Gathering them once into K_keep[b, g, r] =
+// K[b, g, keep_pos[b][r]] (r < keep_count[b], zero rows up to the next
+// multiple of 128) turns them into full 128-row tiles that TMA can load.
+//
+// Work is cut into units of 16 rows of one (batch, kv head) plane and one
+// warp takes a unit.  Units are numbered chunk-major (unit = chunk * planes
+// + plane), so the units that hold rows come first and the kernels below use
+// a grid of a few CTAs per SM that strides over them; a unit past its plane's
+// padded keep count costs one cached load.
+#pragma once
+
+#include "common.cuh"
+#include "layout.h"
+
+namespace sep {
+
+constexpr int kKeepUnitRows = 16;
+
+__host__ __device__ inline int keep_units(int B, int Hkv, int L) {
+  return B * Hkv * ((L + kKeepUnitRows - 1) / kKeepUnitRows);
+}
+
+// Copies the keep rows of one unit (and, if dk_keep is set, zeroes the same
+// rows of the fp32 gradient accumulators dk_keep / dv_keep).
+template <int D>
+__device__ __forceinline__ void gather_keep_unit(IndexPtrs idx, const uint4* __restrict__ k,
+                                                 const uint4* __restrict__ v,
+                                                 uint4* __restrict__ kk, uint4* __restrict__ vk,
+                                                 float4* __restrict__ dk_keep,
+                                                 float4* __restrict__ dv_keep, int B, int Hkv,
+                                                 int L, int unit, int lane) {
+  constexpr int U = D / 8;                         // 16-byte units of a bf16 row
+  constexpr int PER = kKeepUnitRows * U / 32;      // per lane
+  const int planes = B * Hkv;
+  const int plane = unit % planes, row0 = (unit / planes) * kKeepUnitRows;
+  const int b = plane / Hkv;
+  const int count = min(max(idx.keep_count[b], 0), L);
+  const int end = min(L, (count + 127) / 128 * 128);
+  if (row0 >= end) return;
+  const int32_t* kpos = idx.keep_pos + (size_t)b * L;
+  const size_t base = (size_t)plane * L * U;
+  uint4 kv[PER], vv[PER];
+#pragma unroll
+  for (int x = 0; x < PER; ++x) {
+    const int e = x * 32 + lane;
+    const int row = row0 + e / U, u = e % U;
+    const int src = row < count ? kpos[row] : -1;
+    kv[x] = make_uint4(0, 0, 0, 0);
+    vv[x] = make_uint4(0, 0, 0, 0);
+    if (src >= 0 && src < L) {
+      kv[x] = k[base + (size_t)src * U + u];
+      vv[x] = v[base + (size_t)src * U + u];
+    }
+  }
+#pragma unroll
+  for (int x = 0; x < PER; ++x) {
+    const int e = x * 32 + lane;
+    const int row = row0 + e / U, u = e % U;
+    if (row < end) {
+      kk[base + (size_t)row * U + u] = kv[x];
+      vk[base + (size_t)row * U + u] = vv[x];
+    }
+  }
+  if (dk_keep) {
+    constexpr int U4 = D / 4;  // float4 of an fp32 row
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    const size_t base4 = (size_t)plane * L * U4;
+#pragma unroll
+    for (int x = 0; x < 2 * PER; ++x) {
+      const int e = x * 32 + lane;
+      const int row = row0 + e / U4;
+      if (row < end) {
+        dk_keep[base4 + (size_t)row * U4 + e % U4] = z;
+        dv_keep[base4 + (size_t)row * U4 + e % U4] = z;
+      }
+    }
+  }
+}
+
+// dK / dV rows of the keep tokens of one unit, from the fp32 accumulators
+// (dK times the softmax scale), rounded to bf16 once.
+template <int D>
+__device__ __forceinline__ void scatter_keep_unit(IndexPtrs idx, const float4* __restrict__ dk_keep,
+                                                  const float4* __restrict__ dv_keep,
+                                                  __nv_bfloat16* __restrict__ dk,
+                                                  __nv_bfloat16* __restrict__ dv, int B, int Hkv,
+                                                  int L, float scale, int unit, int lane) {
+  constexpr int U4 = D / 4;
+  constexpr int PER = kKeepUnitRows * U4 / 32;
+  const int planes = B * Hkv;
+  const int plane = unit % planes, row0 = (unit / planes) * kKeepUnitRows;
+  const int b = plane / Hkv;
+  const int count = min(max(idx.keep_count[b], 0), L);
+  if (row0 >= count) return;
+  const int32_t* kpos = idx.keep_pos + (size_t)b * L;
+  const size_t base4 = (size_t)plane * L * U4;
+  float4 a[PER], c[PER];
+#pragma unroll
+  for (int x = 0; x < PER; ++x) {
+    const int e = x * 32 + lane;
+    const int row = row0 + e / U4;
+    a[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+    c[x] = a[x];
+    if (row < count) {
+      a[x] = dk_keep[base4 + (size_t)row * U4 + e % U4];
+      c[x] = dv_keep[base4 + (size_t)row * U4 + e % U4];
+    }
+  }
+#pragma unroll
+  for (int x = 0; x < PER; ++x) {
+    const int e = x * 32 + lane;
+    const int row = row0 + e / U4, u = e % U4;
+    if (row >= count) continue;
+    const int j = kpos[row];
+    if (j < 0 || j >= L) continue;
+    uint2 ko, vo;
+    ko.x = pack_bf16x2(a[x].x * scale, a[x].y * scale);
+    ko.y = pack_bf16x2(a[x].z * scale, a[x].w * scale);
+    vo.x = pack_bf16x2(c[x].x, c[x].y);
+    vo.y = pack_bf16x2(c[x].z, c[x].w);
+    const size_t dst = ((size_t)plane * L + j) * D + 4 * u;
+    *reinterpret_cast<uint2*>(dk + dst) = ko;
+    *reinterpret_cast<uint2*>(dv + dst) = vo;
+  }
+}
+
+// Number of SMs of the current device (148 if the query fails).
+inline int num_sms() {
+  static int n[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!n[dev] && cudaDeviceGetAttribute(&n[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    n[dev] = 148;
+  return n[dev];
+}
+
+// CTAs of 256 threads for a keep-row pass over `units` units: a few per SM,
+// at most one warp per unit.
+inline int keep_pass_ctas(long long units, int sms) {
+  const long long want = (units + 7) / 8;
+  const long long cap = 4LL * sms;
+  return static_cast<int>(want < 1 ? 1 : (want < cap ? want : cap));
+}
+
+}  // namespace sep
