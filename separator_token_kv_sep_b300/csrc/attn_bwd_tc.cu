@@ -43,6 +43,7 @@ constexpr int kThreads = 320;      // warp 0 TMA, warp 1 MMA, warps 2-9 elementw
 constexpr int kEwThreads = 256;    // two elementwise warpgroups
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kKeepChunk = 4;      // query tiles per CTA of the keep-tile dK/dV kernel
+constexpr int kCtaItems = 128;     // work items a dK/dV CTA keeps in static shared memory
 
 __device__ __forceinline__ uint32_t range_bits(int lo, int hi, int w) {
   // bits c of word w (columns 32w .. 32w+31) with lo <= c < hi
@@ -278,7 +279,7 @@ struct KvCfg {
   // +64); accumulator buffer b: dV at TM_ACC + 2bD, dK at TM_ACC + 2bD + D
   static constexpr int TM_ACC = 256;
   static constexpr int TM_COLS = 512;
-  static_assert(SMEM <= 227 * 1024, "shared memory");
+  static_assert(SMEM + 16 * kCtaItems + 256 <= 227 * 1024, "shared memory");
   static_assert(TM_ACC + ACB * 2 * D <= TM_COLS, "tensor memory");
 };
 
@@ -320,6 +321,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
   const int n_win = hdr.n;
+  // this CTA's items (i = blockIdx.x + k * gridDim.x), read once; items past
+  // kCtaItems are read from global memory
+  __shared__ int4 s_items[kCtaItems];
+  for (int x = threadIdx.x; x < kCtaItems; x += blockDim.x) {
+    const int i = static_cast<int>(blockIdx.x) + x * static_cast<int>(gridDim.x);
+    if (i < n_items) s_items[x] = items[i];
+  }
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < KVB; ++i) {
@@ -354,8 +362,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   struct Item {
     int kind, b, g, row0, t0, nt;
   };
-  auto item_at = [&](int i) -> Item {
-    const int4 it = items[i];
+  auto item_at = [&](int i, int k) -> Item {  // item i, the k-th of this CTA
+    const int4 it = k < kCtaItems ? s_items[k] : items[i];
     Item r;
     r.kind = it.x;
     r.b = it.y / Hkv;
@@ -372,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int k = 0, ug = 0, kv_issued = 0;
       bool ok = true;
       for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x, ++k) {
-        const Item it = item_at(i);
+        const Item it = item_at(i, k);
         const int kb = k % KVB;
         if (k >= KVB && !mbar_wait(&kv_empty[kb], ((k / KVB) - 1) & 1, status)) {
           ok = false;
@@ -442,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto cur_load = [&](Cur& c) {
         if (c.i < n_items) {
-          c.it = item_at(c.i);
+          c.it = item_at(c.i, c.k);
           c.nU = G * c.it.nt;
         }
       };
@@ -548,18 +556,73 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = quad * 32 + lane;  // key row of the tile
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t tb = tmem + lane_base + 128 * half;
+    // accumulators of item k -> global memory (half 0 dV, half 1 dK)
+    struct Epi {
+      int k;
+      long long rm;  // 4 * row + mode: row of [B*Hkv*L]; mode 1 keep accumulator, 2 output
+    };
+    const float osc = half ? scale : 1.f;
+    auto epilogue = [&](const Epi& e) -> bool {
+      const int ab = e.k % ACB;
+      if (!mbar_wait(&acc_full[ab], (e.k / ACB) & 1, status)) return false;
+      tc_fence_after();
+      const uint32_t tm_acc = tmem + C::TM_ACC + ab * 2 * D + half * D;
+      const int mode = static_cast<int>(e.rm & 3);
+      const size_t row = static_cast<size_t>(e.rm >> 2);
+      float* accr = (half ? dk_keep : dv_keep) + row * D;
+      __nv_bfloat16* outr = (half ? dk : dv) + row * D;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t vb[32];
+        tmem_ld32(tm_acc + lane_base + c0, vb);
+        tmem_ld_wait();
+        if (mode == 1) {
+#pragma unroll
+          for (int x = 0; x < 32; x += 4)
+            red_add_v4(accr + c0 + x, __uint_as_float(vb[x]), __uint_as_float(vb[x + 1]),
+                       __uint_as_float(vb[x + 2]), __uint_as_float(vb[x + 3]));
+        } else if (mode == 2) {
+#pragma unroll
+          for (int x = 0; x < 32; x += 8) {
+            uint4 ov;
+            ov.x = pack_bf16x2(__uint_as_float(vb[x]) * osc, __uint_as_float(vb[x + 1]) * osc);
+            ov.y = pack_bf16x2(__uint_as_float(vb[x + 2]) * osc, __uint_as_float(vb[x + 3]) * osc);
+            ov.z = pack_bf16x2(__uint_as_float(vb[x + 4]) * osc, __uint_as_float(vb[x + 5]) * osc);
+            ov.w = pack_bf16x2(__uint_as_float(vb[x + 6]) * osc, __uint_as_float(vb[x + 7]) * osc);
+            *reinterpret_cast<uint4*>(outr + c0 + x) = ov;
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&acc_empty[ab]);
+      return true;
+    };
+    constexpr bool kDeferEpi = ACB >= 2;
+    Epi pe{};
+    bool pend = false;
     int k = 0, ug = 0;
     bool ok = true;
     for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x, ++k) {
-      const Item it = item_at(i);
+      const Item it = item_at(i, k);
       const bool keep = it.kind == kItemKeep;
-      const int ab = k % ACB;
       const int count = min(max(idx.keep_count[it.b], 0), L);
       const int32_t* blocks = idx.blocks + (size_t)it.b * T * 4;
       const int j = it.row0 + r;  // KEEP: keep index; DENSE: key position
       bool keep_j = false;
       if (!keep && j < L)
         keep_j = (idx.keep_bits[(size_t)it.b * hdr.nwords + (j >> 5)] >> (j & 31)) & 1u;
+      // this item's epilogue: KEEP rows and DENSE keep tokens add into the
+      // fp32 keep accumulators (written to dK/dV by the scatter kernel);
+      // other DENSE rows are final
+      Epi e;
+      e.k = k;
+      {
+        const bool to_acc = keep ? (j < count) : (j < L && keep_j);
+        const bool to_out = !keep && j < L && !keep_j;
+        const int kidx = keep ? j : (keep_j ? idx.keep_prefix[(size_t)it.b * (L + 1) + j] : 0);
+        const long long plane = (long long)it.b * Hkv + it.g;
+        e.rm = to_acc ? (((plane * L + kidx) << 2) | 1) : to_out ? (((plane * L + j) << 2) | 2) : 0;
+      }
       const int nU = G * it.nt;
       int4 blk_next = *reinterpret_cast<const int4*>(blocks + 4 * it.t0);
       for (int u = 0; u < nU; ++u) {
@@ -632,47 +695,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       ug += nU;
-      // ---- epilogue of the item: accumulators -> global (half 0 dV, half 1 dK)
-      if (!mbar_wait(&acc_full[ab], (k / ACB) & 1, status)) {
-        ok = false;
+      // with two accumulator buffers the epilogue of item k runs after the
+      // half-tiles of item k + 1, whose S / dP products overlap it
+      if (kDeferEpi) {
+        if (pend && !(ok = epilogue(pe))) break;
+        pe = e;
+        pend = true;
+      } else if (!(ok = epilogue(e))) {
         break;
       }
-      tc_fence_after();
-      const uint32_t tm_acc = tmem + C::TM_ACC + ab * 2 * D + half * D;
-      // KEEP rows and DENSE keep tokens add into the fp32 keep accumulators
-      // (written to dK/dV by the scatter kernel); other DENSE rows are final.
-      const bool to_acc = keep ? (j < count) : (j < L && keep_j);
-      const bool to_out = !keep && j < L && !keep_j;
-      const int kidx = keep ? j : (keep_j ? idx.keep_prefix[(size_t)it.b * (L + 1) + j] : 0);
-      float* accr = (half ? dk_keep : dv_keep) + (((size_t)it.b * Hkv + it.g) * L + kidx) * D;
-      __nv_bfloat16* outr =
-          (half ? dk : dv) + (((size_t)it.b * Hkv + it.g) * L + (to_out ? j : 0)) * D;
-      const float osc = half ? scale : 1.f;
-#pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t vb[32];
-        tmem_ld32(tm_acc + lane_base + c0, vb);
-        tmem_ld_wait();
-        if (to_acc) {
-#pragma unroll
-          for (int x = 0; x < 32; x += 4)
-            red_add_v4(accr + c0 + x, __uint_as_float(vb[x]), __uint_as_float(vb[x + 1]),
-                       __uint_as_float(vb[x + 2]), __uint_as_float(vb[x + 3]));
-        } else if (to_out) {
-#pragma unroll
-          for (int x = 0; x < 32; x += 8) {
-            uint4 ov;
-            ov.x = pack_bf16x2(__uint_as_float(vb[x]) * osc, __uint_as_float(vb[x + 1]) * osc);
-            ov.y = pack_bf16x2(__uint_as_float(vb[x + 2]) * osc, __uint_as_float(vb[x + 3]) * osc);
-            ov.z = pack_bf16x2(__uint_as_float(vb[x + 4]) * osc, __uint_as_float(vb[x + 5]) * osc);
-            ov.w = pack_bf16x2(__uint_as_float(vb[x + 6]) * osc, __uint_as_float(vb[x + 7]) * osc);
-            *reinterpret_cast<uint4*>(outr + c0 + x) = ov;
-          }
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(&acc_empty[ab]);
     }
+    if (kDeferEpi && ok && pend) epilogue(pe);
   }
 
   tc_fence_before();
@@ -712,7 +745,9 @@ struct DqCfg {
   static constexpr int SMEM = OFF_DS + 2 * kChunk + 1024;
   static constexpr int TM_S = 0, TM_DP = 128, TM_DQ = 256;  // dQ buffer b at +bD
   static constexpr int TM_COLS = 512;
-  static_assert(SMEM <= 227 * 1024, "shared memory");
+  // block records of the CTA's first ITEMS items, in static shared memory
+  static constexpr int ITEMS = D == 64 ? 128 : 48;
+  static_assert(SMEM + 16 * ITEMS + 256 <= 227 * 1024, "shared memory");
   static_assert(TM_DQ + 2 * D <= TM_COLS, "tensor memory");
 };
 
@@ -768,6 +803,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&mma_final, 1);
     fence_mbar_init();
   }
+  // block records of this CTA's items (i = blockIdx.x + k * gridDim.x),
+  // read once; items past C::ITEMS read theirs from global memory
+  __shared__ int4 s_blk[C::ITEMS];
+  for (int x = threadIdx.x; x < C::ITEMS; x += blockDim.x) {
+    const int i = static_cast<int>(blockIdx.x) + x * static_cast<int>(gridDim.x);
+    if (i < n_items) {
+      const int bh = i % (B * Hq);
+      s_blk[x] = *reinterpret_cast<const int4*>(idx.blocks +
+                                                ((size_t)(bh / Hq) * T + (T - 1 - i / (B * Hq))) * 4);
+    }
+  }
   if (warp == 1) {
     tmem_alloc(&tmem_slot, C::TM_COLS);
     tmem_relinquish();
@@ -781,14 +827,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     int b, h, g, t, n_gather, lo, hi, nG, nT;
     bool ok;
   };
-  auto item_at = [&](int i) -> Item {
+  auto item_at = [&](int i, int k) -> Item {  // item i, the k-th of this CTA
     Item r;
     r.t = T - 1 - i / (B * Hq);
     const int bh = i % (B * Hq);
     r.b = bh / Hq;
     r.h = bh % Hq;
     r.g = r.h / (Hq / Hkv);
-    const int4 blk = *reinterpret_cast<const int4*>(idx.blocks + ((size_t)r.b * T + r.t) * 4);
+    const int4 blk = k < C::ITEMS
+                         ? s_blk[k]
+                         : *reinterpret_cast<const int4*>(idx.blocks + ((size_t)r.b * T + r.t) * 4);
     r.n_gather = blk.x;
     r.lo = blk.y;
     r.hi = blk.z;
@@ -805,7 +853,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int k = 0, ug = 0, qd_issued = 0;
       bool ok = true;
       for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x, ++k) {
-        const Item it = item_at(i);
+        const Item it = item_at(i, k);
         if (!it.ok) {
           report(status, SEP_ERR_DEVICE_BOUNDS);
           ok = false;
@@ -861,7 +909,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int k = 0, ug = 0;
       bool ok = true;
       for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x, ++k) {
-        const Item it = item_at(i);
+        const Item it = item_at(i, k);
         if (!it.ok) break;
         const int qb = k % QB, ab = k & 1;
         const uint32_t q_base = smem_u32(smem + C::OFF_QD + qb * 2 * C::TILE);
@@ -950,7 +998,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int k = 0, ug = 0;
     bool ok = true;
     for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x, ++k) {
-      const Item it = item_at(i);
+      const Item it = item_at(i, k);
       if (!it.ok) break;
       const int ab = k & 1;
       const int i_row = it.t * 128 + r;

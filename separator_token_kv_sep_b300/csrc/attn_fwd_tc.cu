@@ -66,7 +66,7 @@ struct FwdCfg {
   // first 64 columns as packed bf16) and the O accumulator (D columns)
   static constexpr int TM_S0 = 0, TM_O0 = 128, TM_S1 = 256, TM_O1 = 384;
   static constexpr int TM_COLS = 512;
-  static_assert(SMEM <= 227 * 1024, "shared memory");
+  static_assert(SMEM + 32 * 64 + 256 <= 227 * 1024, "shared memory (with the item records)");
 };
 
 constexpr int kThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-5 softmax A, 6-9 softmax B
@@ -101,8 +101,26 @@ struct PairPlan {
   }
 };
 
-__device__ __forceinline__ PairPlan load_plan(IndexPtrs idx, int item, int n_items, int B, int Hq,
-                                              int L, int T) {
+constexpr int kCtaItems = 64;  // items whose block records a CTA keeps in shared memory
+
+// Block records (A, B) of the CTA's k-th item, from shared memory for the
+// first kCtaItems items.
+__device__ __forceinline__ void item_records(IndexPtrs idx, const int4* s_rec, int item, int B,
+                                             int Hq, int T, int4& ba, int4& bb) {
+  const int k = (item - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x);
+  if (k < kCtaItems) {
+    ba = s_rec[2 * k];
+    bb = s_rec[2 * k + 1];
+    return;
+  }
+  const int P = (T + 1) >> 1, BH = B * Hq;
+  const int b = (item % BH) / Hq, tA = 2 * (P - 1 - item / BH);
+  ba = *reinterpret_cast<const int4*>(idx.blocks + ((size_t)b * T + tA) * 4);
+  bb = tA + 1 < T ? *reinterpret_cast<const int4*>(idx.blocks + ((size_t)b * T + tA + 1) * 4) : ba;
+}
+
+__device__ __forceinline__ PairPlan load_plan(IndexPtrs idx, const int4* s_rec, int item,
+                                              int n_items, int B, int Hq, int L, int T) {
   PairPlan pl;
   pl.valid = false;
   pl.nT = 0;
@@ -113,10 +131,8 @@ __device__ __forceinline__ PairPlan load_plan(IndexPtrs idx, int item, int n_ite
   pl.h = bh % Hq;
   pl.tA = 2 * pair;
   pl.hasB = pl.tA + 1 < T;
-  const int4 ba = *reinterpret_cast<const int4*>(idx.blocks + ((size_t)pl.b * T + pl.tA) * 4);
-  const int4 bb =
-      pl.hasB ? *reinterpret_cast<const int4*>(idx.blocks + ((size_t)pl.b * T + pl.tA + 1) * 4)
-              : ba;
+  int4 ba, bb;
+  item_records(idx, s_rec, item, B, Hq, T, ba, bb);
   pl.nA = ba.x; pl.loA = ba.y; pl.hiA = ba.z;
   pl.nB = bb.x; pl.loB = bb.y; pl.hiB = bb.z;
   auto bad = [&](int4 r, int q0) {
@@ -161,6 +177,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
   const int n_win = hdr.n;
+  // block records of this CTA's items (item = blockIdx.x + k * G), read once
+  __shared__ int4 s_rec[2 * kCtaItems];
+  for (int x = threadIdx.x; x < kCtaItems; x += blockDim.x) {
+    const int item = static_cast<int>(blockIdx.x) + x * G;
+    if (item < n_items) {
+      const int P = (T + 1) >> 1, BH = B * Hq;
+      const int b = (item % BH) / Hq, tA = 2 * (P - 1 - item / BH);
+      const int4 ra = *reinterpret_cast<const int4*>(idx.blocks + ((size_t)b * T + tA) * 4);
+      s_rec[2 * x] = ra;
+      s_rec[2 * x + 1] =
+          tA + 1 < T ? *reinterpret_cast<const int4*>(idx.blocks + ((size_t)b * T + tA + 1) * 4) : ra;
+    }
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < QB; ++s) {
@@ -199,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int n = 0, kq = 0;  // K/V stages and query pairs loaded
       bool ok = true;
       for (int it = blockIdx.x; ok && it < n_items; it += G) {
-        const PairPlan pl = load_plan(idx, it, n_items, B, Hq, L, T);
+        const PairPlan pl = load_plan(idx, s_rec, it, n_items, B, Hq, L, T);
         if (!pl.valid) {
           report(status, SEP_ERR_DEVICE_BOUNDS);
           continue;
@@ -287,16 +316,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       bool ok = true;
       int it = blockIdx.x;
-      PairPlan pc = load_plan(idx, it, n_items, B, Hq, L, T);
+      PairPlan pc = load_plan(idx, s_rec, it, n_items, B, Hq, L, T);
       while (it < n_items && !pc.valid) {
         it += G;
-        pc = load_plan(idx, it, n_items, B, Hq, L, T);
+        pc = load_plan(idx, s_rec, it, n_items, B, Hq, L, T);
       }
       if (it < n_items) {
         int kq = 0, qs = 0, n = 0;  // current item's index and Q buffer; K/V stage count
         int u = pc.next(-1);
         int itn = it + G;
-        PairPlan pn = load_plan(idx, itn, n_items, B, Hq, L, T);  // prefetched
+        PairPlan pn = load_plan(idx, s_rec, itn, n_items, B, Hq, L, T);  // prefetched
         ok = mbar_wait(&q_full[0], 0, status) && mbar_wait(&kv_full[0], 0, status);
         tc_fence_after();
         if (ok) {
@@ -311,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!same) {
             while (itn < n_items && !pn.valid) {
               itn += G;
-              pn = load_plan(idx, itn, n_items, B, Hq, L, T);
+              pn = load_plan(idx, s_rec, itn, n_items, B, Hq, L, T);
             }
             if (itn < n_items) un = pn.next(-1);
           }
@@ -342,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             qs = qsn;
             ci0 = ci1 = 0;
             itn = it + G;
-            pn = load_plan(idx, itn, n_items, B, Hq, L, T);
+            pn = load_plan(idx, s_rec, itn, n_items, B, Hq, L, T);
           }
           u = un;
         }
@@ -363,10 +392,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nwords = hdr.nwords;
     int cnt = 0, ko = 0;  // S tiles and items finished by this query tile
     bool ok = true;
-    PairPlan pn = load_plan(idx, blockIdx.x, n_items, B, Hq, L, T);
+    PairPlan pn = load_plan(idx, s_rec, blockIdx.x, n_items, B, Hq, L, T);
     for (int it = blockIdx.x; ok && it < n_items; it += G) {
       const PairPlan pl = pn;
-      pn = load_plan(idx, it + G, n_items, B, Hq, L, T);  // prefetch the next item
+      pn = load_plan(idx, s_rec, it + G, n_items, B, Hq, L, T);  // prefetch the next item
       if (!pl.valid || (x == 1 && !pl.hasB)) continue;
       const int b = pl.b, h = pl.h;
       const int i = (pl.tA + x) * 128 + r;
