@@ -438,7 +438,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // bf16), which the dV / dK products then read from TMEM.  Order:
     // S/dP(u,0), S/dP(u,1), then per half-tile j: dV/dK(j), S/dP(j+2) --
     // the two warpgroups' chains interleave on the tensor pipe.
-    if (lane == 0) {
+    // The whole warp runs this loop; the elected lane issues.
+    {
+      const bool leader = elect_one();
       constexpr uint32_t idesc_sd = idesc_bf16_f32(128, 64, false, false);
       constexpr uint32_t idesc_acc = idesc_bf16_f32(128, D, false, true);
       const uint32_t q_base = smem_u32(smem + C::OFF_Q), do_base = smem_u32(smem + C::OFF_DO);
@@ -473,27 +475,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_sd = [&](const Cur& c) -> bool {  // S^T / dP^T of half-tile c
         const int kb = c.k % KVB, st = c.ug % NST;
         if (c.u == 0 && c.h == 0) {
-          if (!mbar_wait(&kv_full[kb], (c.k / KVB) & 1, status)) return false;
+          if (!mbar_wait_warp(&kv_full[kb], (c.k / KVB) & 1, status)) return false;
         }
         if (c.h == 0) {
-          if (!mbar_wait(&qd_full[st], (c.ug / NST) & 1, status)) return false;
+          if (!mbar_wait_warp(&qd_full[st], (c.ug / NST) & 1, status)) return false;
         }
         tc_fence_after();
         const uint64_t dk = dsc_kv + ((kb * 2 * C::TILE) >> 4), dv = dk + (C::TILE >> 4);
         const uint64_t qo = (st * C::TILE + 8192 * c.h) >> 4;  // query rows 64h .. 64h+63
         const uint64_t dq = dsc_q + qo, ddo = dsc_do + qo;
         const uint32_t tb = tmem + 128 * c.h;
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * kChunk + (kk & 3) * 32) >> 4;
-          umma_bf16_ss(tb, dk + off, dq + off, idesc_sd, kk > 0);
-        }
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = ((kk >> 2) * kChunk + (kk & 3) * 32) >> 4;
+            umma_bf16_ss(tb, dk + off, dq + off, idesc_sd, kk > 0);
+          }
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * kChunk + (kk & 3) * 32) >> 4;
-          umma_bf16_ss(tb + 64, dv + off, ddo + off, idesc_sd, kk > 0);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = ((kk >> 2) * kChunk + (kk & 3) * 32) >> 4;
+            umma_bf16_ss(tb + 64, dv + off, ddo + off, idesc_sd, kk > 0);
+          }
+          umma_commit(&sd_full[c.h]);
         }
-        umma_commit(&sd_full[c.h]);
+        __syncwarp();
         return true;
       };
       Cur cs{static_cast<int>(blockIdx.x), 0, 0, 0, 0, 0, Item{}};  // next S/dP to issue
@@ -516,36 +521,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ab = ca.k % ACB, st = ca.ug % NST, kb = ca.k % KVB;
         if (ca.u == 0 && ca.h == 0 && ca.k >= ACB) {
           // the epilogue has drained this accumulator buffer
-          if (!(ok = mbar_wait(&acc_empty[ab], ((ca.k / ACB) - 1) & 1, status))) break;
+          if (!(ok = mbar_wait_warp(&acc_empty[ab], ((ca.k / ACB) - 1) & 1, status))) break;
         }
-        if (!(ok = mbar_wait(&ps_full[ca.h], ca.ug & 1, status))) break;
+        if (!(ok = mbar_wait_warp(&ps_full[ca.h], ca.ug & 1, status))) break;
         tc_fence_after();
         const uint32_t tb = tmem + 128 * ca.h;
         const uint32_t tm_dv = tmem + C::TM_ACC + ab * 2 * D, tm_dk = tm_dv + D;
         const uint64_t qo = (st * C::TILE + 8192 * ca.h) >> 4;
         const uint64_t ddo = dsc_do_mn + qo, dq = dsc_q_mn + qo;
         const uint32_t first = (ca.u > 0 || ca.h > 0) ? 1u : 0u;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {  // 16 queries per step
-          const uint32_t acc = kk > 0 ? 1u : first;
-          umma_bf16_ts(tm_dv, tb + 8 * kk, ddo + ((kk * 2048) >> 4), idesc_acc, acc);
-          umma_bf16_ts(tm_dk, tb + 64 + 8 * kk, dq + ((kk * 2048) >> 4), idesc_acc, acc);
-        }
         const bool last_h = ca.h == 1, last_u = ca.u + 1 == ca.nU;
-        if (last_h) umma_commit(&qd_empty[st]);  // Q / dO / stats of this tile are done
-        if (last_h && last_u) {
-          umma_commit(&kv_empty[kb]);  // every MMA reading this item's K and V is issued
-          umma_commit(&acc_full[ab]);
+        if (leader) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {  // 16 queries per step
+            const uint32_t acc = kk > 0 ? 1u : first;
+            umma_bf16_ts(tm_dv, tb + 8 * kk, ddo + ((kk * 2048) >> 4), idesc_acc, acc);
+            umma_bf16_ts(tm_dk, tb + 64 + 8 * kk, dq + ((kk * 2048) >> 4), idesc_acc, acc);
+          }
+          if (last_h) umma_commit(&qd_empty[st]);  // Q / dO / stats of this tile are done
+          if (last_h && last_u) {
+            umma_commit(&kv_empty[kb]);  // every MMA reading this item's K and V is issued
+            umma_commit(&acc_full[ab]);
+          }
         }
+        __syncwarp();
         cur_next(ca);
         --ahead;
         if (!(ok = top_up())) break;
       }
-      // every MMA issued by this thread completes before TMEM is released
-      umma_commit(&mma_final);
-      mbar_wait(&mma_final, 0, status);
+      // every MMA issued by the leader completes before TMEM is released
+      if (leader) umma_commit(&mma_final);
+      __syncwarp();
+      mbar_wait_warp(&mma_final, 0, status);
     }
-    __syncwarp();
   } else {
     // ---------------------------------------------------------- elementwise
     // Warpgroup `half` owns query columns [64 half, 64 half + 64) of every
@@ -901,7 +909,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs this loop; the elected lane issues.
+    {
+      const bool leader = elect_one();
       constexpr uint32_t idesc_ss = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idesc_acc = idesc_bf16_f32(128, D, false, true);
       const uint32_t k_base = smem_u32(smem + C::OFF_K), v_base = smem_u32(smem + C::OFF_V),
@@ -915,31 +925,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t q_base = smem_u32(smem + C::OFF_QD + qb * 2 * C::TILE);
         const uint32_t do_base = q_base + C::TILE;
         const uint32_t tm_dq = tmem + C::TM_DQ + ab * D;
-        if (!mbar_wait(&qd_full[qb], (k / QB) & 1, status)) {
+        if (!mbar_wait_warp(&qd_full[qb], (k / QB) & 1, status)) {
           ok = false;
           break;
         }
         tc_fence_after();
         auto issue_sdp = [&](int ugl) -> bool {
           const int st = ugl % NST;
-          if (!mbar_wait(&kv_full[st], (ugl / NST) & 1, status)) return false;
+          if (!mbar_wait_warp(&kv_full[st], (ugl / NST) & 1, status)) return false;
           tc_fence_after();
+          if (leader) {
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
-            umma_bf16_ss(tmem + C::TM_S, sdesc_sw128(q_base + off, 16, 1024),
-                         sdesc_sw128(k_base + st * C::TILE + off, 16, 1024), idesc_ss, kk > 0);
-          }
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
+              umma_bf16_ss(tmem + C::TM_S, sdesc_sw128(q_base + off, 16, 1024),
+                           sdesc_sw128(k_base + st * C::TILE + off, 16, 1024), idesc_ss, kk > 0);
+            }
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
-            umma_bf16_ss(tmem + C::TM_DP, sdesc_sw128(do_base + off, 16, 1024),
-                         sdesc_sw128(v_base + st * C::TILE + off, 16, 1024), idesc_ss, kk > 0);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
+              umma_bf16_ss(tmem + C::TM_DP, sdesc_sw128(do_base + off, 16, 1024),
+                           sdesc_sw128(v_base + st * C::TILE + off, 16, 1024), idesc_ss, kk > 0);
+            }
+            umma_commit(&sd_full);
           }
-          umma_commit(&sd_full);
+          __syncwarp();
           return true;
         };
-        if (ug > 0 && !mbar_wait(&sd_free, (ug - 1) & 1, status)) {
+        if (ug > 0 && !mbar_wait_warp(&sd_free, (ug - 1) & 1, status)) {
           ok = false;
           break;
         }
@@ -947,7 +960,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        if (k >= 2 && !mbar_wait(&acc_empty[ab], ((k >> 1) - 1) & 1, status)) {
+        if (k >= 2 && !mbar_wait_warp(&acc_empty[ab], ((k >> 1) - 1) & 1, status)) {
           ok = false;
           break;
         }
@@ -955,34 +968,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int u = 0; ok && u < it.nT; ++u) {
           const int ugl = ug + u;
           if (u + 1 < it.nT) {
-            ok = mbar_wait(&sd_free, ugl & 1, status) && issue_sdp(ugl + 1);
+            ok = mbar_wait_warp(&sd_free, ugl & 1, status) && issue_sdp(ugl + 1);
             if (!ok) break;
           }
-          if (!mbar_wait(&ds_full, ugl & 1, status)) {
+          if (!mbar_wait_warp(&ds_full, ugl & 1, status)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const int st = ugl % NST;
+          if (leader) {
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t aoff = (kk >> 2) * kChunk + (kk & 3) * 32;
-            umma_bf16_ss(tm_dq, sdesc_sw128(ds_base + aoff, 16, 1024),
-                         sdesc_sw128(k_base + st * C::TILE + kk * 2048, kChunk, 1024), idesc_acc,
-                         (u > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t aoff = (kk >> 2) * kChunk + (kk & 3) * 32;
+              umma_bf16_ss(tm_dq, sdesc_sw128(ds_base + aoff, 16, 1024),
+                           sdesc_sw128(k_base + st * C::TILE + kk * 2048, kChunk, 1024),
+                           idesc_acc, (u > 0 || kk > 0) ? 1u : 0u);
+            }
+            umma_commit(&dq_done);
+            umma_commit(&kv_empty[st]);
+            if (u + 1 == it.nT) umma_commit(&qd_empty[qb]);  // Q / dO of this item are done
           }
-          umma_commit(&dq_done);
-          umma_commit(&kv_empty[st]);
-          if (u + 1 == it.nT) umma_commit(&qd_empty[qb]);  // Q / dO of this item are done
+          __syncwarp();
         }
         if (!ok) break;
-        umma_commit(&acc_full[ab]);
+        if (leader) umma_commit(&acc_full[ab]);
         ug += it.nT;
       }
-      umma_commit(&mma_final);
-      mbar_wait(&mma_final, 0, status);
+      // every MMA issued by the leader completes before TMEM is released
+      if (leader) umma_commit(&mma_final);
+      mbar_wait_warp(&mma_final, 0, status);
     }
-    __syncwarp();
   } else {
     // ---------------------------------------------------------- elementwise
     // Two warpgroups share every tile: warps 2-5 take key columns 0-63 and

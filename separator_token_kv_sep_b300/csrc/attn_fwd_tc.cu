@@ -280,8 +280,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // it issues P.V of tile A, S of A's next step, P.V of B, then S of B's
     // next step, so one tile's softmax runs while the other's products do;
     // the next step may belong to the next item, whose S products then
-    // overlap this item's last P.V and the epilogue.
-    if (lane == 0) {
+    // overlap this item's last P.V and the epilogue.  The whole warp runs
+    // this loop; the elected lane issues.
+    {
+      const bool leader = elect_one();
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
       const uint32_t k_base = smem_u32(smem + C::OFF_K), v_base = smem_u32(smem + C::OFF_V);
@@ -290,26 +292,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_qk = [&](int x, int qs, int st) {
         const uint32_t q_base = smem_u32(smem + C::OFF_Q + (qs * 2 + x) * C::TILE);
         const uint32_t d_s = tmem + (x ? C::TM_S1 : C::TM_S0);
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
-          umma_bf16_ss(d_s, sdesc_sw128(q_base + off, 16, 1024),
-                       sdesc_sw128(k_base + st * C::TILE + off, 16, 1024), idesc_qk, kk > 0);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
+            umma_bf16_ss(d_s, sdesc_sw128(q_base + off, 16, 1024),
+                         sdesc_sw128(k_base + st * C::TILE + off, 16, 1024), idesc_qk, kk > 0);
+          }
+          umma_commit(&s_full[x]);
         }
-        umma_commit(&s_full[x]);
+        __syncwarp();
       };
       auto issue_pv = [&](int x, int st) -> bool {  // O_x (+)= P_x V, P_x from TMEM
         int& cx = x ? cnt1 : cnt0;
         int& cix = x ? ci1 : ci0;
-        if (!mbar_wait(&p_full[x], cx & 1, status)) return false;
+        if (!mbar_wait_warp(&p_full[x], cx & 1, status)) return false;
         tc_fence_after();
         const uint32_t a_p = tmem + (x ? C::TM_S1 : C::TM_S0);
         const uint32_t d_o = tmem + (x ? C::TM_O1 : C::TM_O0);
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_bf16_ts(d_o, a_p + 8 * kk,
-                       sdesc_sw128(v_base + st * C::TILE + kk * 2048, kChunk, 1024), idesc_pv,
-                       (cix > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 8; ++kk)
+            umma_bf16_ts(d_o, a_p + 8 * kk,
+                         sdesc_sw128(v_base + st * C::TILE + kk * 2048, kChunk, 1024), idesc_pv,
+                         (cix > 0 || kk > 0) ? 1u : 0u);
+        }
+        __syncwarp();
         ++cx;
         ++cix;
         return true;
@@ -326,12 +334,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         int u = pc.next(-1);
         int itn = it + G;
         PairPlan pn = load_plan(idx, s_rec, itn, n_items, B, Hq, L, T);  // prefetched
-        ok = mbar_wait(&q_full[0], 0, status) && mbar_wait(&kv_full[0], 0, status);
+        ok = mbar_wait_warp(&q_full[0], 0, status) && mbar_wait_warp(&kv_full[0], 0, status);
         tc_fence_after();
         if (ok) {
           if (pc.active(u, 0)) issue_qk(0, 0, 0);
           if (pc.active(u, 1)) issue_qk(1, 0, 0);
-          if (pc.next(u) >= pc.nT) umma_commit(&q_empty[0]);  // every S of the item issued
+          if (leader && pc.next(u) >= pc.nT) umma_commit(&q_empty[0]);  // every S of the item issued
         }
         while (ok) {
           const int st = n % NST, stn = (n + 1) % NST;
@@ -348,19 +356,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int qsn = same ? qs : (kq + 1) % QB;
           const PairPlan px = same ? pc : pn;
           if (pc.active(u, 0) && !(ok = issue_pv(0, st))) break;
-          if (!same) umma_commit(&o_done[0]);
+          if (leader && !same) umma_commit(&o_done[0]);
           if (has_next) {
-            if (!same && !(ok = mbar_wait(&q_full[qsn], ((kq + 1) / QB) & 1, status))) break;
-            if (!(ok = mbar_wait(&kv_full[stn], ((n + 1) / NST) & 1, status))) break;
+            if (!same && !(ok = mbar_wait_warp(&q_full[qsn], ((kq + 1) / QB) & 1, status))) break;
+            if (!(ok = mbar_wait_warp(&kv_full[stn], ((n + 1) / NST) & 1, status))) break;
             tc_fence_after();
             if (px.active(un, 0)) issue_qk(0, qsn, stn);
           }
           if (pc.active(u, 1) && !(ok = issue_pv(1, st))) break;
-          umma_commit(&kv_empty[st]);  // every MMA reading this K/V stage is issued
-          if (!same && pc.hasB) umma_commit(&o_done[1]);
+          if (leader) umma_commit(&kv_empty[st]);  // every MMA reading this K/V stage is issued
+          if (leader && !same && pc.hasB) umma_commit(&o_done[1]);
           if (has_next) {
             if (px.active(un, 1)) issue_qk(1, qsn, stn);
-            if (px.next(un) >= px.nT) umma_commit(&q_empty[qsn]);
+            if (leader && px.next(un) >= px.nT) umma_commit(&q_empty[qsn]);
           }
           ++n;
           if (!has_next) break;
@@ -376,11 +384,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           u = un;
         }
       }
-      // every MMA issued by this thread completes before TMEM is released
-      umma_commit(&mma_final);
-      mbar_wait(&mma_final, 0, status);
+      // every MMA issued by the leader completes before TMEM is released
+      if (leader) umma_commit(&mma_final);
+      mbar_wait_warp(&mma_final, 0, status);
     }
-    __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
     const int x = (warp - 2) >> 2;  // query tile: 0 = A, 1 = B

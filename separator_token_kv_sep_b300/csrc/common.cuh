@@ -90,6 +90,26 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
   }
 }
 
+// mbar_wait by every lane of a converged warp; every lane gets the same
+// result (false if any lane gave up).
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int* status) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, status));
+}
+
+// True in exactly one lane (the lowest active one) of a converged warp.
+// Issuing roles run their control flow on the whole warp, so descriptors
+// and counters stay warp-uniform, and let the elected lane issue each
+// single-thread tcgen05 operation.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "elect.sync _|P, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // ---------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor) tile loads into shared memory
 // ---------------------------------------------------------------------------
