@@ -42,7 +42,7 @@ constexpr int kChunk = 128 * 128;  // bytes of a [128 rows x 64 cols] bf16 block
 constexpr int kThreads = 320;      // warp 0 TMA, warp 1 MMA, warps 2-9 elementwise
 constexpr int kEwThreads = 256;    // two elementwise warpgroups
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kKeepChunk = 4;      // query tiles per CTA of the keep-tile dK/dV kernel
+constexpr int kKeepChunk = 8;      // query tiles per keep item of the dK/dV kernel
 constexpr int kCtaItems = 128;     // work items a dK/dV CTA keeps in static shared memory
 
 __device__ __forceinline__ uint32_t range_bits(int lo, int hi, int w) {
@@ -616,9 +616,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int count = min(max(idx.keep_count[it.b], 0), L);
       const int32_t* blocks = idx.blocks + (size_t)it.b * T * 4;
       const int j = it.row0 + r;  // KEEP: keep index; DENSE: key position
-      bool keep_j = false;
-      if (!keep && j < L)
-        keep_j = (idx.keep_bits[(size_t)it.b * hdr.nwords + (j >> 5)] >> (j & 31)) & 1u;
+      // a dense row's keep bit and keep prefix, loaded together
+      const bool dense_row = !keep && j < L;
+      const uint32_t kbw = dense_row ? idx.keep_bits[(size_t)it.b * hdr.nwords + (j >> 5)] : 0u;
+      const int kpre = dense_row ? idx.keep_prefix[(size_t)it.b * (L + 1) + j] : 0;
+      const bool keep_j = (kbw >> (j & 31)) & 1u;
       // this item's epilogue: KEEP rows and DENSE keep tokens add into the
       // fp32 keep accumulators (written to dK/dV by the scatter kernel);
       // other DENSE rows are final
@@ -627,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         const bool to_acc = keep ? (j < count) : (j < L && keep_j);
         const bool to_out = !keep && j < L && !keep_j;
-        const int kidx = keep ? j : (keep_j ? idx.keep_prefix[(size_t)it.b * (L + 1) + j] : 0);
+        const int kidx = keep ? j : (keep_j ? kpre : 0);
         const long long plane = (long long)it.b * Hkv + it.g;
         e.rm = to_acc ? (((plane * L + kidx) << 2) | 1) : to_out ? (((plane * L + j) << 2) | 2) : 0;
       }
