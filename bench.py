@@ -74,6 +74,14 @@ def visited_pairs_per_head(ids: np.ndarray, a: int, n: int) -> int:
     return int((kp[:, W] + (i - W + 1)[None, :]).sum())
 
 
+def visited_pairs_keep(keep: np.ndarray, n: int) -> int:
+    """visited_pairs_per_head for an explicit keep mask [B, L]."""
+    kp = np.concatenate([np.zeros((keep.shape[0], 1), np.int64), np.cumsum(keep, axis=1)], axis=1)
+    i = np.arange(keep.shape[1])
+    W = np.maximum(0, i - n + 1)
+    return int((kp[:, W] + (i - W + 1)[None, :]).sum())
+
+
 def gathered_band_pairs_per_head(ids: np.ndarray, a: int, n: int, bm: int):
     """Split of the visited pairs of one head (summed over the batch) between
     the two key sources of a 128-row query tile: keep tokens gathered from
@@ -273,6 +281,9 @@ def run_ours(args, rank, world, device):
         total_ms = max_over_ranks(total_ms, world)
         decode = run_decode(args, rank, device, flush, peaks) if args.only == "all" else None
         prefill = run_prefill(args, rank, device, flush, peaks) if args.only == "all" else None
+        variants = run_variants(args, rank, device, flush, peaks) if args.only == "all" else None
+        index_scaling = (run_index_scaling(args, rank, device, flush)
+                         if args.only == "all" else None)
     assert api.sep_get_device_status() == 0
     clocks = sampler.summary()
 
@@ -329,6 +340,8 @@ def run_ours(args, rank, world, device):
         "gpu_launches": 7 * args.steps,
         "decode": decode,
         "prefill": prefill,
+        "mask_variants": variants,
+        "index_scaling": index_scaling,
     }
     if rank == 0 and not args.no_cpu_baseline and args.only == "all":
         line["cpu_baseline"] = cpu_baseline_train(cfg, q_np, k_np, v_np, do_np, ids_np)
@@ -464,6 +477,117 @@ def run_decode(args, rank, device, flush, peaks):
                          "traffic": DECODE_DRAM_TRAFFIC_BYTES,
                          "algorithmic_bytes_per_step": round(alg_bytes / n_dec)},
             "gpu_launches": n_dec}
+
+
+FIXLLM_DELTA = 10  # one kept token per 10 positions: the separator density 0.10 of the workload
+
+
+def run_variants(args, rank, device, flush, peaks):
+    """The training step of the same Pythia-shaped workload under the mask
+    variants the pages set beside SepLLM: windows n = 64 and n = L (full
+    causal, the layer-0 variant), StreamingLLM (no separators) and the
+    FixLLM control (every FIXLLM_DELTA-th token instead of the separators).
+    Each step is sep_build_index(_fixed) + sep_attn_fwd + sep_attn_bwd,
+    replayed from a CUDA graph with L2 flushed before it."""
+    import torch
+    from separator_token_kv_sep_b300 import api
+    cfg = synth.PYTHIA_TRAIN_N128
+    q_np, k_np, v_np, do_np, ids_np = synth.prefill_inputs(cfg, seed=shard_seed(cfg.seed, rank))
+    bf = torch.bfloat16
+    q = torch.from_numpy(q_np).to(device, bf)
+    k = torch.from_numpy(k_np).to(device, bf)
+    v = torch.from_numpy(v_np).to(device, bf)
+    dout = torch.from_numpy(do_np).to(device, bf)
+    ids = torch.from_numpy(ids_np).to(device)
+    B, Hq, L, d = q.shape
+    Hkv = k.shape[1]
+    a = cfg.a
+    pos = np.arange(L)
+    sep_keep = np.isin(ids_np, synth.SEP_IDS) | (pos < a)[None, :]
+    fix_keep = np.broadcast_to(((pos + 1) % FIXLLM_DELTA == 0) | (pos < a), (B, L))
+    sink_keep = np.broadcast_to(pos < a, (B, L))
+    variants = [("sep_n64", 64, sep_keep, "sep"), ("sep_full_layer_nL", L, sep_keep, "sep"),
+                ("streamingllm_n128", 128, sink_keep, "none"),
+                ("fixllm_n128_delta10", 128, fix_keep, "fix")]
+    idx_buf = torch.empty(api.sep_index_bytes(B, L), dtype=torch.uint8, device=device)
+    ws_f = torch.empty(api.sep_attn_workspace_bytes(B, Hq, Hkv, L, d, api.SEP_BF16, False),
+                       dtype=torch.uint8, device=device)
+    ws_b = torch.empty(api.sep_attn_workspace_bytes(B, Hq, Hkv, L, d, api.SEP_BF16, True),
+                       dtype=torch.uint8, device=device)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, L), dtype=torch.float32, device=device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    steps = max(3, min(args.steps, 20))
+    out = {}
+    for name, n, keep, kind in variants:
+        def step():
+            if kind == "fix":
+                api.sep_build_index_fixed(B, L, a, n, FIXLLM_DELTA, index_buf=idx_buf, device=device)
+            else:
+                api.sep_build_index(ids, synth.SEP_IDS if kind == "sep" else [], a, n,
+                                    index_buf=idx_buf)
+            api.sep_attn_fwd(idx_buf, q, k, v, o=o, lse=lse, ws=ws_f)
+            api.sep_attn_bwd(idx_buf, q, k, v, o, lse, dout, dq=dq, dk=dk, dv=dv, ws=ws_b)
+        step()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        times = []
+        for it in range(steps + 3):
+            flush.zero_()
+            e0.record()
+            graph.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            if it >= 3:
+                times.append(e0.elapsed_time(e1))
+        assert api.sep_get_device_status() == 0
+        ms = sum(times) / len(times)
+        pairs = visited_pairs_keep(keep, n)
+        flops = 14.0 * d * pairs * Hq
+        out[name] = {"window_n": n, "ms": round(ms, 5),
+                     "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                     "visited_over_causal": round(pairs / (B * L * (L + 1) / 2), 4),
+                     "frac_of_bf16_peak": round(flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)}
+    out["note"] = ("index + fwd + bwd of the Pythia-shaped workload (B8 H12 L2048 d64 bf16, a4) "
+                   "per variant; FLOPs 14 d per visited pair; CUDA graph, L2 flushed before "
+                   f"each step, {steps} timed steps")
+    return out
+
+
+def run_index_scaling(args, rank, device, flush):
+    """sep_build_index alone at B = 64, L = 65536 (16 MB of ids), the
+    index kernel's scaling run: device time and algorithmic GB/s."""
+    import torch
+    from separator_token_kv_sep_b300 import api
+    B, L, a, n, p = 64, 65536, 4, 8192, 0.12
+    rng = np.random.default_rng(shard_seed(2001, rank))
+    ids_np = synth.token_ids(rng, (B, L), p)
+    ids = torch.from_numpy(ids_np).to(device)
+    idx_buf = torch.empty(api.sep_index_bytes(B, L), dtype=torch.uint8, device=device)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    times = []
+    for it in range(13):
+        flush.zero_()
+        e0.record()
+        api.sep_build_index(ids, synth.SEP_IDS, a, n, index_buf=idx_buf)
+        e1.record()
+        torch.cuda.synchronize()
+        if it >= 3:
+            times.append(e0.elapsed_time(e1))
+    assert api.sep_get_device_status() == 0
+    ms = sum(times) / len(times)
+    count = int((np.isin(ids_np, synth.SEP_IDS) | (np.arange(L) < a)[None, :]).sum())
+    T = (L + 127) // 128
+    alg = 4.0 * B * L + 4.0 * B * (L + 1) + 4.0 * count + 16.0 * B * T + 4.0 * B * ((L + 31) // 32)
+    return {"workload": f"sep_build_index B{B} L{L} a{a} n{n} p{p}", "ms": round(ms, 5),
+            "gbs": round(alg / (ms * 1e-3) / 1e9, 1), "algorithmic_bytes": int(alg),
+            "note": "ids read + keep_prefix, keep_pos (valid entries), block records and keep "
+                    "bits written; L2 flushed before each call"}
 
 
 def run_prefill(args, rank, device, flush, peaks):
