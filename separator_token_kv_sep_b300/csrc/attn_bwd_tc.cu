@@ -11,22 +11,27 @@
 //
 // Every visible pair (i, j) belongs to exactly one of the forward's two key
 // sources (gathered keep tokens before the query tile's window, or the dense
-// band), and the backward keeps that split:
-//   bwd_dq_kernel    query-major, the forward's traversal: S = Q K^T and
-//                    dP = dO V^T into TMEM, dS to shared memory, dQ += dS K.
-//   bwd_kv_kernel<KEEP>   key-major over the gathered keep tiles: each CTA
-//                    owns 128 keep tokens and one q head and walks the query
-//                    tiles that gather them; its fp32 dK/dV sums are added
-//                    into a per-keep-token accumulator with red.global.add.
-//   bwd_kv_kernel<DENSE>  key-major over aligned 128-key tiles and the query
-//                    tiles whose dense band covers them (all q heads of the
-//                    kv group); its epilogue adds the keep accumulator of
-//                    keep tokens and rounds each gradient to bf16 once.
-// In the key-major kernels S^T = K Q^T and dP^T = V dO^T go to TMEM; the
-// elementwise warps (one thread per key) turn them into P^T and dS^T in
-// shared memory and release TMEM first, so (with two Q/dO stages) the next
-// query tile's S^T / dP^T overlap this tile's dV += P^T dO and dK += dS^T Q
-// on the tensor pipe.
+// band), and the backward keeps that split.  Four launches:
+//   bwd_prep_kernel     the keep-token K/V gather, zeroed fp32 keep-token
+//                       gradient accumulators, the per-row stats
+//                       (-LSE log2 e, -Delta) and, in CTA 0, the dK/dV work
+//                       schedule.
+//   bwd_kv_persistent   key-major dK/dV, one CTA per SM over the schedule's
+//                       items: a 128-key tile (gathered keep tokens, or a
+//                       dense key range) against the query tiles that see it,
+//                       for every q head of its kv group.  S^T = K Q^T and
+//                       dP^T = V dO^T go to TMEM per 64-query half-tile; the
+//                       elementwise warpgroups overwrite them with P^T and
+//                       dS^T, which the dV += P^T dO and dK += dS^T Q products
+//                       read from TMEM.  Keep tokens add into the fp32
+//                       accumulators with red.global.add; other keys are
+//                       written as bf16 at once.
+//   bwd_dq_persistent   query-major dQ, one CTA per SM: the forward's
+//                       traversal, S = Q K^T and dP = dO V^T into TMEM, dS to
+//                       shared memory, dQ += dS K.
+//   bwd_keep_scatter_kernel  the keep tokens' dK / dV rows from the
+//                       accumulators.
+// The MMA issuers run warp-uniform, with one elected lane issuing.
 // All waits are bounded; on expiry a kernel records SEP_ERR_TIMEOUT, drains
 // its copies and MMAs, frees TMEM and returns.
 #include "common.cuh"
@@ -70,7 +75,7 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
 //   DENSE  keys are positions [row0, row0+128) of K/V; the query tiles are
 //          those whose dense band reaches the tile, element mask as in the
 //          forward.
-// Items are written by the last CTA of the prep kernel: keep items first
+// Items are written by CTA 0 of the prep kernel: keep items first
 // (they are the longest), then dense items.  Persistent CTAs take items
 // round-robin.
 // ---------------------------------------------------------------------------
