@@ -485,8 +485,9 @@ FIXLLM_DELTA = 10  # one kept token per 10 positions: the separator density 0.10
 def run_variants(args, rank, device, flush, peaks):
     """The training step of the same Pythia-shaped workload under the mask
     variants the pages set beside SepLLM: windows n = 64 and n = L (full
-    causal, the layer-0 variant), StreamingLLM (no separators) and the
-    FixLLM control (every FIXLLM_DELTA-th token instead of the separators).
+    causal, the layer-0 variant), StreamingLLM (no separators), the FixLLM
+    control (every FIXLLM_DELTA-th token instead of the separators) and
+    hybrid heads (half the kv groups on full causal attention).
     Each step is sep_build_index(_fixed) + sep_attn_fwd + sep_attn_bwd,
     replayed from a CUDA graph with L2 flushed before it."""
     import torch
@@ -506,9 +507,12 @@ def run_variants(args, rank, device, flush, peaks):
     sep_keep = np.isin(ids_np, synth.SEP_IDS) | (pos < a)[None, :]
     fix_keep = np.broadcast_to(((pos + 1) % FIXLLM_DELTA == 0) | (pos < a), (B, L))
     sink_keep = np.broadcast_to(pos < a, (B, L))
-    variants = [("sep_n64", 64, sep_keep, "sep"), ("sep_full_layer_nL", L, sep_keep, "sep"),
-                ("streamingllm_n128", 128, sink_keep, "none"),
-                ("fixllm_n128_delta10", 128, fix_keep, "fix")]
+    # hybrid heads: the first half of the kv groups on full causal attention
+    half_full = (1 << (Hkv // 2)) - 1
+    variants = [("sep_n64", 64, sep_keep, "sep", 0), ("sep_full_layer_nL", L, sep_keep, "sep", 0),
+                ("streamingllm_n128", 128, sink_keep, "none", 0),
+                ("fixllm_n128_delta10", 128, fix_keep, "fix", 0),
+                ("hybrid_half_full_sep_n128", 128, sep_keep, "sep", half_full)]
     idx_buf = torch.empty(api.sep_index_bytes(B, L), dtype=torch.uint8, device=device)
     ws_f = torch.empty(api.sep_attn_workspace_bytes(B, Hq, Hkv, L, d, api.SEP_BF16, False),
                        dtype=torch.uint8, device=device)
@@ -519,15 +523,20 @@ def run_variants(args, rank, device, flush, peaks):
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     steps = max(3, min(args.steps, 20))
     out = {}
-    for name, n, keep, kind in variants:
+    for name, n, keep, kind, fg in variants:
         def step():
             if kind == "fix":
                 api.sep_build_index_fixed(B, L, a, n, FIXLLM_DELTA, index_buf=idx_buf, device=device)
             else:
                 api.sep_build_index(ids, synth.SEP_IDS if kind == "sep" else [], a, n,
                                     index_buf=idx_buf)
-            api.sep_attn_fwd(idx_buf, q, k, v, o=o, lse=lse, ws=ws_f)
-            api.sep_attn_bwd(idx_buf, q, k, v, o, lse, dout, dq=dq, dk=dk, dv=dv, ws=ws_b)
+            if fg:
+                api.sep_attn_fwd_hybrid(idx_buf, q, k, v, fg, o=o, lse=lse, ws=ws_f)
+                api.sep_attn_bwd_hybrid(idx_buf, q, k, v, o, lse, dout, fg, dq=dq, dk=dk, dv=dv,
+                                        ws=ws_b)
+            else:
+                api.sep_attn_fwd(idx_buf, q, k, v, o=o, lse=lse, ws=ws_f)
+                api.sep_attn_bwd(idx_buf, q, k, v, o, lse, dout, dq=dq, dk=dk, dv=dv, ws=ws_b)
         step()
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
@@ -546,9 +555,14 @@ def run_variants(args, rank, device, flush, peaks):
                 times.append(e0.elapsed_time(e1))
         assert api.sep_get_device_status() == 0
         ms = sum(times) / len(times)
+        # per head: full-attention groups visit every causal pair
+        n_full = bin(fg).count("1") * (Hq // Hkv)
+        causal = B * L * (L + 1) // 2
         pairs = visited_pairs_keep(keep, n)
-        flops = 14.0 * d * pairs * Hq
-        out[name] = {"window_n": n, "ms": round(ms, 5),
+        head_pairs = (Hq - n_full) * pairs + n_full * causal
+        pairs = head_pairs / Hq
+        flops = 14.0 * d * head_pairs
+        out[name] = {"window_n": n, "full_kv_groups": bin(fg).count("1"), "ms": round(ms, 5),
                      "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                      "visited_over_causal": round(pairs / (B * L * (L + 1) / 2), 4),
                      "frac_of_bf16_peak": round(flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)}

@@ -180,6 +180,35 @@ sep_status sep_attn_bwd(const void* index_buf, const void* q, const void* k,
                         int B, int Hq, int Hkv, int L, int d, sep_dtype dtype,
                         float scale, void* ws, size_t ws_bytes, void* stream);
 
+/* sep_attn_fwd_hybrid / sep_attn_bwd_hybrid -- hybrid heads: some kv groups
+ * attend with full causal attention, the others under the index's mask.
+ * The pages evaluate this layout two ways:
+ *  - as a baseline with some heads on a sliding window and the rest on
+ *    full attention (paperhub rebuttal page, reply A5 to the third
+ *    reviewer).  Build the index with no separator ids and a = 0 for
+ *    those window heads;
+ *  - with the first, or first and last, layers on full attention
+ *    (anthology record lit-748, "Training from scratch").
+ *
+ * Bit g of full_groups (g < Hkv <= 64) puts kv group g -- q heads
+ * g*(Hq/Hkv) .. (g+1)*(Hq/Hkv)-1 and kv head g -- on the causal mask
+ * j <= i, exactly the index's mask with a window n >= L.  The other groups
+ * use the index's mask.  full_groups = 0 is sep_attn_fwd / sep_attn_bwd.
+ * All other arguments, layouts, workspaces and errors are those of
+ * sep_attn_fwd and sep_attn_bwd with dtype SEP_BF16.  Bits at or above Hkv
+ * give SEP_ERR_INVALID_ARG. */
+sep_status sep_attn_fwd_hybrid(const void* index_buf, const void* q, const void* k,
+                               const void* v, void* o, float* lse,
+                               int B, int Hq, int Hkv, int L, int d,
+                               unsigned long long full_groups, float scale,
+                               void* ws, size_t ws_bytes, void* stream);
+sep_status sep_attn_bwd_hybrid(const void* index_buf, const void* q, const void* k,
+                               const void* v, const void* o, const float* lse,
+                               const void* dout, void* dq, void* dk, void* dv,
+                               int B, int Hq, int Hkv, int L, int d,
+                               unsigned long long full_groups, float scale,
+                               void* ws, size_t ws_bytes, void* stream);
+
 /* Size of the fixed device scratch array behind sep_attn_fwd_static. */
 #define SEP_STATIC_SCRATCH_BYTES (64u << 20)
 

@@ -17,6 +17,8 @@ Modules
                and its textbook backward.
 ``fixllm``     the FixLLM control (one kept token per fixed interval instead
                of the separators) on the same mask machinery.
+``hybrid``     hybrid heads: kv groups with full causal attention beside
+               groups under the SepLLM (or sliding-window) mask.
 ``streaming``  the four-block streaming KV cache (initial, separator, past
                window, local window) with eviction into the separator cache,
                position shifting inside the cache, RoPE and decode attention.
@@ -30,4 +32,4 @@ the block-list record format).  Those are marked "parity unpinned" where
 they are defined.
 """
 
-from . import fixllm, sepllm, streaming  # noqa: F401
+from . import fixllm, hybrid, sepllm, streaming  # noqa: F401

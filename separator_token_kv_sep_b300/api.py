@@ -33,7 +33,8 @@ EXPORTED = ["sep_index_bytes", "sep_build_index", "sep_index_views",
             "sep_cache_export_bytes", "sep_cache_export", "sep_cache_import",
             "sep_get_device_status", "sep_status_string", "sep_attn_fwd_static",
             "sep_profile_events", "sep_selftest_wait_timeout", "sep_build_index_fixed",
-            "sep_cache_prefill_workspace_bytes", "sep_cache_prefill"]
+            "sep_cache_prefill_workspace_bytes", "sep_cache_prefill", "sep_attn_fwd_hybrid",
+            "sep_attn_bwd_hybrid"]
 
 
 class SepError(RuntimeError):
@@ -54,6 +55,7 @@ def _load() -> ctypes.CDLL:
                            "separator_token_kv_sep_b300.build.build()")
     lib = ctypes.CDLL(LIB_PATH)
     P, I, Z, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
+    U64 = ctypes.c_ulonglong
     PP = ctypes.POINTER(ctypes.c_void_p)
     CP = ctypes.POINTER(CacheParams)
     sig = {
@@ -77,6 +79,9 @@ def _load() -> ctypes.CDLL:
         "sep_build_index_fixed": (I, [I, I, I, I, I, I, P, Z, P]),
         "sep_cache_prefill_workspace_bytes": (Z, [CP, I]),
         "sep_cache_prefill": (I, [CP, P, P, P, P, I, P, I, P, Z, P]),
+        "sep_attn_fwd_hybrid": (I, [P, P, P, P, P, P, I, I, I, I, I, U64, F, P, Z, P]),
+        "sep_attn_bwd_hybrid": (I, [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, U64, F, P, Z,
+                                    P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -248,6 +253,54 @@ def sep_attn_bwd(index_buf, q, k, v, o, lse, dout, scale: float = 0.0, dq=None, 
                              _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, L, d, dt,
                              float(scale), _ptr(ws), ws.numel(), _stream(stream)),
            "sep_attn_bwd")
+    return dq, dk, dv
+
+
+def full_groups_mask(groups: Sequence[int]) -> int:
+    """Bitmask of the kv groups that attend with full causal attention."""
+    m = 0
+    for g in groups:
+        m |= 1 << int(g)
+    return m
+
+
+def sep_attn_fwd_hybrid(index_buf, q, k, v, full_groups: int, scale: float = 0.0, o=None,
+                        lse=None, ws=None, stream=None):
+    """sep_attn_fwd with hybrid heads: kv groups whose bit is set in
+    full_groups attend with full causal attention, the others under the
+    index's mask.  bf16 only.  Returns (o, lse)."""
+    B, Hq, L, d = q.shape
+    Hkv = k.shape[1]
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, L), dtype=torch.float32, device=q.device)
+    nws = sep_attn_workspace_bytes(B, Hq, Hkv, L, d, SEP_BF16, False)
+    if ws is None:
+        ws = _empty_bytes(nws, q.device)
+    _check(_lib.sep_attn_fwd_hybrid(_ptr(index_buf), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                    _ptr(lse), B, Hq, Hkv, L, d, int(full_groups), float(scale),
+                                    _ptr(ws), ws.numel(), _stream(stream)),
+           "sep_attn_fwd_hybrid")
+    return o, lse
+
+
+def sep_attn_bwd_hybrid(index_buf, q, k, v, o, lse, dout, full_groups: int, scale: float = 0.0,
+                        dq=None, dk=None, dv=None, ws=None, stream=None):
+    """sep_attn_bwd with hybrid heads (see sep_attn_fwd_hybrid).
+    Returns (dq, dk, dv)."""
+    B, Hq, L, d = q.shape
+    Hkv = k.shape[1]
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    nws = sep_attn_workspace_bytes(B, Hq, Hkv, L, d, SEP_BF16, True)
+    if ws is None:
+        ws = _empty_bytes(nws, q.device)
+    _check(_lib.sep_attn_bwd_hybrid(_ptr(index_buf), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                    _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), B, Hq,
+                                    Hkv, L, d, int(full_groups), float(scale), _ptr(ws),
+                                    ws.numel(), _stream(stream)), "sep_attn_bwd_hybrid")
     return dq, dk, dv
 
 

@@ -17,13 +17,13 @@ __device__ int g_device_status;
 
 size_t attn_fwd_tc_workspace(int B, int Hkv, int L, int d);
 int launch_attn_fwd_tc(IndexPtrs idx, const void* q, const void* k, const void* v, void* o,
-                       float* lse, int B, int Hq, int Hkv, int L, int d, float scale, void* ws,
-                       int* status, void* stream);
+                       float* lse, int B, int Hq, int Hkv, int L, int d, float scale,
+                       uint64_t full_groups, void* ws, int* status, void* stream);
 size_t attn_bwd_tc_workspace(int B, int Hq, int Hkv, int L, int d);
 int launch_attn_bwd_tc(IndexPtrs idx, const void* q, const void* k, const void* v, const void* o,
                        const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
-                       int Hq, int Hkv, int L, int d, float scale, void* ws, int* status,
-                       void* stream);
+                       int Hq, int Hkv, int L, int d, float scale, uint64_t full_groups, void* ws,
+                       int* status, void* stream);
 
 namespace {
 thread_local void* t_prof_events[SEP_MAX_PROFILE_EVENTS] = {nullptr};
@@ -137,20 +137,28 @@ SEP_API size_t sep_attn_workspace_bytes(int B, int Hq, int Hkv, int L, int d, se
   return attn_fwd_tc_workspace(B, Hkv, L, d);
 }
 
-SEP_API sep_status sep_attn_fwd(const void* index_buf, const void* q, const void* k,
-                                const void* v, void* o, float* lse, int B, int Hq, int Hkv,
-                                int L, int d, sep_dtype dtype, float scale, void* ws,
-                                size_t ws_bytes, void* stream) {
+namespace {
+
+// Bits of full_groups at or above Hkv must be clear.
+bool groups_ok(uint64_t full_groups, int Hkv) {
+  return Hkv >= 64 || (full_groups >> Hkv) == 0;
+}
+
+sep_status attn_fwd(const void* index_buf, const void* q, const void* k, const void* v, void* o,
+                    float* lse, int B, int Hq, int Hkv, int L, int d, sep_dtype dtype,
+                    float scale, uint64_t full_groups, void* ws, size_t ws_bytes, void* stream) {
   if (!index_buf || !q || !k || !v || !o || !lse) return SEP_ERR_INVALID_ARG;
   if (!attn_shape_ok(B, Hq, Hkv, L, d)) {
     if (B >= 1 && Hq >= 1 && Hkv >= 1 && L >= 1 && Hq % Hkv == 0) return SEP_ERR_UNSUPPORTED;
     return SEP_ERR_INVALID_ARG;
   }
+  if (!groups_ok(full_groups, Hkv)) return SEP_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
       !aligned(lse, 4) || !aligned(index_buf, 256))
     return SEP_ERR_INVALID_ARG;
   if (!(scale > 0.f)) scale = 1.0f / sqrtf(static_cast<float>(d));
   if (dtype != SEP_F32 && dtype != SEP_BF16) return SEP_ERR_UNSUPPORTED;
+  if (dtype == SEP_F32 && full_groups != 0) return SEP_ERR_UNSUPPORTED;
   if (dtype == SEP_BF16) {
     const size_t need = attn_fwd_tc_workspace(B, Hkv, L, d);
     if (!ws || ws_bytes < need) return SEP_ERR_WORKSPACE;
@@ -165,21 +173,21 @@ SEP_API sep_status sep_attn_fwd(const void* index_buf, const void* q, const void
                                           static_cast<const float*>(v), static_cast<float*>(o),
                                           lse, B, Hq, Hkv, L, d, scale, st, stream));
   }
-  return from_cuda(launch_attn_fwd_tc(idx, q, k, v, o, lse, B, Hq, Hkv, L, d, scale, ws, st,
-                                      stream));
+  return from_cuda(launch_attn_fwd_tc(idx, q, k, v, o, lse, B, Hq, Hkv, L, d, scale, full_groups,
+                                      ws, st, stream));
 }
 
-SEP_API sep_status sep_attn_bwd(const void* index_buf, const void* q, const void* k,
-                                const void* v, const void* o, const float* lse,
-                                const void* dout, void* dq, void* dk, void* dv, int B, int Hq,
-                                int Hkv, int L, int d, sep_dtype dtype, float scale, void* ws,
-                                size_t ws_bytes, void* stream) {
+sep_status attn_bwd(const void* index_buf, const void* q, const void* k, const void* v,
+                    const void* o, const float* lse, const void* dout, void* dq, void* dk,
+                    void* dv, int B, int Hq, int Hkv, int L, int d, sep_dtype dtype, float scale,
+                    uint64_t full_groups, void* ws, size_t ws_bytes, void* stream) {
   if (!index_buf || !q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv)
     return SEP_ERR_INVALID_ARG;
   if (!attn_shape_ok(B, Hq, Hkv, L, d)) {
     if (B >= 1 && Hq >= 1 && Hkv >= 1 && L >= 1 && Hq % Hkv == 0) return SEP_ERR_UNSUPPORTED;
     return SEP_ERR_INVALID_ARG;
   }
+  if (!groups_ok(full_groups, Hkv)) return SEP_ERR_INVALID_ARG;
   if (dtype != SEP_BF16) return SEP_ERR_UNSUPPORTED;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
       !aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
@@ -193,7 +201,44 @@ SEP_API sep_status sep_attn_bwd(const void* index_buf, const void* q, const void
   if (!st) return SEP_ERR_CUDA;
   const IndexPtrs idx = index_ptrs(const_cast<void*>(index_buf), index_layout(B, L, SEP_BLOCK_M));
   return from_cuda(launch_attn_bwd_tc(idx, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, L, d,
-                                      scale, ws, st, stream));
+                                      scale, full_groups, ws, st, stream));
+}
+
+}  // namespace
+
+SEP_API sep_status sep_attn_fwd(const void* index_buf, const void* q, const void* k,
+                                const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                                int L, int d, sep_dtype dtype, float scale, void* ws,
+                                size_t ws_bytes, void* stream) {
+  return attn_fwd(index_buf, q, k, v, o, lse, B, Hq, Hkv, L, d, dtype, scale, 0, ws, ws_bytes,
+                  stream);
+}
+
+SEP_API sep_status sep_attn_fwd_hybrid(const void* index_buf, const void* q, const void* k,
+                                       const void* v, void* o, float* lse, int B, int Hq,
+                                       int Hkv, int L, int d, unsigned long long full_groups,
+                                       float scale, void* ws, size_t ws_bytes, void* stream) {
+  return attn_fwd(index_buf, q, k, v, o, lse, B, Hq, Hkv, L, d, SEP_BF16, scale, full_groups, ws,
+                  ws_bytes, stream);
+}
+
+SEP_API sep_status sep_attn_bwd(const void* index_buf, const void* q, const void* k,
+                                const void* v, const void* o, const float* lse,
+                                const void* dout, void* dq, void* dk, void* dv, int B, int Hq,
+                                int Hkv, int L, int d, sep_dtype dtype, float scale, void* ws,
+                                size_t ws_bytes, void* stream) {
+  return attn_bwd(index_buf, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, L, d, dtype, scale, 0,
+                  ws, ws_bytes, stream);
+}
+
+SEP_API sep_status sep_attn_bwd_hybrid(const void* index_buf, const void* q, const void* k,
+                                       const void* v, const void* o, const float* lse,
+                                       const void* dout, void* dq, void* dk, void* dv, int B,
+                                       int Hq, int Hkv, int L, int d,
+                                       unsigned long long full_groups, float scale, void* ws,
+                                       size_t ws_bytes, void* stream) {
+  return attn_bwd(index_buf, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, L, d, SEP_BF16, scale,
+                  full_groups, ws, ws_bytes, stream);
 }
 
 SEP_API sep_status sep_profile_events(void* const* events, int n_events) {

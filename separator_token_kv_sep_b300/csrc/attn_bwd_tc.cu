@@ -123,9 +123,13 @@ __device__ __forceinline__ int block_exclusive_scan(int x, int* sh, int* total) 
 
 // Builds the schedule (one CTA).  blocks[b][t] = {n_gather, dense_lo, dense_hi, flags}.
 __device__ void build_bwd_schedule(IndexPtrs idx, int B, int Hkv, int L, int T,
-                                   BwdSchedule* sched, int4* items) {
+                                   uint64_t full_groups, BwdSchedule* sched, int4* items) {
   __shared__ int sh[33];
   int total = 0;
+  // kv groups with full causal attention have no keep items, and every
+  // query tile from the key tile on sees their dense key tiles
+  const uint64_t gmask = Hkv >= 64 ? ~0ull : ((1ull << Hkv) - 1ull);
+  const int nsep = Hkv - __popcll(full_groups & gmask);
   // keep items: (b, keep tile kt) -> chunks of query tiles from t_begin(kt)
   for (int base = 0; base < B * T; base += blockDim.x) {
     const int id = base + threadIdx.x;
@@ -150,12 +154,16 @@ __device__ void build_bwd_schedule(IndexPtrs idx, int B, int Hkv, int L, int T,
       const int b = id / T, kt = id % T;
       for (int cc = 0; cc < n; ++cc) {
         const int t0 = tb + cc * kKeepChunk, t1 = min(T, t0 + kKeepChunk);
-        for (int g = 0; g < Hkv; ++g)
-          items[total + (size_t)(ex + cc) * Hkv + g] =
+        int gi = 0;
+        for (int g = 0; g < Hkv; ++g) {
+          if ((full_groups >> g) & 1ull) continue;
+          items[total + (size_t)(ex + cc) * nsep + gi] =
               make_int4(kItemKeep, b * Hkv + g, kt * 128, (t0 << 16) | t1);
+          ++gi;
+        }
       }
     }
-    total += sum * Hkv;
+    total += sum * nsep;
   }
   const int n_keep = total;
   // dense items: (b, key tile jt) -> query tiles jt .. (last whose band starts
@@ -170,7 +178,8 @@ __device__ void build_bwd_schedule(IndexPtrs idx, int B, int Hkv, int L, int T,
     }
     for (int g = 0; g < Hkv; ++g)
       items[n_keep + (size_t)id * Hkv + g] =
-          make_int4(kItemDense, b * Hkv + g, jt * 128, (jt << 16) | max(lo, jt + 1));
+          make_int4(kItemDense, b * Hkv + g, jt * 128,
+                    (jt << 16) | (((full_groups >> g) & 1ull) ? T : max(lo, jt + 1)));
   }
   if (threadIdx.x == 0) {
     sched->n_items = n_keep + B * T * Hkv;
@@ -243,11 +252,12 @@ __global__ void __launch_bounds__(kPrepThreads)
                     const uint4* __restrict__ dout, const float* __restrict__ lse,
                     float2* __restrict__ stats, float4* __restrict__ dk_keep,
                     float4* __restrict__ dv_keep, int B, int Hq, int Hkv, int L,
-                    BwdSchedule* __restrict__ sched, int4* __restrict__ items) {
+                    uint64_t full_groups, BwdSchedule* __restrict__ sched,
+                    int4* __restrict__ items) {
   const IndexHeader hdr = *idx.header;
   if (hdr.magic != kIndexMagic || hdr.B != B || hdr.L != L) return;
   if (blockIdx.x == 0) {
-    build_bwd_schedule(idx, B, Hkv, L, (L + 127) / 128, sched, items);
+    build_bwd_schedule(idx, B, Hkv, L, (L + 127) / 128, full_groups, sched, items);
     return;
   }
   constexpr int WPB = kPrepThreads / 32;
@@ -300,7 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const float2* __restrict__ stats,
                       float* __restrict__ dk_keep, float* __restrict__ dv_keep,
                       __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int B,
-                      int Hq, int Hkv, int L, float scale, float scale_log2, int* status) {
+                      int Hq, int Hkv, int L, float scale, float scale_log2,
+                      uint64_t full_groups, int* status) {
   using C = KvCfg<D>;
   constexpr int KVB = C::KVB, NST = C::NST, ACB = C::ACB;
   extern __shared__ uint8_t smem_raw[];
@@ -639,14 +650,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         e.rm = to_acc ? (((plane * L + kidx) << 2) | 1) : to_out ? (((plane * L + j) << 2) | 2) : 0;
       }
       const int nU = G * it.nt;
-      int4 blk_next = *reinterpret_cast<const int4*>(blocks + 4 * it.t0);
+      // a kv group with full causal attention: records for a window n >= L
+      const bool full = (full_groups >> it.g) & 1ull;
+      const int n_w = full ? L : n_win;
+      auto record = [&](int t2) {
+        return full ? full_block_record(t2, L) : *reinterpret_cast<const int4*>(blocks + 4 * t2);
+      };
+      int4 blk_next = record(it.t0);
       for (int u = 0; u < nU; ++u) {
         const int ugl = ug + u;
         const int t = it.t0 + u % it.nt;
         const int i0 = t * 128;
         const int4 blk = blk_next;  // loaded one iteration ahead
-        if (u + 1 < nU)
-          blk_next = *reinterpret_cast<const int4*>(blocks + 4 * (it.t0 + (u + 1) % it.nt));
+        if (u + 1 < nU) blk_next = record(it.t0 + (u + 1) % it.nt);
         // visible query columns of this row among the half's 64, as 2 words
         uint32_t vm[2];
         {
@@ -656,7 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (j < blk.x && j < count) c_hi = c_end;  // gathered by this query tile
           } else if (j >= blk.y && j < blk.z && j < L) {
             c_lo = j - i0;
-            c_hi = keep_j ? c_end : min(c_end, j + n_win - i0);
+            c_hi = keep_j ? c_end : min(c_end, j + n_w - i0);
           }
           vm[0] = range_bits(c_lo, c_hi, 2 * half);
           vm[1] = range_bits(c_lo, c_hi, 2 * half + 1);
@@ -776,7 +792,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tm_vk, IndexPtrs idx,
                       const float2* __restrict__ stats,
                       __nv_bfloat16* __restrict__ dq, int B, int Hq, int Hkv, int L, float scale,
-                      float scale_log2, int* status) {
+                      float scale_log2, uint64_t full_groups, int* status) {
   using C = DqCfg<D>;
   constexpr int QB = C::QB, NST = C::NST;
   extern __shared__ uint8_t smem_raw[];
@@ -840,7 +856,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   struct Item {
     int b, h, g, t, n_gather, lo, hi, nG, nT;
-    bool ok;
+    bool ok, full;
   };
   auto item_at = [&](int i, int k) -> Item {  // item i, the k-th of this CTA
     Item r;
@@ -849,7 +865,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     r.b = bh / Hq;
     r.h = bh % Hq;
     r.g = r.h / (Hq / Hkv);
-    const int4 blk = k < C::ITEMS
+    r.full = (full_groups >> r.g) & 1ull;  // full causal attention: records for n >= L
+    const int4 blk = r.full ? full_block_record(r.t, L)
+                     : k < C::ITEMS
                          ? s_blk[k]
                          : *reinterpret_cast<const int4*>(idx.blocks + ((size_t)r.b * T + r.t) * 4);
     r.n_gather = blk.x;
@@ -1041,7 +1059,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           const int jt = it.lo + 128 * (u - it.nG) + 64 * half;  // first key of this half
           const int n_causal = min(64, max(0, i_row - jt + 1));
-          const int c_win = i_row - n_win + 1 - jt;
+          const int c_win = i_row - (it.full ? L : n_win) + 1 - jt;
           const int wj = jt >> 5, sh = jt & 31;
           uint32_t kw[3];
 #pragma unroll
@@ -1169,8 +1187,8 @@ BwdWs bwd_ws(void* base, int B, int Hq, int Hkv, int L, int d) {
 template <int D>
 int launch_bwd_impl(IndexPtrs idx, const void* q, const void* k, const void* v, const void* o,
                     const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
-                    int Hq, int Hkv, int L, float scale, void* ws, int* status,
-                    cudaStream_t s) {
+                    int Hq, int Hkv, int L, float scale, uint64_t full_groups, void* ws,
+                    int* status, cudaStream_t s) {
   const BwdWs w = bwd_ws(ws, B, Hq, Hkv, L, D);
   const int T = (L + 127) / 128;
   const int sms = num_sms();
@@ -1186,7 +1204,7 @@ int launch_bwd_impl(IndexPtrs idx, const void* q, const void* k, const void* v, 
         reinterpret_cast<uint4*>(w.kk), reinterpret_cast<uint4*>(w.vk),
         static_cast<const uint4*>(o), static_cast<const uint4*>(dout), lse, w.stats,
         reinterpret_cast<float4*>(w.dk_keep), reinterpret_cast<float4*>(w.dv_keep), B, Hq, Hkv,
-        L, w.sched, w.items);
+        L, full_groups, w.sched, w.items);
   }
   CUtensorMap mq, mdo, mk, mv, mkk, mvk;
   if (!make_bf16_map(&mq, q, (uint64_t)B * Hq, L, D, 128) ||
@@ -1210,12 +1228,12 @@ int launch_bwd_impl(IndexPtrs idx, const void* q, const void* k, const void* v, 
   profile_mark(1, s);
   kv_k<<<sms, kThreads, KC::SMEM, s>>>(mkk, mvk, mk, mv, mq, mdo, idx, w.sched, w.items,
                                        w.stats, w.dk_keep, w.dv_keep, dkb, dvb, B, Hq, Hkv, L,
-                                       scale, scale_log2, status);
+                                       scale, scale_log2, full_groups, status);
   profile_mark(2, s);
   const int dq_items = B * Hq * T;
   dq_k<<<dq_items < sms ? dq_items : sms, kThreads, QC::SMEM, s>>>(
       mq, mdo, mk, mv, mkk, mvk, idx, w.stats, static_cast<__nv_bfloat16*>(dq), B, Hq, Hkv,
-      L, scale, scale_log2, status);
+      L, scale, scale_log2, full_groups, status);
   profile_mark(3, s);
   bwd_keep_scatter_kernel<D><<<keep_pass_ctas(keep_units(B, Hkv, L), sms), 256, 0, s>>>(
       idx, reinterpret_cast<const float4*>(w.dk_keep), reinterpret_cast<const float4*>(w.dv_keep),
@@ -1233,14 +1251,14 @@ size_t attn_bwd_tc_workspace(int B, int Hq, int Hkv, int L, int d) {
 
 int launch_attn_bwd_tc(IndexPtrs idx, const void* q, const void* k, const void* v, const void* o,
                        const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
-                       int Hq, int Hkv, int L, int d, float scale, void* ws, int* status,
-                       void* stream) {
+                       int Hq, int Hkv, int L, int d, float scale, uint64_t full_groups, void* ws,
+                       int* status, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (d == 64)
-    return launch_bwd_impl<64>(idx, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, L, scale, ws,
-                               status, s);
-  return launch_bwd_impl<128>(idx, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, L, scale, ws,
-                              status, s);
+    return launch_bwd_impl<64>(idx, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, L, scale,
+                               full_groups, ws, status, s);
+  return launch_bwd_impl<128>(idx, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, L, scale,
+                              full_groups, ws, status, s);
 }
 
 }  // namespace sep

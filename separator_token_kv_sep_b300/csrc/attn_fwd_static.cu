@@ -32,8 +32,8 @@ namespace sep {
 
 size_t attn_fwd_tc_workspace(int B, int Hkv, int L, int d);
 int launch_attn_fwd_tc(IndexPtrs idx, const void* q, const void* k, const void* v, void* o,
-                       float* lse, int B, int Hq, int Hkv, int L, int d, float scale, void* ws,
-                       int* status, void* stream);
+                       float* lse, int B, int Hq, int Hkv, int L, int d, float scale,
+                       uint64_t full_groups, void* ws, int* status, void* stream);
 
 namespace {
 
@@ -80,7 +80,7 @@ SEP_API sep_status sep_attn_fwd_static(const void* index_buf, const void* q, con
   int* st = device_status_ptr();
   if (!ws || !st) return SEP_ERR_CUDA;
   const IndexPtrs idx = index_ptrs(const_cast<void*>(index_buf), index_layout(B, L, SEP_BLOCK_M));
-  return launch_attn_fwd_tc(idx, q, k, v, o, lse, B, Hq, Hkv, L, d, scale, ws, st, stream) == 0
+  return launch_attn_fwd_tc(idx, q, k, v, o, lse, B, Hq, Hkv, L, d, scale, 0, ws, st, stream) == 0
              ? SEP_OK
              : SEP_ERR_CUDA;
 }

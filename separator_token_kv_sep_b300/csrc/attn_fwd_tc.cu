@@ -120,7 +120,8 @@ __device__ __forceinline__ void item_records(IndexPtrs idx, const int4* s_rec, i
 }
 
 __device__ __forceinline__ PairPlan load_plan(IndexPtrs idx, const int4* s_rec, int item,
-                                              int n_items, int B, int Hq, int L, int T) {
+                                              int n_items, int B, int Hq, int L, int T,
+                                              uint64_t full_groups, int grp) {
   PairPlan pl;
   pl.valid = false;
   pl.nT = 0;
@@ -133,6 +134,10 @@ __device__ __forceinline__ PairPlan load_plan(IndexPtrs idx, const int4* s_rec, 
   pl.hasB = pl.tA + 1 < T;
   int4 ba, bb;
   item_records(idx, s_rec, item, B, Hq, T, ba, bb);
+  if ((full_groups >> (pl.h / grp)) & 1ull) {
+    ba = full_block_record(pl.tA, L);
+    bb = full_block_record(pl.tA + 1, L);
+  }
   pl.nA = ba.x; pl.loA = ba.y; pl.hiA = ba.z;
   pl.nB = bb.x; pl.loB = bb.y; pl.hiB = bb.z;
   auto bad = [&](int4 r, int q0) {
@@ -155,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tm_kk,
                        const __grid_constant__ CUtensorMap tm_vk, IndexPtrs idx,
                        __nv_bfloat16* __restrict__ o, float* __restrict__ lse, int B, int Hq,
-                       int Hkv, int L, float scale_log2, int* status) {
+                       int Hkv, int L, float scale_log2, uint64_t full_groups, int* status) {
   using C = FwdCfg<D>;
   constexpr int QB = C::QB, NST = C::NST;
   extern __shared__ uint8_t smem_raw[];
@@ -228,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int n = 0, kq = 0;  // K/V stages and query pairs loaded
       bool ok = true;
       for (int it = blockIdx.x; ok && it < n_items; it += G) {
-        const PairPlan pl = load_plan(idx, s_rec, it, n_items, B, Hq, L, T);
+        const PairPlan pl = load_plan(idx, s_rec, it, n_items, B, Hq, L, T, full_groups, grp);
         if (!pl.valid) {
           report(status, SEP_ERR_DEVICE_BOUNDS);
           continue;
@@ -324,16 +329,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       bool ok = true;
       int it = blockIdx.x;
-      PairPlan pc = load_plan(idx, s_rec, it, n_items, B, Hq, L, T);
+      PairPlan pc = load_plan(idx, s_rec, it, n_items, B, Hq, L, T, full_groups, grp);
       while (it < n_items && !pc.valid) {
         it += G;
-        pc = load_plan(idx, s_rec, it, n_items, B, Hq, L, T);
+        pc = load_plan(idx, s_rec, it, n_items, B, Hq, L, T, full_groups, grp);
       }
       if (it < n_items) {
         int kq = 0, qs = 0, n = 0;  // current item's index and Q buffer; K/V stage count
         int u = pc.next(-1);
         int itn = it + G;
-        PairPlan pn = load_plan(idx, s_rec, itn, n_items, B, Hq, L, T);  // prefetched
+        PairPlan pn = load_plan(idx, s_rec, itn, n_items, B, Hq, L, T, full_groups, grp);  // prefetched
         ok = mbar_wait_warp(&q_full[0], 0, status) && mbar_wait_warp(&kv_full[0], 0, status);
         tc_fence_after();
         if (ok) {
@@ -348,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!same) {
             while (itn < n_items && !pn.valid) {
               itn += G;
-              pn = load_plan(idx, s_rec, itn, n_items, B, Hq, L, T);
+              pn = load_plan(idx, s_rec, itn, n_items, B, Hq, L, T, full_groups, grp);
             }
             if (itn < n_items) un = pn.next(-1);
           }
@@ -379,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             qs = qsn;
             ci0 = ci1 = 0;
             itn = it + G;
-            pn = load_plan(idx, s_rec, itn, n_items, B, Hq, L, T);
+            pn = load_plan(idx, s_rec, itn, n_items, B, Hq, L, T, full_groups, grp);
           }
           u = un;
         }
@@ -399,16 +404,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nwords = hdr.nwords;
     int cnt = 0, ko = 0;  // S tiles and items finished by this query tile
     bool ok = true;
-    PairPlan pn = load_plan(idx, s_rec, blockIdx.x, n_items, B, Hq, L, T);
+    PairPlan pn = load_plan(idx, s_rec, blockIdx.x, n_items, B, Hq, L, T, full_groups, grp);
     for (int it = blockIdx.x; ok && it < n_items; it += G) {
       const PairPlan pl = pn;
-      pn = load_plan(idx, s_rec, it + G, n_items, B, Hq, L, T);  // prefetch the next item
+      pn = load_plan(idx, s_rec, it + G, n_items, B, Hq, L, T, full_groups, grp);  // prefetch the next item
       if (!pl.valid || (x == 1 && !pl.hasB)) continue;
       const int b = pl.b, h = pl.h;
       const int i = (pl.tA + x) * 128 + r;
       const uint32_t* kbits = idx.keep_bits + (size_t)b * nwords;
       const int n_gath = x ? pl.nB : pl.nA;
       const int lo_x = x ? pl.loB : pl.loA;
+      const int n_w = ((full_groups >> (h / grp)) & 1ull) ? L : n_win;  // full groups: no window
       float m_used = -INFINITY, l = 0.f;
       int ci = 0;
       for (int u = 0; u < pl.nT; ++u) {
@@ -425,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           const int jt = pl.loA + 128 * (u - pl.nG);
           const int n_causal = min(128, max(0, i - jt + 1));  // columns c with jt+c <= i
-          const int c_win = i - n_win + 1 - jt;               // columns c >= c_win: window
+          const int c_win = i - n_w + 1 - jt;                 // columns c >= c_win: window
           const int c_lo = lo_x - jt;                         // columns below it: gathered
           const int wj = jt >> 5, sh = jt & 31;
           uint32_t kw[5];
@@ -556,8 +562,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D>
 int launch_fwd_impl(IndexPtrs idx, const void* q, const void* k, const void* v, void* o, float* lse,
-                    int B, int Hq, int Hkv, int L, float scale, void* ws, int* status,
-                    cudaStream_t s) {
+                    int B, int Hq, int Hkv, int L, float scale, uint64_t full_groups, void* ws,
+                    int* status, cudaStream_t s) {
   using C = FwdCfg<D>;
   const size_t plane_elems = (size_t)L * D;
   uint8_t* kk = static_cast<uint8_t*>(ws);
@@ -583,7 +589,7 @@ int launch_fwd_impl(IndexPtrs idx, const void* q, const void* k, const void* v, 
   const int grid = static_cast<int>(items < sms ? items : sms);  // persistent: one CTA per SM
   profile_mark(1, s);
   kern<<<grid, kThreads, C::SMEM, s>>>(mq, mk, mv, mkk, mvk, idx, static_cast<__nv_bfloat16*>(o),
-                                       lse, B, Hq, Hkv, L, scale_log2, status);
+                                       lse, B, Hq, Hkv, L, scale_log2, full_groups, status);
   const cudaError_t err = cudaGetLastError();
   profile_mark(2, s);
   return static_cast<int>(err);
@@ -596,11 +602,14 @@ size_t attn_fwd_tc_workspace(int B, int Hkv, int L, int d) {
 }
 
 int launch_attn_fwd_tc(IndexPtrs idx, const void* q, const void* k, const void* v, void* o,
-                       float* lse, int B, int Hq, int Hkv, int L, int d, float scale, void* ws,
-                       int* status, void* stream) {
+                       float* lse, int B, int Hq, int Hkv, int L, int d, float scale,
+                       uint64_t full_groups, void* ws, int* status, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (d == 64) return launch_fwd_impl<64>(idx, q, k, v, o, lse, B, Hq, Hkv, L, scale, ws, status, s);
-  return launch_fwd_impl<128>(idx, q, k, v, o, lse, B, Hq, Hkv, L, scale, ws, status, s);
+  if (d == 64)
+    return launch_fwd_impl<64>(idx, q, k, v, o, lse, B, Hq, Hkv, L, scale, full_groups, ws, status,
+                               s);
+  return launch_fwd_impl<128>(idx, q, k, v, o, lse, B, Hq, Hkv, L, scale, full_groups, ws, status,
+                              s);
 }
 
 }  // namespace sep

@@ -321,6 +321,13 @@ __device__ __forceinline__ void fmul2(float& d0, float& d1, float a0, float a1, 
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
+// Block record {n_gather, dense_lo, dense_hi, flags} of query tile t for a
+// head that attends with full causal attention: what the index holds for a
+// window n >= L (no gathered keys, the band from key 0 to the tile's last row).
+__device__ __forceinline__ int4 full_block_record(int t, int L) {
+  return make_int4(0, 0, min(L, 128 * t + 128), 1);
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

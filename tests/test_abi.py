@@ -61,6 +61,14 @@ def test_host_checks_reject_bad_arguments(lib):
     assert L.sep_attn_fwd(P, P, P, P, P, P, 1, 2, 2, 128, 64, 1, F(0), P, 16, None) == 7
     assert L.sep_attn_bwd(P, P, P, P, P, P, P, P, P, P, 1, 2, 2, 128, 64, 0, F(0), P, 10**9,
                           None) == 2
+    # hybrid heads: a full-group bit at or above Hkv, and the shape checks
+    assert L.sep_attn_fwd_hybrid(P, P, P, P, P, P, 1, 4, 2, 128, 64, 1 << 2, F(0), P, 10**9,
+                                 None) == 1
+    assert L.sep_attn_fwd_hybrid(P, P, P, P, P, P, 1, 4, 2, 128, 96, 1, F(0), P, 10**9,
+                                 None) == 2
+    assert L.sep_attn_fwd_hybrid(P, P, P, P, P, P, 1, 4, 2, 128, 64, 3, F(0), P, 16, None) == 7
+    assert L.sep_attn_bwd_hybrid(P, P, P, P, P, P, P, P, P, P, 1, 4, 2, 128, 64, 1 << 5, F(0),
+                                 P, 10**9, None) == 1
     assert L.sep_status_string(5) == b"device wait timed out"
 
 
