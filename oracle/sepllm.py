@@ -216,6 +216,37 @@ def attention_forward_sampled(q, k, v, ids, sep_ids, a: int, n: int,
     return o, lse
 
 
+def attention_forward_heads(q, k, v, ids, sep_ids, a: int, n: int, heads,
+                            row_block: int = 256, scale: float | None = None):
+    """Every row of the given q heads, for sizes where the dense L x L
+    problem is too large for one float64 pass.  Rows are taken in blocks;
+    for each block the explicit mask rows are built over the keys up to the
+    block's last row, and the key columns that no row of the block sees are
+    left out before attention_rows -- their masked scores are -inf, so they
+    add exp(-inf) = 0 to every row's sums and change nothing.
+    Returns O [B, |heads|, L, d] and LSE [B, |heads|, L]."""
+    q = np.asarray(q)
+    B, Hq, L, d = q.shape
+    Hkv = k.shape[1]
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    o = np.zeros((B, len(heads), L, d))
+    lse = np.zeros((B, len(heads), L))
+    for b in range(B):
+        for r0 in range(0, L, row_block):
+            r1 = min(L, r0 + row_block)
+            rows = np.arange(r0, r1)
+            mask = sepllm_mask_rows(ids[b, :r1], sep_ids, a, n, rows)
+            cols = np.flatnonzero(mask.any(axis=0))
+            mask = mask[:, cols]
+            for hi, h in enumerate(heads):
+                g = _kv_head(h, Hq, Hkv)
+                o[b, hi, r0:r1], lse[b, hi, r0:r1] = attention_rows(
+                    np.asarray(q[b, h, r0:r1], dtype=np.float64),
+                    k[b, g, cols], v[b, g, cols], mask, scale)
+    return o, lse
+
+
 def attention_backward(q, k, v, dout, ids, sep_ids, a: int, n: int,
                        scale: float | None = None):
     """Textbook backward of masked softmax attention, float64.

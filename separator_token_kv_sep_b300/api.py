@@ -126,6 +126,21 @@ def _dtype_code(t: torch.Tensor) -> int:
     raise TypeError(f"unsupported dtype {t.dtype}")
 
 
+def _require(t: torch.Tensor, name: str, dtype, shape=None) -> None:
+    """Raise unless t is a contiguous CUDA tensor of the given dtype (and
+    shape): for entry points whose C signature fixes the element type."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor, got {type(t).__name__}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: expected a CUDA tensor, got device {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous tensor")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
 def _empty_bytes(nbytes: int, device) -> torch.Tensor:
     # torch's caching allocator returns 512-byte aligned blocks
     return torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=device)
@@ -227,10 +242,16 @@ def sep_attn_fwd_static(index_buf, q, k, v, scale: float = 0.0, o=None, lse=None
     Returns (o, lse)."""
     B, Hq, L, d = q.shape
     Hkv = k.shape[1]
+    # the C entry has no dtype argument and reads bf16: anything else would
+    # be reinterpreted silently, so it is rejected here
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _require(t, name, torch.bfloat16)
     if o is None:
         o = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, Hq, L), dtype=torch.float32, device=q.device)
+    _require(o, "o", torch.bfloat16, shape=tuple(q.shape))
+    _require(lse, "lse", torch.float32, shape=(B, Hq, L))
     _check(_lib.sep_attn_fwd_static(_ptr(index_buf), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
                                     _ptr(lse), B, Hq, Hkv, L, d, float(scale),
                                     _stream(stream)), "sep_attn_fwd_static")

@@ -4,6 +4,8 @@
 #include <math.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "layout.h"
 
@@ -41,14 +43,18 @@ void profile_mark(int i, void* stream) {
 int* device_status_ptr() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
-  static int* cache[64] = {nullptr};
   if (dev < 0 || dev >= 64) return nullptr;
-  if (!cache[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
-    cache[dev] = static_cast<int*>(p);
+  // per-device cache; host threads may race on the first lookup, so the
+  // entries are atomic (a lost race repeats the same lookup)
+  static std::atomic<int*> cache[64];
+  int* p = cache[dev].load(std::memory_order_acquire);
+  if (!p) {
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_device_status) != cudaSuccess || !a) return nullptr;
+    p = static_cast<int*>(a);
+    cache[dev].store(p, std::memory_order_release);
   }
-  return cache[dev];
+  return p;
 }
 
 namespace {
@@ -139,9 +145,11 @@ SEP_API size_t sep_attn_workspace_bytes(int B, int Hq, int Hkv, int L, int d, se
 
 namespace {
 
-// Bits of full_groups at or above Hkv must be clear.
+// Bits of full_groups at or above Hkv must be clear; with more than 64 kv
+// heads no group can be named, so the mask must be 0.
 bool groups_ok(uint64_t full_groups, int Hkv) {
-  return Hkv >= 64 || (full_groups >> Hkv) == 0;
+  if (Hkv > 64) return full_groups == 0;
+  return Hkv == 64 || (full_groups >> Hkv) == 0;
 }
 
 sep_status attn_fwd(const void* index_buf, const void* q, const void* k, const void* v, void* o,

@@ -156,7 +156,7 @@ __device__ void build_bwd_schedule(IndexPtrs idx, int B, int Hkv, int L, int T,
         const int t0 = tb + cc * kKeepChunk, t1 = min(T, t0 + kKeepChunk);
         int gi = 0;
         for (int g = 0; g < Hkv; ++g) {
-          if ((full_groups >> g) & 1ull) continue;
+          if (group_full(full_groups, g)) continue;
           items[total + (size_t)(ex + cc) * nsep + gi] =
               make_int4(kItemKeep, b * Hkv + g, kt * 128, (t0 << 16) | t1);
           ++gi;
@@ -179,7 +179,7 @@ __device__ void build_bwd_schedule(IndexPtrs idx, int B, int Hkv, int L, int T,
     for (int g = 0; g < Hkv; ++g)
       items[n_keep + (size_t)id * Hkv + g] =
           make_int4(kItemDense, b * Hkv + g, jt * 128,
-                    (jt << 16) | (((full_groups >> g) & 1ull) ? T : max(lo, jt + 1)));
+                    (jt << 16) | (group_full(full_groups, g) ? T : max(lo, jt + 1)));
   }
   if (threadIdx.x == 0) {
     sched->n_items = n_keep + B * T * Hkv;
@@ -651,7 +651,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int nU = G * it.nt;
       // a kv group with full causal attention: records for a window n >= L
-      const bool full = (full_groups >> it.g) & 1ull;
+      const bool full = group_full(full_groups, it.g);
       const int n_w = full ? L : n_win;
       auto record = [&](int t2) {
         return full ? full_block_record(t2, L) : *reinterpret_cast<const int4*>(blocks + 4 * t2);
@@ -865,7 +865,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     r.b = bh / Hq;
     r.h = bh % Hq;
     r.g = r.h / (Hq / Hkv);
-    r.full = (full_groups >> r.g) & 1ull;  // full causal attention: records for n >= L
+    r.full = group_full(full_groups, r.g);  // full causal attention: records for n >= L
     const int4 blk = r.full ? full_block_record(r.t, L)
                      : k < C::ITEMS
                          ? s_blk[k]

@@ -134,7 +134,7 @@ __device__ __forceinline__ PairPlan load_plan(IndexPtrs idx, const int4* s_rec, 
   pl.hasB = pl.tA + 1 < T;
   int4 ba, bb;
   item_records(idx, s_rec, item, B, Hq, T, ba, bb);
-  if ((full_groups >> (pl.h / grp)) & 1ull) {
+  if (group_full(full_groups, pl.h / grp)) {
     ba = full_block_record(pl.tA, L);
     bb = full_block_record(pl.tA + 1, L);
   }
@@ -414,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t* kbits = idx.keep_bits + (size_t)b * nwords;
       const int n_gath = x ? pl.nB : pl.nA;
       const int lo_x = x ? pl.loB : pl.loA;
-      const int n_w = ((full_groups >> (h / grp)) & 1ull) ? L : n_win;  // full groups: no window
+      const int n_w = group_full(full_groups, h / grp) ? L : n_win;  // full groups: no window
       float m_used = -INFINITY, l = 0.f;
       int ci = 0;
       for (int u = 0; u < pl.nT; ++u) {

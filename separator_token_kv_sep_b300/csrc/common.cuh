@@ -321,6 +321,12 @@ __device__ __forceinline__ void fmul2(float& d0, float& d1, float a0, float a1, 
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
+// Whether kv group g attends with full causal attention (bit g of the
+// hybrid-heads mask; groups at or above 64 never do).
+__host__ __device__ __forceinline__ bool group_full(uint64_t full_groups, int g) {
+  return g >= 0 && g < 64 && ((full_groups >> g) & 1ull) != 0;
+}
+
 // Block record {n_gather, dense_lo, dense_hi, flags} of query tile t for a
 // head that attends with full causal attention: what the index holds for a
 // window n >= L (no gathered keys, the band from key 0 to the tile's last row).

@@ -14,6 +14,8 @@
 // padded keep count costs one cached load.
 #pragma once
 
+#include <atomic>
+
 #include "common.cuh"
 #include "layout.h"
 
@@ -131,12 +133,17 @@ __device__ __forceinline__ void scatter_keep_unit(IndexPtrs idx, const float4* _
 
 // Number of SMs of the current device (148 if the query fails).
 inline int num_sms() {
-  static int n[64] = {0};
+  // per-device cache; concurrent first lookups store the same value
+  static std::atomic<int> n[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (!n[dev] && cudaDeviceGetAttribute(&n[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    n[dev] = 148;
-  return n[dev];
+  int v = n[dev].load(std::memory_order_relaxed);
+  if (!v) {
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v < 1)
+      v = 148;
+    n[dev].store(v, std::memory_order_relaxed);
+  }
+  return v;
 }
 
 // CTAs of 256 threads for a keep-row pass over `units` units: a few per SM,

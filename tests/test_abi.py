@@ -115,3 +115,18 @@ def test_cache_host_checks():
                              ctypes.c_float(0), None) == 1
     assert L_.sep_cache_step(ctypes.byref(good), P, P, P, P, P, arr, 1, P, 30,
                              ctypes.c_float(0), None) == 1
+
+
+def test_static_forward_binding_rejects_wrong_tensors(lib):
+    """sep_attn_fwd_static's C signature has no dtype: the binding refuses
+    anything but contiguous bf16 CUDA tensors before calling the library
+    (checked here on CPU tensors, so no call reaches a kernel)."""
+    import torch
+    from separator_token_kv_sep_b300 import api
+    buf = torch.zeros(4096, dtype=torch.uint8)
+    q32 = torch.zeros(1, 2, 128, 64, dtype=torch.float32)
+    with pytest.raises(TypeError):
+        api.sep_attn_fwd_static(buf, q32, q32, q32)
+    qbf = torch.zeros(1, 2, 128, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):  # bf16 but not on a CUDA device
+        api.sep_attn_fwd_static(buf, qbf, qbf, qbf)

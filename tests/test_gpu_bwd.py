@@ -7,7 +7,7 @@ import torch
 
 from oracle import sepllm as O
 from separator_token_kv_sep_b300 import synth
-from helpers import assert_close_rel, to_dev
+from helpers import assert_close_abs, assert_close_rel, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -20,16 +20,22 @@ def gpu_fwd_bwd(q, k, v, do, ids, a, n, sep_ids=synth.SEP_IDS):
     dq, dk, dv = api.sep_attn_bwd(buf, tq, tk, tv, o, lse, tdo)
     torch.cuda.synchronize()
     assert api.sep_get_device_status() == 0
-    return [x.float().cpu().numpy() for x in (dq, dk, dv)]
+    return [x.float().cpu().numpy() for x in (dq, dk, dv, o)] + [lse.cpu().numpy()]
 
 
-def check(q, k, v, do, ids, a, n, batches=None, sep_ids=synth.SEP_IDS):
-    gq, gk, gv = gpu_fwd_bwd(q, k, v, do, ids, a, n, sep_ids)
+def check(q, k, v, do, ids, a, n, batches=None, sep_ids=synth.SEP_IDS, forward=False):
+    """dQ, dK, dV (and with forward=True the forward's O and LSE) of the
+    given batch rows against the oracle."""
+    gq, gk, gv, go, glse = gpu_fwd_bwd(q, k, v, do, ids, a, n, sep_ids)
     bs = list(range(q.shape[0])) if batches is None else batches
     rq, rk, rv = O.attention_backward(q[bs], k[bs], v[bs], do[bs], ids[bs], sep_ids, a, n)
     assert_close_rel(gq[bs], rq, what="dQ")
     assert_close_rel(gk[bs], rk, what="dK")
     assert_close_rel(gv[bs], rv, what="dV")
+    if forward:
+        ro, rl = O.attention_forward(q[bs], k[bs], v[bs], ids[bs], sep_ids, a, n)
+        assert_close_rel(go[bs], ro, what="O")
+        assert_close_abs(glse[bs], rl, 1e-3, "LSE")
 
 
 @pytest.mark.parametrize("B,Hq,Hkv,L,d,a,n,p", [
@@ -63,6 +69,8 @@ def test_bwd_pythia_train_n128_full():
 
 @pytest.mark.parametrize("cfg", [synth.PYTHIA_TRAIN_N64, synth.PYTHIA_TRAIN_FULL],
                          ids=lambda c: c.name)
-def test_bwd_pythia_train_sampled_batches(cfg):
+def test_bwd_pythia_train_variants_full(cfg):
+    """The n = 64 and full-attention (n = L) training variants on every
+    batch row: forward O and LSE, then dQ, dK, dV."""
     q, k, v, do, ids = synth.prefill_inputs(cfg)
-    check(q, k, v, do, ids, cfg.a, cfg.n, batches=[0, cfg.B - 1])
+    check(q, k, v, do, ids, cfg.a, cfg.n, forward=True)

@@ -98,3 +98,17 @@ def test_long_prefill_sampled(cfg):
     ro, rl = O.attention_forward_sampled(q, k, v, ids, synth.SEP_IDS, cfg.a, cfg.n, rows, heads)
     assert_close_rel(o[:, heads][:, :, rows], ro, what="O")
     assert_close_abs(lse[:, heads][:, :, rows], rl, 1e-3, "LSE")
+
+
+def test_long_prefill_all_rows_two_heads():
+    """The L = 65536 prefill on every row of two q heads (of different kv
+    groups), beside the row sample above: a fault confined to rows between
+    the samples, deep in the sequence, shows up here."""
+    cfg = synth.LONG_PREFILL
+    q, k, v, _, ids = synth.prefill_inputs(cfg)
+    o, lse = gpu_forward(q, k, v, ids, cfg.a, cfg.n, "bf16")
+    heads = [3, 28]
+    ro, rl = O.attention_forward_heads(q, k, v, ids, synth.SEP_IDS, cfg.a, cfg.n, heads,
+                                       row_block=512)
+    assert_close_rel(o[:, heads], ro, what="O")
+    assert_close_abs(lse[:, heads], rl, 1e-3, "LSE")

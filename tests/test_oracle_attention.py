@@ -122,3 +122,20 @@ def test_backward_matches_library_autograd(a, n, p, Hq, Hkv):
     out.backward(torch.from_numpy(do.astype(np.float64)))
     for mine, ref in ((dq, tq.grad), (dk, tk.grad), (dv, tv.grad)):
         np.testing.assert_allclose(mine, ref.numpy(), rtol=1e-10, atol=1e-11)
+
+
+@pytest.mark.parametrize("L,a,n,p,rb", [(300, 4, 37, 0.12, 64), (257, 0, 1, 0.5, 100),
+                                         (200, 3, 500, 0.0, 7)])
+def test_forward_heads_equals_dense_forward(L, a, n, p, rb):
+    """The row-blocked forward that leaves out the key columns no row of a
+    block sees equals the dense masked forward (pinned against SDPA above)."""
+    rng = np.random.default_rng(L + n)
+    q = rng.standard_normal((2, 4, L, 8))
+    k = rng.standard_normal((2, 2, L, 8))
+    v = rng.standard_normal((2, 2, L, 8))
+    ids = synth.token_ids(rng, (2, L), p)
+    o, lse = O.attention_forward(q, k, v, ids, synth.SEP_IDS, a, n)
+    heads = [0, 3]
+    oh, lh = O.attention_forward_heads(q, k, v, ids, synth.SEP_IDS, a, n, heads, row_block=rb)
+    assert np.max(np.abs(oh - o[:, heads])) < 1e-12
+    assert np.max(np.abs(lh - lse[:, heads])) < 1e-12

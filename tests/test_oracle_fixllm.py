@@ -4,6 +4,8 @@ keep-mask helper with the pinned SepLLM mask, delta = 1 as full causal
 attention (against torch's float64 SDPA), and the backward against central
 finite differences."""
 
+import itertools
+
 import numpy as np
 import pytest
 import torch
@@ -71,3 +73,51 @@ def test_fixllm_backward_finite_differences():
             args_m = [xm if y is x else y for y in (q, k, v)]
             fd = (loss(*args_p) - loss(*args_m)) / (2 * eps)
             assert abs(fd - g[idx]) < 1e-6, (idx, fd, g[idx])
+
+
+@pytest.mark.parametrize("L", [1, 6, 10])
+def test_keep_index_from_flags_invariants_exhaustive(L):
+    """keep_index_from_flags over every keep pattern of length L: the
+    positions are the kept ones in ascending order, the count is their
+    number, the prefix steps by one at each kept token and indexes the
+    positions back (a prefix-scan compaction, checked element by element)."""
+    pats = np.array(list(itertools.product([0, 1], repeat=L)), bool)
+    kp, kpos, kc = F.keep_index_from_flags(pats)
+    for b, keep in enumerate(pats):
+        pos = kpos[b]
+        assert kc[b] == keep.sum() == len(pos)
+        assert np.all(np.diff(pos) > 0)
+        assert all(keep[p] for p in pos)
+        assert kp[b, 0] == 0 and kp[b, L] == kc[b]
+        for j in range(L):
+            assert kp[b, j + 1] - kp[b, j] == int(keep[j])
+        for k, p in enumerate(pos):
+            assert kp[b, p] == k
+
+
+def test_bitmask_from_flags_bits():
+    """Bit j % 32 of word j // 32 is keep[j], read back bit by bit with
+    Python integers; words past the row end are zero-padded."""
+    rng = np.random.default_rng(6)
+    keep = rng.random((3, 101)) < 0.3
+    bm = F.bitmask_from_flags(keep)
+    assert bm.shape == (3, 4) and bm.dtype == np.uint32
+    for b in range(3):
+        for j in range(101):
+            assert ((int(bm[b, j >> 5]) >> (j & 31)) & 1) == int(keep[b, j])
+        assert int(bm[b, 3]) >> (101 - 96) == 0
+
+
+def test_flag_helpers_equal_pinned_sepllm_functions():
+    """On SepLLM keep sets the FixLLM helpers give what the pinned SepLLM
+    index functions give from the token ids."""
+    rng = np.random.default_rng(9)
+    ids = synth.token_ids(rng, (3, 333), 0.15)
+    for a in (0, 4):
+        keep = O.keep_flags(ids, synth.SEP_IDS, a)
+        kp, kpos, kc = F.keep_index_from_flags(keep)
+        kp2, kpos2, kc2 = O.keep_index(ids, synth.SEP_IDS, a)
+        assert np.array_equal(kp, kp2) and np.array_equal(kc, kc2)
+        assert all(np.array_equal(x, y) for x, y in zip(kpos, kpos2))
+        assert np.array_equal(F.bitmask_from_flags(keep),
+                              O.separator_bitmask(ids, synth.SEP_IDS, a))

@@ -8,7 +8,8 @@ nothing after start-up.  For them the library keeps the forward's scratch
 caller workspace.  These tests call it through the C ABI and check it
 against sep_attn_fwd, which takes a workspace, on two calls in a row: the
 second call runs on a shape with a different keep count, so stale rows of
-the shared array would show up in its output.
+the shared array would show up in its output.  The first call is also
+checked directly against the float64 oracle.
 
 This file is named to be collected last.
 """
@@ -19,6 +20,7 @@ import numpy as np
 import pytest
 import torch
 
+from oracle import sepllm as O
 from separator_token_kv_sep_b300 import synth
 from helpers import assert_close_abs, assert_close_rel, to_dev
 
@@ -49,15 +51,22 @@ def _forward_both(api, B, Hq, Hkv, L, d, a, n, p, seed):
     torch.cuda.synchronize()
     assert api.sep_get_device_status() == 0
     return o.float().cpu().numpy(), lse.cpu().numpy(), \
-        o_ref.float().cpu().numpy(), lse_ref.cpu().numpy()
+        o_ref.float().cpu().numpy(), lse_ref.cpu().numpy(), (q, k, v, ids)
 
 
 def test_static_forward_matches_workspace_forward_twice():
     from separator_token_kv_sep_b300 import api
-    for case in CASES:
-        o, lse, o_ref, lse_ref = _forward_both(api, *case)
+    for x, case in enumerate(CASES):
+        o, lse, o_ref, lse_ref, inputs = _forward_both(api, *case)
         assert_close_rel(o, o_ref, what=f"O {case}")
         assert_close_abs(lse, lse_ref, 1e-3, f"LSE {case}")
+        if x == 0:
+            # the first call also against the float64 oracle directly
+            q, k, v, ids = inputs
+            a, n = case[5], case[6]
+            ro, rl = O.attention_forward(q, k, v, ids, synth.SEP_IDS, a, n)
+            assert_close_rel(o, ro, what=f"O vs oracle {case}")
+            assert_close_abs(lse, rl, 1e-3, f"LSE vs oracle {case}")
 
 
 def test_static_forward_rejects_shapes_beyond_its_scratch():
