@@ -19,6 +19,8 @@ Modules
                of the separators) on the same mask machinery.
 ``hybrid``     hybrid heads: kv groups with full causal attention beside
                groups under the SepLLM (or sliding-window) mask.
+``varlen``     packed batches: several sequences in one row, the mask
+               restarting at each sequence start.
 ``streaming``  the four-block streaming KV cache (initial, separator, past
                window, local window) with eviction into the separator cache,
                position shifting inside the cache, RoPE and decode attention.
@@ -32,4 +34,4 @@ the block-list record format).  Those are marked "parity unpinned" where
 they are defined.
 """
 
-from . import fixllm, hybrid, sepllm, streaming  # noqa: F401
+from . import fixllm, hybrid, sepllm, streaming, varlen  # noqa: F401

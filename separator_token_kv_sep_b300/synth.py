@@ -177,3 +177,25 @@ def stream_inputs(cfg: StreamConfig, seed: int | None = None, S: int | None = No
     k = round_to_bf16(rng.standard_normal((P, S, cfg.Hkv, cfg.d), dtype=np.float32))
     v = round_to_bf16(rng.standard_normal((P, S, cfg.Hkv, cfg.d), dtype=np.float32))
     return q, k, v, ids
+
+
+def packed_inputs(lengths, Hq: int, Hkv: int, d: int, p: float, seed: int,
+                  backward: bool = True):
+    """A packed batch of sequences of the given lengths: q [Hq, total, d],
+    k, v [Hkv, total, d], dO [Hq, total, d] (bf16-exact float32; dO None
+    without backward), ids int32 [total] and cu int32 [B + 1] (cu[b] = first
+    packed position of sequence b).  Draw order: ids, Q, K, V, dO."""
+    lengths = [int(x) for x in lengths]
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    total = int(cu[-1])
+    rng = np.random.Generator(np.random.PCG64(seed))
+    ids = token_ids(rng, (total,), p)
+
+    def draw(shape):
+        return round_to_bf16(rng.standard_normal(shape, dtype=np.float32))
+
+    q = draw((Hq, total, d))
+    k = draw((Hkv, total, d))
+    v = draw((Hkv, total, d))
+    do = draw((Hq, total, d)) if backward else None
+    return q, k, v, do, ids, cu
