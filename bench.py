@@ -613,10 +613,90 @@ def run_variants(args, rank, device, flush, peaks):
                      "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                      "visited_over_causal": round(pairs / (B * L * (L + 1) / 2), 4),
                      "frac_of_bf16_peak": round(flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)}
+    out["packed_docs_n128"] = run_packed_variant(q, k, v, dout, ids_np, cfg, steps, device, flush,
+                                                 peaks, rank)
     out["note"] = ("index + fwd + bwd of the Pythia-shaped workload (B8 H12 L2048 d64 bf16, a4) "
                    "per variant; FLOPs 14 d per visited pair; CUDA graph, L2 flushed before "
                    f"each step, {steps} timed steps")
     return out
+
+
+def pack_lengths(total: int, lo: int, hi: int, seed: int):
+    """Seeded document lengths, uniform in [lo, hi], the last one cut so they
+    sum to total."""
+    rng = np.random.default_rng(seed)
+    out = []
+    while sum(out) < total:
+        out.append(int(min(rng.integers(lo, hi + 1), total - sum(out))))
+    return out
+
+
+def run_packed_variant(q, k, v, dout, ids_np, cfg, steps, device, flush, peaks, rank):
+    """The same token budget (B8 x 2048 tokens, 12 heads, d64) as one pack of
+    documents of seeded lengths in [64, 2048]: sep_build_index_varlen +
+    sep_attn_fwd_varlen + sep_attn_bwd_varlen, each document masked on its
+    own (its own sinks, window and separators)."""
+    import torch
+    from separator_token_kv_sep_b300 import api
+    B, Hq, L, d = q.shape
+    Hkv = k.shape[1]
+    total = B * L
+    lengths = pack_lengths(total, 64, L, shard_seed(3001, rank))
+    cu_np = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    max_len = int(max(lengths))
+    nb = len(lengths)
+    # per head, the batch rows' tokens one after another, cut at the
+    # document boundaries instead of the row boundaries
+    pq = q.permute(1, 0, 2, 3).reshape(Hq, total, d).contiguous()
+    pk = k.permute(1, 0, 2, 3).reshape(Hkv, total, d).contiguous()
+    pv = v.permute(1, 0, 2, 3).reshape(Hkv, total, d).contiguous()
+    pdo = dout.permute(1, 0, 2, 3).reshape(Hq, total, d).contiguous()
+    ids_flat = ids_np.reshape(-1)
+    ids = torch.from_numpy(ids_flat).to(device)
+    cu = torch.from_numpy(cu_np).to(device)
+    idx_buf = torch.empty(api.sep_index_bytes(nb, max_len), dtype=torch.uint8, device=device)
+    ws_f = torch.empty(api.sep_attn_workspace_bytes_varlen(nb, total, max_len, Hq, Hkv, d, False),
+                       dtype=torch.uint8, device=device)
+    ws_b = torch.empty(api.sep_attn_workspace_bytes_varlen(nb, total, max_len, Hq, Hkv, d, True),
+                       dtype=torch.uint8, device=device)
+    o = torch.empty_like(pq)
+    lse = torch.empty((Hq, total), dtype=torch.float32, device=device)
+    dq, dk, dv = torch.empty_like(pq), torch.empty_like(pk), torch.empty_like(pv)
+
+    def step():
+        api.sep_build_index_varlen(ids, cu, max_len, synth.SEP_IDS, cfg.a, cfg.n,
+                                   index_buf=idx_buf)
+        api.sep_attn_fwd_varlen(idx_buf, pq, pk, pv, nb, max_len, o=o, lse=lse, ws=ws_f)
+        api.sep_attn_bwd_varlen(idx_buf, pq, pk, pv, o, lse, pdo, nb, max_len, dq=dq, dk=dk,
+                                dv=dv, ws=ws_b)
+    step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    times = []
+    for it in range(steps + 3):
+        flush.zero_()
+        e0.record()
+        graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        if it >= 3:
+            times.append(e0.elapsed_time(e1))
+    assert api.sep_get_device_status() == 0
+    ms = sum(times) / len(times)
+    pairs = sum(visited_pairs_per_head(ids_flat[None, cu_np[b]:cu_np[b + 1]], cfg.a, cfg.n)
+                for b in range(nb))
+    flops = 14.0 * d * pairs * Hq
+    causal = sum(x * (x + 1) // 2 for x in lengths)
+    return {"window_n": cfg.n, "documents": nb, "max_len": max_len, "total_tokens": total,
+            "ms": round(ms, 5), "value": round(flops / (ms * 1e-3) / 1e12, 2),
+            "unit": "TFLOP/s", "visited_over_causal": round(pairs / causal, 4),
+            "frac_of_bf16_peak": round(flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+            "note": "one pack of seeded document lengths in [64, 2048] (the last one cut): "
+                    "sep_build_index_varlen + sep_attn_fwd_varlen + sep_attn_bwd_varlen"}
 
 
 def run_index_scaling(args, rank, device, flush):

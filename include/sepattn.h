@@ -119,6 +119,36 @@ sep_status sep_build_index(const int32_t* ids, int B, int L,
 sep_status sep_build_index_fixed(int B, int L, int a, int n, int delta, int block_m,
                                  void* index_buf, size_t index_bytes, void* stream);
 
+/* sep_build_index_varlen -- the index of a PACK: B sequences of different
+ * lengths stored one after another, as a training step packs documents.
+ * The mask is defined per sequence (anthology record lit-748, "The mask",
+ * "Training from scratch"); the pages say nothing of packing, so each
+ * sequence of a pack is treated as a sequence of its own: its positions
+ * restart at 0, its first `a` tokens are its sinks, and no query sees a key
+ * of another sequence.
+ *
+ *   ids         device int32 [total] token ids of all sequences, packed.
+ *   cu_seqlens  device int32 [B + 1] sequence starts: sequence b is packed
+ *               rows [cu_seqlens[b], cu_seqlens[b+1]); cu_seqlens[0] = 0 and
+ *               cu_seqlens[B] = total.  Empty sequences are allowed.
+ *   max_len     the longest sequence length (>= 1); every per-sequence
+ *               field of the index is padded to it.  Size the buffer with
+ *               sep_index_bytes(B, max_len, block_m).
+ *   other arguments as sep_build_index.
+ * The fields (sep_index_views with L = max_len) hold, for each sequence, what
+ * sep_build_index gives for that sequence alone in local positions, padded:
+ * keep_prefix[b][j] = keep_count[b] for j >= len_b, keep_pos -1 past the
+ * count, empty block records {0, 0, 0, 0} for tiles at or past len_b, zero
+ * keep bits past len_b.
+ * Errors: SEP_ERR_INVALID_ARG, SEP_ERR_UNSUPPORTED, SEP_ERR_WORKSPACE,
+ * SEP_ERR_CUDA; device: SEP_ERR_DEVICE_BOUNDS if cu_seqlens is not a valid
+ * partition of [0, total) into lengths <= max_len (the offending sequences
+ * index as empty). */
+sep_status sep_build_index_varlen(const int32_t* ids, const int32_t* cu_seqlens, int B,
+                                  int total, int max_len, const int32_t* sep_ids,
+                                  int n_sep_ids, int a, int n, int block_m, void* index_buf,
+                                  size_t index_bytes, void* stream);
+
 /* Device pointers to the fields of an index buffer (pure pointer arithmetic,
  * no device access).  Any output pointer may be NULL. */
 sep_status sep_index_views(void* index_buf, int B, int L, int block_m,
@@ -209,6 +239,36 @@ sep_status sep_attn_bwd_hybrid(const void* index_buf, const void* q, const void*
                                unsigned long long full_groups, float scale,
                                void* ws, size_t ws_bytes, void* stream);
 
+/* Workspace bytes of sep_attn_fwd_varlen (backward = 0) and
+ * sep_attn_bwd_varlen (backward = 1) for a pack of B sequences of at most
+ * max_len rows in `total` rows (0 if the shape is invalid). */
+size_t sep_attn_workspace_bytes_varlen(int B, int total, int max_len, int Hq, int Hkv, int d,
+                                       int backward);
+
+/* sep_attn_fwd_varlen / sep_attn_bwd_varlen -- sep_attn_fwd and
+ * sep_attn_bwd over a pack indexed by sep_build_index_varlen: the mask of
+ * each sequence on its own, no pair across sequences.
+ *
+ *   q, o, dout, dq  [Hq, total, d] bf16: per head, the sequences' rows packed
+ *                   in the order of cu_seqlens.
+ *   k, v, dk, dv    [Hkv, total, d] bf16.
+ *   lse             float32 [Hq, total].
+ *   B, total, max_len  as given to sep_build_index_varlen.
+ *   ws              ws_bytes >= sep_attn_workspace_bytes_varlen(..).
+ * Everything else (GQA mapping, d in {64, 128}, scale, errors) as
+ * sep_attn_fwd / sep_attn_bwd with dtype SEP_BF16.  total = 0 does nothing.
+ * Device: SEP_ERR_DEVICE_BOUNDS if the index is not a pack index of these
+ * B, max_len and total. */
+sep_status sep_attn_fwd_varlen(const void* index_buf, const void* q, const void* k,
+                               const void* v, void* o, float* lse, int B, int total,
+                               int max_len, int Hq, int Hkv, int d, float scale, void* ws,
+                               size_t ws_bytes, void* stream);
+sep_status sep_attn_bwd_varlen(const void* index_buf, const void* q, const void* k,
+                               const void* v, const void* o, const float* lse,
+                               const void* dout, void* dq, void* dk, void* dv, int B, int total,
+                               int max_len, int Hq, int Hkv, int d, float scale, void* ws,
+                               size_t ws_bytes, void* stream);
+
 /* Size of the fixed device scratch array behind sep_attn_fwd_static. */
 #define SEP_STATIC_SCRATCH_BYTES (64u << 20)
 
@@ -227,7 +287,8 @@ sep_status sep_attn_bwd_hybrid(const void* index_buf, const void* q, const void*
  * Arguments, layouts and the index are those of sep_attn_fwd (bf16 only;
  * d 64 or 128).  The caller still allocates q, k, v, o, lse and the index.
  * Limit: the forward workspace, sep_attn_workspace_bytes(B, Hq, Hkv, L, d,
- * SEP_BF16, 0) (about 4 * B * Hkv * L * d bytes), must not exceed
+ * SEP_BF16, 0) (4 * B * Hkv * L' * d bytes with L' = L rounded up to a
+ * multiple of 128), must not exceed
  * SEP_STATIC_SCRATCH_BYTES; larger shapes return SEP_ERR_TOO_LARGE before
  * any device work.
  *

@@ -34,7 +34,8 @@ EXPORTED = ["sep_index_bytes", "sep_build_index", "sep_index_views",
             "sep_get_device_status", "sep_status_string", "sep_attn_fwd_static",
             "sep_profile_events", "sep_selftest_wait_timeout", "sep_build_index_fixed",
             "sep_cache_prefill_workspace_bytes", "sep_cache_prefill", "sep_attn_fwd_hybrid",
-            "sep_attn_bwd_hybrid"]
+            "sep_attn_bwd_hybrid", "sep_build_index_varlen", "sep_attn_workspace_bytes_varlen",
+            "sep_attn_fwd_varlen", "sep_attn_bwd_varlen"]
 
 
 class SepError(RuntimeError):
@@ -82,6 +83,10 @@ def _load() -> ctypes.CDLL:
         "sep_attn_fwd_hybrid": (I, [P, P, P, P, P, P, I, I, I, I, I, U64, F, P, Z, P]),
         "sep_attn_bwd_hybrid": (I, [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, U64, F, P, Z,
                                     P]),
+        "sep_build_index_varlen": (I, [P, P, I, I, I, P, I, I, I, I, P, Z, P]),
+        "sep_attn_workspace_bytes_varlen": (Z, [I, I, I, I, I, I, I]),
+        "sep_attn_fwd_varlen": (I, [P, P, P, P, P, P, I, I, I, I, I, I, F, P, Z, P]),
+        "sep_attn_bwd_varlen": (I, [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, P, Z, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -183,6 +188,24 @@ def sep_build_index_fixed(B: int, L: int, a: int, n: int, delta: int,
     return index_buf
 
 
+def sep_build_index_varlen(ids: torch.Tensor, cu_seqlens: torch.Tensor, max_len: int,
+                           sep_ids: Sequence[int], a: int, n: int,
+                           block_m: int = SEP_BLOCK_M, index_buf: torch.Tensor | None = None,
+                           stream=None) -> torch.Tensor:
+    """Index of a pack.  ids: int32 [total], cu_seqlens: int32 [B + 1] (both
+    on the GPU); max_len: the longest sequence.  Returns the index buffer;
+    its fields are sep_index_views(buf, B, max_len)."""
+    total = int(ids.shape[0])
+    B = int(cu_seqlens.shape[0]) - 1
+    if index_buf is None:
+        index_buf = _empty_bytes(sep_index_bytes(B, max_len, block_m), cu_seqlens.device)
+    arr, n_ids = _sep_array(sep_ids)
+    _check(_lib.sep_build_index_varlen(_ptr(ids), _ptr(cu_seqlens), B, total, int(max_len), arr,
+                                       n_ids, a, n, block_m, _ptr(index_buf), index_buf.numel(),
+                                       _stream(stream)), "sep_build_index_varlen")
+    return index_buf
+
+
 def sep_index_views(index_buf: torch.Tensor, B: int, L: int,
                     block_m: int = SEP_BLOCK_M) -> dict:
     """Tensor views of the index fields (no copy)."""
@@ -274,6 +297,50 @@ def sep_attn_bwd(index_buf, q, k, v, o, lse, dout, scale: float = 0.0, dq=None, 
                              _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, L, d, dt,
                              float(scale), _ptr(ws), ws.numel(), _stream(stream)),
            "sep_attn_bwd")
+    return dq, dk, dv
+
+
+def sep_attn_workspace_bytes_varlen(B, total, max_len, Hq, Hkv, d, backward: bool) -> int:
+    return int(_lib.sep_attn_workspace_bytes_varlen(B, total, max_len, Hq, Hkv, d,
+                                                    int(backward)))
+
+
+def sep_attn_fwd_varlen(index_buf, q, k, v, B: int, max_len: int, scale: float = 0.0, o=None,
+                        lse=None, ws=None, stream=None):
+    """Forward over a pack: q [Hq, total, d], k/v [Hkv, total, d] bf16 on the
+    GPU, B and max_len as given to sep_build_index_varlen.  Returns (o, lse)
+    with lse [Hq, total]."""
+    Hq, total, d = q.shape
+    Hkv = k.shape[0]
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((Hq, total), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = _empty_bytes(sep_attn_workspace_bytes_varlen(B, total, max_len, Hq, Hkv, d, False),
+                          q.device)
+    _check(_lib.sep_attn_fwd_varlen(_ptr(index_buf), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                    _ptr(lse), B, total, int(max_len), Hq, Hkv, d, float(scale),
+                                    _ptr(ws), ws.numel(), _stream(stream)), "sep_attn_fwd_varlen")
+    return o, lse
+
+
+def sep_attn_bwd_varlen(index_buf, q, k, v, o, lse, dout, B: int, max_len: int,
+                        scale: float = 0.0, dq=None, dk=None, dv=None, ws=None, stream=None):
+    """Backward over a pack (layouts of sep_attn_fwd_varlen).  Returns
+    (dq, dk, dv)."""
+    Hq, total, d = q.shape
+    Hkv = k.shape[0]
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if ws is None:
+        ws = _empty_bytes(sep_attn_workspace_bytes_varlen(B, total, max_len, Hq, Hkv, d, True),
+                          q.device)
+    _check(_lib.sep_attn_bwd_varlen(_ptr(index_buf), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                    _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), B,
+                                    total, int(max_len), Hq, Hkv, d, float(scale), _ptr(ws),
+                                    ws.numel(), _stream(stream)), "sep_attn_bwd_varlen")
     return dq, dk, dv
 
 

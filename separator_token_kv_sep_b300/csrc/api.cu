@@ -17,14 +17,14 @@ namespace sep {
 // error they meet here.
 __device__ int g_device_status;
 
-size_t attn_fwd_tc_workspace(int B, int Hkv, int L, int d);
+size_t attn_fwd_tc_workspace(const Geom& geo, int d);
 int launch_attn_fwd_tc(IndexPtrs idx, const void* q, const void* k, const void* v, void* o,
-                       float* lse, int B, int Hq, int Hkv, int L, int d, float scale,
-                       uint64_t full_groups, void* ws, int* status, void* stream);
-size_t attn_bwd_tc_workspace(int B, int Hq, int Hkv, int L, int d);
+                       float* lse, const Geom& geo, int d, float scale, uint64_t full_groups,
+                       void* ws, int* status, void* stream);
+size_t attn_bwd_tc_workspace(const Geom& geo, int d);
 int launch_attn_bwd_tc(IndexPtrs idx, const void* q, const void* k, const void* v, const void* o,
-                       const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
-                       int Hq, int Hkv, int L, int d, float scale, uint64_t full_groups, void* ws,
+                       const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                       const Geom& geo, int d, float scale, uint64_t full_groups, void* ws,
                        int* status, void* stream);
 
 namespace {
@@ -81,6 +81,15 @@ bool attn_shape_ok(int B, int Hq, int Hkv, int L, int d) {
   return true;
 }
 
+// A pack: B sequences of at most max_len rows in `total` packed rows; row and
+// tile indices of one head plane stay below 2^31.
+bool pack_shape_ok(int B, int total, int max_len, int Hq, int Hkv, int d) {
+  if (B < 1 || total < 0 || max_len < 1 || Hq < 1 || Hkv < 1) return false;
+  if (Hq % Hkv != 0 || (d != 64 && d != 128)) return false;
+  if ((double)total + 128.0 * (B + 1) >= 2.0e9 || (double)B * max_len >= 2.0e9) return false;
+  return true;
+}
+
 }  // namespace
 }  // namespace sep
 
@@ -103,7 +112,29 @@ SEP_API sep_status sep_build_index(const int32_t* ids, int B, int L, const int32
   if (index_bytes < lay.total) return SEP_ERR_WORKSPACE;
   int* st = device_status_ptr();
   if (!st) return SEP_ERR_CUDA;
-  return from_cuda(launch_build_index(ids, B, L, sids, a, n, block_m, 0,
+  return from_cuda(launch_build_index(ids, nullptr, L, B, L, sids, a, n, block_m, 0,
+                                      index_ptrs(index_buf, lay), st, stream));
+}
+
+SEP_API sep_status sep_build_index_varlen(const int32_t* ids, const int32_t* cu_seqlens, int B,
+                                          int total, int max_len, const int32_t* sep_ids,
+                                          int n_sep_ids, int a, int n, int block_m,
+                                          void* index_buf, size_t index_bytes, void* stream) {
+  if (B < 1 || total < 0 || max_len < 1 || a < 0 || n < 1 || !cu_seqlens || !index_buf ||
+      (total > 0 && !ids))
+    return SEP_ERR_INVALID_ARG;
+  if ((double)B * max_len >= 2.0e9 || (double)total + 128.0 * (B + 1) >= 2.0e9)
+    return SEP_ERR_INVALID_ARG;
+  if (!aligned(ids, 4) || !aligned(cu_seqlens, 4) || !aligned(index_buf, 256))
+    return SEP_ERR_INVALID_ARG;
+  if (block_m != SEP_BLOCK_M) return SEP_ERR_UNSUPPORTED;
+  SepIdList sids;
+  if (!fill_sep_ids(sep_ids, n_sep_ids, &sids)) return SEP_ERR_INVALID_ARG;
+  const IndexLayout lay = index_layout(B, max_len, block_m);
+  if (index_bytes < lay.total) return SEP_ERR_WORKSPACE;
+  int* st = device_status_ptr();
+  if (!st) return SEP_ERR_CUDA;
+  return from_cuda(launch_build_index(ids, cu_seqlens, total, B, max_len, sids, a, n, block_m, 0,
                                       index_ptrs(index_buf, lay), st, stream));
 }
 
@@ -118,7 +149,7 @@ SEP_API sep_status sep_build_index_fixed(int B, int L, int a, int n, int delta, 
   if (!st) return SEP_ERR_CUDA;
   SepIdList none;
   memset(&none, 0, sizeof(none));
-  return from_cuda(launch_build_index(nullptr, B, L, none, a, n, block_m, delta,
+  return from_cuda(launch_build_index(nullptr, nullptr, L, B, L, none, a, n, block_m, delta,
                                       index_ptrs(index_buf, lay), st, stream));
 }
 
@@ -139,8 +170,17 @@ SEP_API size_t sep_attn_workspace_bytes(int B, int Hq, int Hkv, int L, int d, se
                                         int backward) {
   if (!attn_shape_ok(B, Hq, Hkv, L, d)) return 0;
   if (dtype == SEP_F32) return backward ? 0 : 256;
-  if (backward) return attn_bwd_tc_workspace(B, Hq, Hkv, L, d);
-  return attn_fwd_tc_workspace(B, Hkv, L, d);
+  const Geom geo = make_geom(B, Hq, Hkv, L, L, 0);
+  if (backward) return attn_bwd_tc_workspace(geo, d);
+  return attn_fwd_tc_workspace(geo, d);
+}
+
+SEP_API size_t sep_attn_workspace_bytes_varlen(int B, int total, int max_len, int Hq, int Hkv,
+                                               int d, int backward) {
+  if (!pack_shape_ok(B, total, max_len, Hq, Hkv, d)) return 0;
+  const Geom geo = make_geom(B, Hq, Hkv, max_len, total, 1);
+  if (backward) return attn_bwd_tc_workspace(geo, d);
+  return attn_fwd_tc_workspace(geo, d);
 }
 
 namespace {
@@ -167,8 +207,9 @@ sep_status attn_fwd(const void* index_buf, const void* q, const void* k, const v
   if (!(scale > 0.f)) scale = 1.0f / sqrtf(static_cast<float>(d));
   if (dtype != SEP_F32 && dtype != SEP_BF16) return SEP_ERR_UNSUPPORTED;
   if (dtype == SEP_F32 && full_groups != 0) return SEP_ERR_UNSUPPORTED;
+  const Geom geo = make_geom(B, Hq, Hkv, L, L, 0);
   if (dtype == SEP_BF16) {
-    const size_t need = attn_fwd_tc_workspace(B, Hkv, L, d);
+    const size_t need = attn_fwd_tc_workspace(geo, d);
     if (!ws || ws_bytes < need) return SEP_ERR_WORKSPACE;
     if (!aligned(ws, 256)) return SEP_ERR_INVALID_ARG;
   }
@@ -181,8 +222,8 @@ sep_status attn_fwd(const void* index_buf, const void* q, const void* k, const v
                                           static_cast<const float*>(v), static_cast<float*>(o),
                                           lse, B, Hq, Hkv, L, d, scale, st, stream));
   }
-  return from_cuda(launch_attn_fwd_tc(idx, q, k, v, o, lse, B, Hq, Hkv, L, d, scale, full_groups,
-                                      ws, st, stream));
+  return from_cuda(launch_attn_fwd_tc(idx, q, k, v, o, lse, geo, d, scale, full_groups, ws, st,
+                                      stream));
 }
 
 sep_status attn_bwd(const void* index_buf, const void* q, const void* k, const void* v,
@@ -201,15 +242,71 @@ sep_status attn_bwd(const void* index_buf, const void* q, const void* k, const v
       !aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
       !aligned(lse, 4) || !aligned(index_buf, 256))
     return SEP_ERR_INVALID_ARG;
-  const size_t need = attn_bwd_tc_workspace(B, Hq, Hkv, L, d);
+  const Geom geo = make_geom(B, Hq, Hkv, L, L, 0);
+  const size_t need = attn_bwd_tc_workspace(geo, d);
   if (!ws || ws_bytes < need) return SEP_ERR_WORKSPACE;
   if (!aligned(ws, 256)) return SEP_ERR_INVALID_ARG;
   if (!(scale > 0.f)) scale = 1.0f / sqrtf(static_cast<float>(d));
   int* st = device_status_ptr();
   if (!st) return SEP_ERR_CUDA;
   const IndexPtrs idx = index_ptrs(const_cast<void*>(index_buf), index_layout(B, L, SEP_BLOCK_M));
-  return from_cuda(launch_attn_bwd_tc(idx, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, L, d,
-                                      scale, full_groups, ws, st, stream));
+  return from_cuda(launch_attn_bwd_tc(idx, q, k, v, o, lse, dout, dq, dk, dv, geo, d, scale,
+                                      full_groups, ws, st, stream));
+}
+
+// Packed batches: the same kernels over the pack's geometry (bf16 only).
+sep_status attn_fwd_pack(const void* index_buf, const void* q, const void* k, const void* v,
+                         void* o, float* lse, int B, int total, int max_len, int Hq, int Hkv,
+                         int d, float scale, void* ws, size_t ws_bytes, void* stream) {
+  if (!index_buf || !q || !k || !v || !o || !lse) return SEP_ERR_INVALID_ARG;
+  if (!pack_shape_ok(B, total, max_len, Hq, Hkv, d)) {
+    if (B >= 1 && total >= 0 && max_len >= 1 && Hq >= 1 && Hkv >= 1 && Hq % Hkv == 0 &&
+        d != 64 && d != 128)
+      return SEP_ERR_UNSUPPORTED;
+    return SEP_ERR_INVALID_ARG;
+  }
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(lse, 4) || !aligned(index_buf, 256))
+    return SEP_ERR_INVALID_ARG;
+  const Geom geo = make_geom(B, Hq, Hkv, max_len, total, 1);
+  if (!ws || ws_bytes < attn_fwd_tc_workspace(geo, d)) return SEP_ERR_WORKSPACE;
+  if (!aligned(ws, 256)) return SEP_ERR_INVALID_ARG;
+  if (total == 0) return SEP_OK;
+  if (!(scale > 0.f)) scale = 1.0f / sqrtf(static_cast<float>(d));
+  int* st = device_status_ptr();
+  if (!st) return SEP_ERR_CUDA;
+  const IndexPtrs idx =
+      index_ptrs(const_cast<void*>(index_buf), index_layout(B, max_len, SEP_BLOCK_M));
+  return from_cuda(launch_attn_fwd_tc(idx, q, k, v, o, lse, geo, d, scale, 0, ws, st, stream));
+}
+
+sep_status attn_bwd_pack(const void* index_buf, const void* q, const void* k, const void* v,
+                         const void* o, const float* lse, const void* dout, void* dq, void* dk,
+                         void* dv, int B, int total, int max_len, int Hq, int Hkv, int d,
+                         float scale, void* ws, size_t ws_bytes, void* stream) {
+  if (!index_buf || !q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv)
+    return SEP_ERR_INVALID_ARG;
+  if (!pack_shape_ok(B, total, max_len, Hq, Hkv, d)) {
+    if (B >= 1 && total >= 0 && max_len >= 1 && Hq >= 1 && Hkv >= 1 && Hq % Hkv == 0 &&
+        d != 64 && d != 128)
+      return SEP_ERR_UNSUPPORTED;
+    return SEP_ERR_INVALID_ARG;
+  }
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
+      !aligned(lse, 4) || !aligned(index_buf, 256))
+    return SEP_ERR_INVALID_ARG;
+  const Geom geo = make_geom(B, Hq, Hkv, max_len, total, 1);
+  if (!ws || ws_bytes < attn_bwd_tc_workspace(geo, d)) return SEP_ERR_WORKSPACE;
+  if (!aligned(ws, 256)) return SEP_ERR_INVALID_ARG;
+  if (total == 0) return SEP_OK;
+  if (!(scale > 0.f)) scale = 1.0f / sqrtf(static_cast<float>(d));
+  int* st = device_status_ptr();
+  if (!st) return SEP_ERR_CUDA;
+  const IndexPtrs idx =
+      index_ptrs(const_cast<void*>(index_buf), index_layout(B, max_len, SEP_BLOCK_M));
+  return from_cuda(launch_attn_bwd_tc(idx, q, k, v, o, lse, dout, dq, dk, dv, geo, d, scale, 0,
+                                      ws, st, stream));
 }
 
 }  // namespace
@@ -247,6 +344,23 @@ SEP_API sep_status sep_attn_bwd_hybrid(const void* index_buf, const void* q, con
                                        size_t ws_bytes, void* stream) {
   return attn_bwd(index_buf, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, L, d, SEP_BF16, scale,
                   full_groups, ws, ws_bytes, stream);
+}
+
+SEP_API sep_status sep_attn_fwd_varlen(const void* index_buf, const void* q, const void* k,
+                                       const void* v, void* o, float* lse, int B, int total,
+                                       int max_len, int Hq, int Hkv, int d, float scale,
+                                       void* ws, size_t ws_bytes, void* stream) {
+  return attn_fwd_pack(index_buf, q, k, v, o, lse, B, total, max_len, Hq, Hkv, d, scale, ws,
+                       ws_bytes, stream);
+}
+
+SEP_API sep_status sep_attn_bwd_varlen(const void* index_buf, const void* q, const void* k,
+                                       const void* v, const void* o, const float* lse,
+                                       const void* dout, void* dq, void* dk, void* dv, int B,
+                                       int total, int max_len, int Hq, int Hkv, int d,
+                                       float scale, void* ws, size_t ws_bytes, void* stream) {
+  return attn_bwd_pack(index_buf, q, k, v, o, lse, dout, dq, dk, dv, B, total, max_len, Hq, Hkv,
+                       d, scale, ws, ws_bytes, stream);
 }
 
 SEP_API sep_status sep_profile_events(void* const* events, int n_events) {

@@ -121,31 +121,47 @@ __device__ __forceinline__ int block_exclusive_scan(int x, int* sh, int* total) 
   return r;
 }
 
-// Builds the schedule (one CTA).  blocks[b][t] = {n_gather, dense_lo, dense_hi, flags}.
-__device__ void build_bwd_schedule(IndexPtrs idx, int B, int Hkv, int L, int T,
-                                   uint64_t full_groups, BwdSchedule* sched, int4* items) {
+// The index header sits at offset 0 of any index buffer: every kernel checks
+// it against the call's geometry before using the fields whose offsets
+// depend on B and L.
+__device__ __forceinline__ bool header_matches(const IndexHeader& h, const Geom& geo) {
+  return h.magic == kIndexMagic && h.B == geo.B && h.L == geo.L && h.block_m == 128 &&
+         h.packed == geo.packed && h.total == geo.R;
+}
+
+// Builds the schedule (one CTA).  blocks[b][t] = {n_gather, dense_lo, dense_hi, flags};
+// sequence b has T_b = ceil(len_b / 128) query tiles (all T in an
+// equal-length batch).  Items of a sequence whose record is unusable are left
+// out (the attention kernels report it).
+__device__ void build_bwd_schedule(IndexPtrs idx, const Geom& geo, uint64_t full_groups,
+                                   BwdSchedule* sched, int4* items) {
   __shared__ int sh[33];
+  const int B = geo.B, Hkv = geo.Hkv, T = geo.T;
   int total = 0;
   // kv groups with full causal attention have no keep items, and every
   // query tile from the key tile on sees their dense key tiles
-  const uint64_t gmask = Hkv >= 64 ? ~0ull : ((1ull << Hkv) - 1ull);
-  const int nsep = Hkv - __popcll(full_groups & gmask);
+  int nsep = 0;
+  for (int g = 0; g < Hkv; ++g) nsep += group_full(full_groups, g) ? 0 : 1;
   // keep items: (b, keep tile kt) -> chunks of query tiles from t_begin(kt)
   for (int base = 0; base < B * T; base += blockDim.x) {
     const int id = base + threadIdx.x;
-    int n = 0, tb = T;
+    int n = 0, tb = T, Tb = 0;
     if (id < B * T) {
       const int b = id / T, kt = id % T;
-      const int count = min(max(idx.keep_count[b], 0), L);
-      if (kt * 128 < count) {
-        const int32_t* blk = idx.blocks + (size_t)b * T * 4;
-        int lo = 0, hi = T;  // first t with n_gather(t) > 128 kt
-        while (lo < hi) {
-          const int mid = (lo + hi) >> 1;
-          if (blk[4 * mid] > kt * 128) hi = mid; else lo = mid + 1;
+      const SeqRec sr = idx.seq[b];
+      if (seq_ok(sr, geo)) {
+        Tb = (sr.len + 127) >> 7;
+        const int count = min(max(idx.keep_count[b], 0), sr.len);
+        if (kt * 128 < count) {
+          const int32_t* blk = idx.blocks + (size_t)b * T * 4;
+          int lo = 0, hi = Tb;  // first t with n_gather(t) > 128 kt
+          while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (blk[4 * mid] > kt * 128) hi = mid; else lo = mid + 1;
+          }
+          tb = lo;
+          n = (Tb - tb + kKeepChunk - 1) / kKeepChunk;
         }
-        tb = lo;
-        n = (T - tb + kKeepChunk - 1) / kKeepChunk;
       }
     }
     int sum;
@@ -153,7 +169,7 @@ __device__ void build_bwd_schedule(IndexPtrs idx, int B, int Hkv, int L, int T,
     if (n > 0) {
       const int b = id / T, kt = id % T;
       for (int cc = 0; cc < n; ++cc) {
-        const int t0 = tb + cc * kKeepChunk, t1 = min(T, t0 + kKeepChunk);
+        const int t0 = tb + cc * kKeepChunk, t1 = min(Tb, t0 + kKeepChunk);
         int gi = 0;
         for (int g = 0; g < Hkv; ++g) {
           if (group_full(full_groups, g)) continue;
@@ -166,23 +182,37 @@ __device__ void build_bwd_schedule(IndexPtrs idx, int B, int Hkv, int L, int T,
     total += sum * nsep;
   }
   const int n_keep = total;
-  // dense items: (b, key tile jt) -> query tiles jt .. (last whose band starts
-  // before the tile ends)
-  for (int id = threadIdx.x; id < B * T; id += blockDim.x) {
-    const int b = id / T, jt = id % T;
-    const int32_t* blk = idx.blocks + (size_t)b * T * 4;
-    int lo = jt, hi = T;  // first t >= jt with dense_lo(t) >= 128 jt + 128
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (blk[4 * mid + 1] < jt * 128 + 128) lo = mid + 1; else hi = mid;
+  // dense items: (b, key tile jt < T_b) -> query tiles jt .. (last whose band
+  // starts before the tile ends)
+  for (int base = 0; base < B * T; base += blockDim.x) {
+    const int id = base + threadIdx.x;
+    int live = 0, Tb = 0;
+    if (id < B * T) {
+      const SeqRec sr = idx.seq[id / T];
+      if (seq_ok(sr, geo)) {
+        Tb = (sr.len + 127) >> 7;
+        live = (id % T) < Tb ? 1 : 0;
+      }
     }
-    for (int g = 0; g < Hkv; ++g)
-      items[n_keep + (size_t)id * Hkv + g] =
-          make_int4(kItemDense, b * Hkv + g, jt * 128,
-                    (jt << 16) | (group_full(full_groups, g) ? T : max(lo, jt + 1)));
+    int sum;
+    const int ex = block_exclusive_scan(live, sh, &sum);
+    if (live) {
+      const int b = id / T, jt = id % T;
+      const int32_t* blk = idx.blocks + (size_t)b * T * 4;
+      int lo = jt, hi = Tb;  // first t >= jt with dense_lo(t) >= 128 jt + 128
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (blk[4 * mid + 1] < jt * 128 + 128) lo = mid + 1; else hi = mid;
+      }
+      for (int g = 0; g < Hkv; ++g)
+        items[total + (size_t)ex * Hkv + g] =
+            make_int4(kItemDense, b * Hkv + g, jt * 128,
+                      (jt << 16) | (group_full(full_groups, g) ? Tb : max(lo, jt + 1)));
+    }
+    total += sum * Hkv;
   }
   if (threadIdx.x == 0) {
-    sched->n_items = n_keep + B * T * Hkv;
+    sched->n_items = total;
     sched->n_keep = n_keep;
   }
 }
@@ -201,30 +231,33 @@ constexpr int kPrepThreads = 256;
 constexpr int kPrepRows = 16;  // rows per stats unit
 
 template <int D>
-__device__ __forceinline__ void prep_stats_unit(const uint4* __restrict__ o,
+__device__ __forceinline__ void prep_stats_unit(IndexPtrs idx, const Geom& geo,
+                                                const uint4* __restrict__ o,
                                                 const uint4* __restrict__ dout,
                                                 const float* __restrict__ lse,
-                                                float2* __restrict__ stats, int B, int Hq, int L,
-                                                size_t unit, int lane) {
+                                                float2* __restrict__ stats, size_t unit,
+                                                int lane) {
   constexpr int U = D / 8;         // 16-byte units per row
   constexpr int RPI = 32 / U;      // rows per warp instruction
   constexpr int IT = kPrepRows / RPI;
-  const int LP = (L + 127) / 128 * 128;
-  const size_t R = (size_t)B * Hq * LP;
-  const size_t row0 = unit * kPrepRows;
+  // unit -> (sequence b, q head h, rows [i0, i0 + kPrepRows) of its T*128)
+  const int TP = geo.T * 128;
+  const size_t r0 = unit * kPrepRows;
+  const int bh = static_cast<int>(r0 / TP), i0 = static_cast<int>(r0 % TP);
+  const int b = bh / geo.Hq, h = bh % geo.Hq;
+  const SeqRec sr = idx.seq[b];
+  if (!seq_ok(sr, geo) || i0 >= (sr.len + 127) / 128 * 128) return;  // no stats rows here
+  const size_t src0 = (size_t)geo.qplane(b, h) * geo.R + sr.row0;
+  float2* dst = stats + ((size_t)h * geo.TT + sr.tile0) * 128;
   const int sub = lane / U, u = lane % U;
   uint4 xo[IT], xd[IT];
-  size_t src[IT];
   bool live[IT];
 #pragma unroll
   for (int it = 0; it < IT; ++it) {
-    const size_t row = row0 + it * RPI + sub;
-    const size_t plane = row / LP;
-    const int i = static_cast<int>(row % LP);
-    live[it] = row < R && i < L;
-    src[it] = plane * L + i;
-    xo[it] = live[it] ? o[src[it] * U + u] : make_uint4(0, 0, 0, 0);
-    xd[it] = live[it] ? dout[src[it] * U + u] : make_uint4(0, 0, 0, 0);
+    const int i = i0 + it * RPI + sub;
+    live[it] = i < sr.len;
+    xo[it] = live[it] ? o[(src0 + i) * U + u] : make_uint4(0, 0, 0, 0);
+    xd[it] = live[it] ? dout[(src0 + i) * U + u] : make_uint4(0, 0, 0, 0);
   }
 #pragma unroll
   for (int it = 0; it < IT; ++it) {
@@ -239,39 +272,38 @@ __device__ __forceinline__ void prep_stats_unit(const uint4* __restrict__ o,
     }
 #pragma unroll
     for (int off = U / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    const size_t row = row0 + it * RPI + sub;
-    if (u == 0 && row < R)
-      stats[row] = live[it] ? make_float2(-lse[src[it]] * kLog2e, -acc) : make_float2(0.f, 0.f);
+    const int i = i0 + it * RPI + sub;
+    if (u == 0)
+      dst[i] = live[it] ? make_float2(-lse[src0 + i] * kLog2e, -acc) : make_float2(0.f, 0.f);
   }
 }
 
 template <int D>
 __global__ void __launch_bounds__(kPrepThreads)
-    bwd_prep_kernel(IndexPtrs idx, const uint4* __restrict__ k, const uint4* __restrict__ v,
-                    uint4* __restrict__ kk, uint4* __restrict__ vk, const uint4* __restrict__ o,
-                    const uint4* __restrict__ dout, const float* __restrict__ lse,
-                    float2* __restrict__ stats, float4* __restrict__ dk_keep,
-                    float4* __restrict__ dv_keep, int B, int Hq, int Hkv, int L,
+    bwd_prep_kernel(IndexPtrs idx, Geom geo, const uint4* __restrict__ k,
+                    const uint4* __restrict__ v, uint4* __restrict__ kk, uint4* __restrict__ vk,
+                    const uint4* __restrict__ o, const uint4* __restrict__ dout,
+                    const float* __restrict__ lse, float2* __restrict__ stats,
+                    float4* __restrict__ dk_keep, float4* __restrict__ dv_keep,
                     uint64_t full_groups, BwdSchedule* __restrict__ sched,
                     int4* __restrict__ items) {
   const IndexHeader hdr = *idx.header;
-  if (hdr.magic != kIndexMagic || hdr.B != B || hdr.L != L) return;
+  if (!header_matches(hdr, geo)) return;
   if (blockIdx.x == 0) {
-    build_bwd_schedule(idx, B, Hkv, L, (L + 127) / 128, full_groups, sched, items);
+    build_bwd_schedule(idx, geo, full_groups, sched, items);
     return;
   }
   constexpr int WPB = kPrepThreads / 32;
   const int lane = threadIdx.x & 31;
   const size_t w0 = (size_t)(blockIdx.x - 1) * WPB + (threadIdx.x >> 5);
   const size_t nw = (size_t)(gridDim.x - 1) * WPB;
-  const size_t gunits = static_cast<size_t>(keep_units(B, Hkv, L));
-  const size_t sunits = ((size_t)B * Hq * ((L + 127) / 128 * 128)) / kPrepRows;
+  const size_t gunits = static_cast<size_t>(keep_units(geo.B, geo.Hkv, geo.L));
+  const size_t sunits = (size_t)geo.B * geo.Hq * geo.T * 128 / kPrepRows;
   for (size_t u = w0; u < gunits + sunits; u += nw) {
     if (u < gunits)
-      gather_keep_unit<D>(idx, k, v, kk, vk, dk_keep, dv_keep, B, Hkv, L, static_cast<int>(u),
-                          lane);
+      gather_keep_unit<D>(idx, geo, k, v, kk, vk, dk_keep, dv_keep, static_cast<int>(u), lane);
     else
-      prep_stats_unit<D>(o, dout, lse, stats, B, Hq, L, u - gunits, lane);
+      prep_stats_unit<D>(idx, geo, o, dout, lse, stats, u - gunits, lane);
   }
 }
 
@@ -309,9 +341,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const BwdSchedule* __restrict__ sched, const int4* __restrict__ items,
                       const float2* __restrict__ stats,
                       float* __restrict__ dk_keep, float* __restrict__ dv_keep,
-                      __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int B,
-                      int Hq, int Hkv, int L, float scale, float scale_log2,
-                      uint64_t full_groups, int* status) {
+                      __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, Geom geo,
+                      float scale, float scale_log2, uint64_t full_groups, int* status) {
   using C = KvCfg<D>;
   constexpr int KVB = C::KVB, NST = C::NST, ACB = C::ACB;
   extern __shared__ uint8_t smem_raw[];
@@ -323,16 +354,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint32_t tmem_slot;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int T = (L + 127) >> 7;
+  const int T = geo.T, Hq = geo.Hq, Hkv = geo.Hkv, L = geo.L;
   const int G = Hq / Hkv;
 
   const IndexHeader hdr = *idx.header;
-  if (hdr.magic != kIndexMagic || hdr.B != B || hdr.L != L || hdr.block_m != 128) {
+  if (!header_matches(hdr, geo)) {
     if (threadIdx.x == 0) report(status, SEP_ERR_DEVICE_BOUNDS);
     return;
   }
   const int n_items = sched->n_items;
-  if (n_items < 0 || (size_t)n_items > bwd_max_items(B, Hkv, T)) {
+  if (n_items < 0 || (size_t)n_items > bwd_max_items(geo.B, Hkv, T)) {
     if (threadIdx.x == 0) report(status, SEP_ERR_DEVICE_BOUNDS);
     return;
   }
@@ -374,9 +405,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
-  // item decoding shared by every role
+  // item decoding shared by every role; the schedule holds items of usable
+  // sequences only, whose records {len, row0, tile0} are read here
   struct Item {
     int kind, b, g, row0, t0, nt;
+    int len, srow0, tile0;
   };
   auto item_at = [&](int i, int k) -> Item {  // item i, the k-th of this CTA
     const int4 it = k < kCtaItems ? s_items[k] : items[i];
@@ -387,6 +420,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     r.row0 = it.z;
     r.t0 = it.w >> 16;
     r.nt = (it.w & 0xffff) - r.t0;
+    const SeqRec sr = idx.seq[r.b];
+    r.len = sr.len;
+    r.srow0 = sr.row0;
+    r.tile0 = sr.tile0;
     return r;
   };
 
@@ -403,15 +440,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         const bool keep = it.kind == kItemKeep;
-        const int plane_kv = it.b * Hkv + it.g;
+        // keep tiles: the sequence's gathered rows in plane g of the
+        // workspace; dense tiles: rows of the sequence in its kv plane
+        const int plane = keep ? it.g : geo.kvplane(it.b, it.g);
+        const int krow = keep ? it.tile0 * 128 + it.row0 : it.srow0 + it.row0;
         uint8_t* sK = smem + C::OFF_KV + kb * 2 * C::TILE;
         uint8_t* sV = sK + C::TILE;
         mbar_arrive_expect_tx(&kv_full[kb], 2 * C::TILE);
         for (int c = 0; c < C::DCH; ++c) {
-          tma_load_3d(sK + c * kChunk, keep ? &tm_kk : &tm_k, &kv_full[kb], 64 * c, it.row0,
-                      plane_kv);
-          tma_load_3d(sV + c * kChunk, keep ? &tm_vk : &tm_v, &kv_full[kb], 64 * c, it.row0,
-                      plane_kv);
+          tma_load_3d(sK + c * kChunk, keep ? &tm_kk : &tm_k, &kv_full[kb], 64 * c, krow, plane);
+          tma_load_3d(sV + c * kChunk, keep ? &tm_vk : &tm_v, &kv_full[kb], 64 * c, krow, plane);
         }
         kv_issued = k + 1;
         const int nU = G * it.nt;
@@ -423,15 +461,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ++ug;  // counts issued Q/dO tiles
           const int h = it.g * G + u / it.nt, t = it.t0 + u % it.nt;
-          const int plane_q = it.b * Hq + h;
+          const int plane_q = geo.qplane(it.b, h);
           mbar_arrive_expect_tx(&qd_full[st], 2 * C::TILE + 128 * 8);
-          bulk_g2s(smem + C::OFF_STAT + st * 1024, stats + ((size_t)plane_q * T + t) * 128, 1024,
-                   &qd_full[st]);
+          bulk_g2s(smem + C::OFF_STAT + st * 1024,
+                   stats + ((size_t)h * geo.TT + it.tile0 + t) * 128, 1024, &qd_full[st]);
           for (int c = 0; c < C::DCH; ++c) {
             tma_load_3d(smem + C::OFF_Q + st * C::TILE + c * kChunk, &tm_q, &qd_full[st],
-                        64 * c, t * 128, plane_q);
+                        64 * c, it.srow0 + t * 128, plane_q);
             tma_load_3d(smem + C::OFF_DO + st * C::TILE + c * kChunk, &tm_do, &qd_full[st],
-                        64 * c, t * 128, plane_q);
+                        64 * c, it.srow0 + t * 128, plane_q);
           }
         }
       }
@@ -583,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // accumulators of item k -> global memory (half 0 dV, half 1 dK)
     struct Epi {
       int k;
-      long long rm;  // 4 * row + mode: row of [B*Hkv*L]; mode 1 keep accumulator, 2 output
+      long long rm;  // 4 * row + mode: mode 1 keep-accumulator row, mode 2 output row
     };
     const float osc = half ? scale : 1.f;
     auto epilogue = [&](const Epi& e) -> bool {
@@ -629,11 +667,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x, ++k) {
       const Item it = item_at(i, k);
       const bool keep = it.kind == kItemKeep;
-      const int count = min(max(idx.keep_count[it.b], 0), L);
+      const int len = it.len;
+      const int count = min(max(idx.keep_count[it.b], 0), len);
       const int32_t* blocks = idx.blocks + (size_t)it.b * T * 4;
       const int j = it.row0 + r;  // KEEP: keep index; DENSE: key position
       // a dense row's keep bit and keep prefix, loaded together
-      const bool dense_row = !keep && j < L;
+      const bool dense_row = !keep && j < len;
       const uint32_t kbw = dense_row ? idx.keep_bits[(size_t)it.b * hdr.nwords + (j >> 5)] : 0u;
       const int kpre = dense_row ? idx.keep_prefix[(size_t)it.b * (L + 1) + j] : 0;
       const bool keep_j = (kbw >> (j & 31)) & 1u;
@@ -643,18 +682,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       Epi e;
       e.k = k;
       {
-        const bool to_acc = keep ? (j < count) : (j < L && keep_j);
-        const bool to_out = !keep && j < L && !keep_j;
+        const bool to_acc = keep ? (j < count) : (j < len && keep_j);
+        const bool to_out = !keep && j < len && !keep_j;
         const int kidx = keep ? j : (keep_j ? kpre : 0);
-        const long long plane = (long long)it.b * Hkv + it.g;
-        e.rm = to_acc ? (((plane * L + kidx) << 2) | 1) : to_out ? (((plane * L + j) << 2) | 2) : 0;
+        const long long acc_row = ((long long)it.g * geo.TT + it.tile0) * 128 + kidx;
+        const long long out_row = (long long)geo.kvplane(it.b, it.g) * geo.R + it.srow0 + j;
+        e.rm = to_acc ? ((acc_row << 2) | 1) : to_out ? ((out_row << 2) | 2) : 0;
       }
       const int nU = G * it.nt;
-      // a kv group with full causal attention: records for a window n >= L
+      // a kv group with full causal attention: records for a window n >= len
       const bool full = group_full(full_groups, it.g);
-      const int n_w = full ? L : n_win;
+      const int n_w = full ? len : n_win;
       auto record = [&](int t2) {
-        return full ? full_block_record(t2, L) : *reinterpret_cast<const int4*>(blocks + 4 * t2);
+        return full ? full_block_record(t2, len) : *reinterpret_cast<const int4*>(blocks + 4 * t2);
       };
       int4 blk_next = record(it.t0);
       for (int u = 0; u < nU; ++u) {
@@ -666,11 +706,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // visible query columns of this row among the half's 64, as 2 words
         uint32_t vm[2];
         {
-          const int c_end = min(128, L - i0);  // query rows past L are padding
+          const int c_end = min(128, len - i0);  // query rows past len are padding
           int c_lo = 0, c_hi = 0;
           if (keep) {
             if (j < blk.x && j < count) c_hi = c_end;  // gathered by this query tile
-          } else if (j >= blk.y && j < blk.z && j < L) {
+          } else if (j >= blk.y && j < blk.z && j < len) {
             c_lo = j - i0;
             c_hi = keep_j ? c_end : min(c_end, j + n_w - i0);
           }
@@ -750,13 +790,13 @@ template <int D>
 __global__ void __launch_bounds__(256)
     bwd_keep_scatter_kernel(IndexPtrs idx, const float4* __restrict__ dk_keep,
                             const float4* __restrict__ dv_keep, __nv_bfloat16* __restrict__ dk,
-                            __nv_bfloat16* __restrict__ dv, int B, int Hkv, int L, float scale) {
+                            __nv_bfloat16* __restrict__ dv, Geom geo, float scale) {
   const IndexHeader hdr = *idx.header;
-  if (hdr.magic != kIndexMagic || hdr.B != B || hdr.L != L) return;
-  const int units = keep_units(B, Hkv, L);
+  if (!header_matches(hdr, geo)) return;
+  const int units = keep_units(geo.B, geo.Hkv, geo.L);
   const int lane = threadIdx.x & 31;
   for (int u = blockIdx.x * 8 + (threadIdx.x >> 5); u < units; u += gridDim.x * 8)
-    scatter_keep_unit<D>(idx, dk_keep, dv_keep, dk, dv, B, Hkv, L, scale, u, lane);
+    scatter_keep_unit<D>(idx, geo, dk_keep, dv_keep, dk, dv, scale, u, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -776,9 +816,10 @@ struct DqCfg {
   static constexpr int SMEM = OFF_DS + 2 * kChunk + 1024;
   static constexpr int TM_S = 0, TM_DP = 128, TM_DQ = 256;  // dQ buffer b at +bD
   static constexpr int TM_COLS = 512;
-  // block records of the CTA's first ITEMS items, in static shared memory
+  // block and sequence records of the CTA's first ITEMS items, in static
+  // shared memory
   static constexpr int ITEMS = D == 64 ? 128 : 48;
-  static_assert(SMEM + 16 * ITEMS + 256 <= 227 * 1024, "shared memory");
+  static_assert(SMEM + 32 * ITEMS + 256 <= 227 * 1024, "shared memory");
   static_assert(TM_DQ + 2 * D <= TM_COLS, "tensor memory");
 };
 
@@ -791,7 +832,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tm_kk,
                       const __grid_constant__ CUtensorMap tm_vk, IndexPtrs idx,
                       const float2* __restrict__ stats,
-                      __nv_bfloat16* __restrict__ dq, int B, int Hq, int Hkv, int L, float scale,
+                      __nv_bfloat16* __restrict__ dq, Geom geo, float scale,
                       float scale_log2, uint64_t full_groups, int* status) {
   using C = DqCfg<D>;
   constexpr int QB = C::QB, NST = C::NST;
@@ -804,11 +845,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint32_t tmem_slot;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int T = (L + 127) >> 7;
+  const int T = geo.T, B = geo.B, Hq = geo.Hq, Hkv = geo.Hkv;
   const int n_items = B * Hq * T;
 
   const IndexHeader hdr = *idx.header;
-  if (hdr.magic != kIndexMagic || hdr.B != B || hdr.L != L || hdr.block_m != 128) {
+  if (!header_matches(hdr, geo)) {
     if (threadIdx.x == 0) report(status, SEP_ERR_DEVICE_BOUNDS);
     return;
   }
@@ -834,15 +875,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&mma_final, 1);
     fence_mbar_init();
   }
-  // block records of this CTA's items (i = blockIdx.x + k * gridDim.x),
-  // read once; items past C::ITEMS read theirs from global memory
-  __shared__ int4 s_blk[C::ITEMS];
+  // block and sequence records of this CTA's items (i = blockIdx.x + x *
+  // gridDim.x), read once; items past C::ITEMS read theirs from global memory
+  __shared__ int4 s_blk[C::ITEMS], s_seq[C::ITEMS];
   for (int x = threadIdx.x; x < C::ITEMS; x += blockDim.x) {
     const int i = static_cast<int>(blockIdx.x) + x * static_cast<int>(gridDim.x);
     if (i < n_items) {
       const int bh = i % (B * Hq);
       s_blk[x] = *reinterpret_cast<const int4*>(idx.blocks +
                                                 ((size_t)(bh / Hq) * T + (T - 1 - i / (B * Hq))) * 4);
+      s_seq[x] = *reinterpret_cast<const int4*>(idx.seq + bh / Hq);
     }
   }
   if (warp == 1) {
@@ -854,27 +896,41 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
+  // Items are (sequence, q head, query tile), longest tiles first.  Tiles
+  // past the end of their sequence (a pack's shorter sequences) are empty and
+  // skipped by every role; only live items advance the buffer counters.
   struct Item {
     int b, h, g, t, n_gather, lo, hi, nG, nT;
-    bool ok, full;
+    int len, srow0, tile0;
+    bool ok, full, empty;
   };
-  auto item_at = [&](int i, int k) -> Item {  // item i, the k-th of this CTA
+  auto item_at = [&](int i, int x) -> Item {  // item i, the x-th of this CTA
     Item r;
     r.t = T - 1 - i / (B * Hq);
     const int bh = i % (B * Hq);
     r.b = bh / Hq;
     r.h = bh % Hq;
     r.g = r.h / (Hq / Hkv);
-    r.full = group_full(full_groups, r.g);  // full causal attention: records for n >= L
-    const int4 blk = r.full ? full_block_record(r.t, L)
-                     : k < C::ITEMS
-                         ? s_blk[k]
+    const int4 sq = x < C::ITEMS ? s_seq[x] : *reinterpret_cast<const int4*>(idx.seq + r.b);
+    SeqRec sr;
+    sr.len = sq.x; sr.row0 = sq.y; sr.tile0 = sq.z; sr.pad = 0;
+    r.len = sr.len;
+    r.srow0 = sr.row0;
+    r.tile0 = sr.tile0;
+    const bool sok = seq_ok(sr, geo);
+    r.empty = sok && r.t * 128 >= sr.len;
+    r.full = group_full(full_groups, r.g);  // full causal attention: records for n >= len
+    const int4 blk = r.full ? full_block_record(r.t, sr.len)
+                     : x < C::ITEMS
+                         ? s_blk[x]
                          : *reinterpret_cast<const int4*>(idx.blocks + ((size_t)r.b * T + r.t) * 4);
     r.n_gather = blk.x;
     r.lo = blk.y;
     r.hi = blk.z;
     const int q0 = r.t * 128;
-    r.ok = !(blk.x < 0 || blk.x > blk.y || blk.y < 0 || blk.y > q0 || blk.z <= q0 || blk.z > L);
+    r.ok = sok && !r.empty &&
+           !(blk.x < 0 || blk.x > blk.y || blk.y < 0 || blk.y > q0 || blk.z <= q0 ||
+             blk.z > sr.len);
     r.nG = r.ok ? (blk.x + 127) >> 7 : 0;
     r.nT = r.ok ? r.nG + ((blk.z - blk.y + 127) >> 7) : 0;
     return r;
@@ -883,10 +939,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      int k = 0, ug = 0, qd_issued = 0;
+      int k = 0, ug = 0, qd_issued = 0;  // k: live items so far
       bool ok = true;
-      for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x, ++k) {
-        const Item it = item_at(i, k);
+      for (int i = blockIdx.x, ix = 0; ok && i < n_items; i += gridDim.x, ++ix) {
+        const Item it = item_at(i, ix);
+        if (it.empty) continue;
         if (!it.ok) {
           report(status, SEP_ERR_DEVICE_BOUNDS);
           ok = false;
@@ -897,13 +954,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        const int plane_q = it.b * Hq + it.h, plane_kv = it.b * Hkv + it.g;
+        const int plane_q = geo.qplane(it.b, it.h), plane_kv = geo.kvplane(it.b, it.g);
+        const int qrow = it.srow0 + it.t * 128;
         uint8_t* sQ = smem + C::OFF_QD + qb * 2 * C::TILE;
         mbar_arrive_expect_tx(&qd_full[qb], 2 * C::TILE);
         for (int c = 0; c < C::DCH; ++c) {
-          tma_load_3d(sQ + c * kChunk, &tm_q, &qd_full[qb], 64 * c, it.t * 128, plane_q);
-          tma_load_3d(sQ + C::TILE + c * kChunk, &tm_do, &qd_full[qb], 64 * c, it.t * 128,
-                      plane_q);
+          tma_load_3d(sQ + c * kChunk, &tm_q, &qd_full[qb], 64 * c, qrow, plane_q);
+          tma_load_3d(sQ + C::TILE + c * kChunk, &tm_do, &qd_full[qb], 64 * c, qrow, plane_q);
         }
         qd_issued = k + 1;
         for (int u = 0; u < it.nT; ++u) {
@@ -914,15 +971,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ++ug;  // counts issued K/V tiles
           const bool gat = u < it.nG;
-          const int row = gat ? 128 * u : it.lo + 128 * (u - it.nG);
+          // gathered tiles: the sequence's keep rows in plane g of the
+          // workspace; band tiles: rows of the sequence in its kv plane
+          const int row = gat ? 128 * (it.tile0 + u) : it.srow0 + it.lo + 128 * (u - it.nG);
+          const int plane = gat ? it.g : plane_kv;
           mbar_arrive_expect_tx(&kv_full[st], 2 * C::TILE);
           for (int c = 0; c < C::DCH; ++c) {
             tma_load_3d(smem + C::OFF_K + st * C::TILE + c * kChunk, gat ? &tm_kk : &tm_k,
-                        &kv_full[st], 64 * c, row, plane_kv);
+                        &kv_full[st], 64 * c, row, plane);
             tma_load_3d(smem + C::OFF_V + st * C::TILE + c * kChunk, gat ? &tm_vk : &tm_v,
-                        &kv_full[st], 64 * c, row, plane_kv);
+                        &kv_full[st], 64 * c, row, plane);
           }
         }
+        ++k;
       }
       if (!ok) {
         // after a failed wait, let the copies still in flight land
@@ -941,10 +1002,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_acc = idesc_bf16_f32(128, D, false, true);
       const uint32_t k_base = smem_u32(smem + C::OFF_K), v_base = smem_u32(smem + C::OFF_V),
                      ds_base = smem_u32(smem + C::OFF_DS);
-      int k = 0, ug = 0;
+      int k = 0, ug = 0;  // k: live items so far
       bool ok = true;
-      for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x, ++k) {
-        const Item it = item_at(i, k);
+      for (int i = blockIdx.x, ix = 0; ok && i < n_items; i += gridDim.x, ++ix) {
+        const Item it = item_at(i, ix);
+        if (it.empty) continue;
         if (!it.ok) break;
         const int qb = k % QB, ab = k & 1;
         const uint32_t q_base = smem_u32(smem + C::OFF_QD + qb * 2 * C::TILE);
@@ -1019,6 +1081,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         if (leader) umma_commit(&acc_full[ab]);
         ug += it.nT;
+        ++k;
       }
       // every MMA issued by the leader completes before TMEM is released
       if (leader) umma_commit(&mma_final);
@@ -1036,16 +1099,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t* kb_all = idx.keep_bits;
     const int nwords = hdr.nwords;
     uint8_t* sDS = smem + C::OFF_DS;
-    int k = 0, ug = 0;
+    int k = 0, ug = 0;  // k: live items so far
     bool ok = true;
-    for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x, ++k) {
-      const Item it = item_at(i, k);
+    for (int i = blockIdx.x, ix = 0; ok && i < n_items; i += gridDim.x, ++ix) {
+      const Item it = item_at(i, ix);
+      if (it.empty) continue;
       if (!it.ok) break;
       const int ab = k & 1;
       const int i_row = it.t * 128 + r;
-      const bool row_live = i_row < L;
+      const bool row_live = i_row < it.len;
       // (-LSE log2, -Delta) of this row (zero for padding rows)
-      const float2 st2 = stats[((size_t)it.b * Hq + it.h) * T * 128 + it.t * 128 + r];
+      const float2 st2 = stats[((size_t)it.h * geo.TT + it.tile0 + it.t) * 128 + r];
       const uint32_t* kbits = kb_all + (size_t)it.b * nwords;
       for (int u = 0; u < it.nT; ++u) {
         const int ugl = ug + u;
@@ -1059,7 +1123,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           const int jt = it.lo + 128 * (u - it.nG) + 64 * half;  // first key of this half
           const int n_causal = min(64, max(0, i_row - jt + 1));
-          const int c_win = i_row - (it.full ? L : n_win) + 1 - jt;
+          const int c_win = i_row - (it.full ? it.len : n_win) + 1 - jt;
           const int wj = jt >> 5, sh = jt & 31;
           uint32_t kw[3];
 #pragma unroll
@@ -1124,7 +1188,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const uint32_t tm_dq = tmem + C::TM_DQ + ab * D;
-      __nv_bfloat16* qrow = dq + (((size_t)it.b * Hq + it.h) * L + (row_live ? i_row : 0)) * D;
+      __nv_bfloat16* qrow =
+          dq + ((size_t)geo.qplane(it.b, it.h) * geo.R + it.srow0 + (row_live ? i_row : 0)) * D;
 #pragma unroll
       for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
         uint32_t qb2[32];
@@ -1147,6 +1212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(&acc_empty[ab]);
+      ++k;
     }
   }
 
@@ -1159,60 +1225,62 @@ __global__ void __launch_bounds__(kThreads, 1)
 struct BwdWs {
   uint8_t *kk, *vk;
   float *dk_keep, *dv_keep;
-  float2* stats;  // [B*Hq][ceil(L/128)*128] (-LSE in log2 units, -Delta)
+  float2* stats;  // [Hq][TT * 128] (-LSE in log2 units, -Delta)
   BwdSchedule* sched;
   int4* items;
   size_t total;
 };
 
-BwdWs bwd_ws(void* base, int B, int Hq, int Hkv, int L, int d) {
+BwdWs bwd_ws(void* base, const Geom& geo, int d) {
   BwdWs w;
   uint8_t* p = static_cast<uint8_t*>(base);
   size_t off = 0;
-  const size_t kv_bf16 = align_up((size_t)B * Hkv * L * d * 2, 256);
-  const size_t kv_f32 = align_up((size_t)B * Hkv * L * d * 4, 256);
+  const size_t rows = (size_t)geo.TT * 128;  // rows of one head plane of the tile space
+  const size_t kv_bf16 = align_up((size_t)geo.Hkv * rows * d * 2, 256);
+  const size_t kv_f32 = align_up((size_t)geo.Hkv * rows * d * 4, 256);
   w.kk = p + off; off += kv_bf16;
   w.vk = p + off; off += kv_bf16;
   w.dk_keep = reinterpret_cast<float*>(p + off); off += kv_f32;
   w.dv_keep = reinterpret_cast<float*>(p + off); off += kv_f32;
   w.stats = reinterpret_cast<float2*>(p + off);
-  off += align_up((size_t)B * Hq * ((L + 127) / 128 * 128) * 8, 256);
+  off += align_up((size_t)geo.Hq * rows * 8, 256);
   w.sched = reinterpret_cast<BwdSchedule*>(p + off); off += 256;
   w.items = reinterpret_cast<int4*>(p + off);
-  off += align_up(sizeof(int4) * bwd_max_items(B, Hkv, (L + 127) / 128), 256);
+  off += align_up(sizeof(int4) * bwd_max_items(geo.B, geo.Hkv, geo.T), 256);
   w.total = off;
   return w;
 }
 
 template <int D>
 int launch_bwd_impl(IndexPtrs idx, const void* q, const void* k, const void* v, const void* o,
-                    const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
-                    int Hq, int Hkv, int L, float scale, uint64_t full_groups, void* ws,
-                    int* status, cudaStream_t s) {
-  const BwdWs w = bwd_ws(ws, B, Hq, Hkv, L, D);
-  const int T = (L + 127) / 128;
+                    const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                    const Geom& geo, float scale, uint64_t full_groups, void* ws, int* status,
+                    cudaStream_t s) {
+  const BwdWs w = bwd_ws(ws, geo, D);
   const int sms = num_sms();
   profile_mark(0, s);
   {
     // one CTA for the schedule, then a few CTAs per SM for the strided units
-    const size_t units = static_cast<size_t>(keep_units(B, Hkv, L)) +
-                         (size_t)B * Hq * T * 128 / kPrepRows;
+    const size_t units = static_cast<size_t>(keep_units(geo.B, geo.Hkv, geo.L)) +
+                         (size_t)geo.B * geo.Hq * geo.T * 128 / kPrepRows;
     const size_t want = (units + kPrepThreads / 32 - 1) / (kPrepThreads / 32);
     const int ctas = static_cast<int>(want < (size_t)8 * sms ? want : (size_t)8 * sms);
     bwd_prep_kernel<D><<<ctas + 1, kPrepThreads, 0, s>>>(
-        idx, static_cast<const uint4*>(k), static_cast<const uint4*>(v),
+        idx, geo, static_cast<const uint4*>(k), static_cast<const uint4*>(v),
         reinterpret_cast<uint4*>(w.kk), reinterpret_cast<uint4*>(w.vk),
         static_cast<const uint4*>(o), static_cast<const uint4*>(dout), lse, w.stats,
-        reinterpret_cast<float4*>(w.dk_keep), reinterpret_cast<float4*>(w.dv_keep), B, Hq, Hkv,
-        L, full_groups, w.sched, w.items);
+        reinterpret_cast<float4*>(w.dk_keep), reinterpret_cast<float4*>(w.dv_keep), full_groups,
+        w.sched, w.items);
   }
+  const uint64_t pq = geo.packed ? geo.Hq : (uint64_t)geo.B * geo.Hq;
+  const uint64_t pkv = geo.packed ? geo.Hkv : (uint64_t)geo.B * geo.Hkv;
+  const uint64_t rk = (uint64_t)geo.TT * 128;
   CUtensorMap mq, mdo, mk, mv, mkk, mvk;
-  if (!make_bf16_map(&mq, q, (uint64_t)B * Hq, L, D, 128) ||
-      !make_bf16_map(&mdo, dout, (uint64_t)B * Hq, L, D, 128) ||
-      !make_bf16_map(&mk, k, (uint64_t)B * Hkv, L, D, 128) ||
-      !make_bf16_map(&mv, v, (uint64_t)B * Hkv, L, D, 128) ||
-      !make_bf16_map(&mkk, w.kk, (uint64_t)B * Hkv, L, D, 128) ||
-      !make_bf16_map(&mvk, w.vk, (uint64_t)B * Hkv, L, D, 128))
+  if (!make_bf16_map(&mq, q, pq, geo.R, D, 128) ||
+      !make_bf16_map(&mdo, dout, pq, geo.R, D, 128) ||
+      !make_bf16_map(&mk, k, pkv, geo.R, D, 128) || !make_bf16_map(&mv, v, pkv, geo.R, D, 128) ||
+      !make_bf16_map(&mkk, w.kk, geo.Hkv, rk, D, 128) ||
+      !make_bf16_map(&mvk, w.vk, geo.Hkv, rk, D, 128))
     return static_cast<int>(cudaErrorInvalidValue);
   const float scale_log2 = scale * kLog2e;
   using KC = KvCfg<D>;
@@ -1227,17 +1295,17 @@ int launch_bwd_impl(IndexPtrs idx, const void* q, const void* k, const void* v, 
   __nv_bfloat16* dvb = static_cast<__nv_bfloat16*>(dv);
   profile_mark(1, s);
   kv_k<<<sms, kThreads, KC::SMEM, s>>>(mkk, mvk, mk, mv, mq, mdo, idx, w.sched, w.items,
-                                       w.stats, w.dk_keep, w.dv_keep, dkb, dvb, B, Hq, Hkv, L,
-                                       scale, scale_log2, full_groups, status);
+                                       w.stats, w.dk_keep, w.dv_keep, dkb, dvb, geo, scale,
+                                       scale_log2, full_groups, status);
   profile_mark(2, s);
-  const int dq_items = B * Hq * T;
+  const int dq_items = geo.B * geo.Hq * geo.T;
   dq_k<<<dq_items < sms ? dq_items : sms, kThreads, QC::SMEM, s>>>(
-      mq, mdo, mk, mv, mkk, mvk, idx, w.stats, static_cast<__nv_bfloat16*>(dq), B, Hq, Hkv,
-      L, scale, scale_log2, full_groups, status);
+      mq, mdo, mk, mv, mkk, mvk, idx, w.stats, static_cast<__nv_bfloat16*>(dq), geo, scale,
+      scale_log2, full_groups, status);
   profile_mark(3, s);
-  bwd_keep_scatter_kernel<D><<<keep_pass_ctas(keep_units(B, Hkv, L), sms), 256, 0, s>>>(
+  bwd_keep_scatter_kernel<D><<<keep_pass_ctas(keep_units(geo.B, geo.Hkv, geo.L), sms), 256, 0, s>>>(
       idx, reinterpret_cast<const float4*>(w.dk_keep), reinterpret_cast<const float4*>(w.dv_keep),
-      dkb, dvb, B, Hkv, L, scale);
+      dkb, dvb, geo, scale);
   const cudaError_t err = cudaGetLastError();
   profile_mark(4, s);
   return static_cast<int>(err);
@@ -1245,20 +1313,18 @@ int launch_bwd_impl(IndexPtrs idx, const void* q, const void* k, const void* v, 
 
 }  // namespace
 
-size_t attn_bwd_tc_workspace(int B, int Hq, int Hkv, int L, int d) {
-  return bwd_ws(nullptr, B, Hq, Hkv, L, d).total;
-}
+size_t attn_bwd_tc_workspace(const Geom& geo, int d) { return bwd_ws(nullptr, geo, d).total; }
 
 int launch_attn_bwd_tc(IndexPtrs idx, const void* q, const void* k, const void* v, const void* o,
-                       const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
-                       int Hq, int Hkv, int L, int d, float scale, uint64_t full_groups, void* ws,
+                       const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                       const Geom& geo, int d, float scale, uint64_t full_groups, void* ws,
                        int* status, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (d == 64)
-    return launch_bwd_impl<64>(idx, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, L, scale,
-                               full_groups, ws, status, s);
-  return launch_bwd_impl<128>(idx, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, L, scale,
-                              full_groups, ws, status, s);
+    return launch_bwd_impl<64>(idx, q, k, v, o, lse, dout, dq, dk, dv, geo, scale, full_groups,
+                               ws, status, s);
+  return launch_bwd_impl<128>(idx, q, k, v, o, lse, dout, dq, dk, dv, geo, scale, full_groups,
+                              ws, status, s);
 }
 
 }  // namespace sep

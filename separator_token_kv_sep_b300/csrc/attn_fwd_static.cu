@@ -30,10 +30,10 @@
 
 namespace sep {
 
-size_t attn_fwd_tc_workspace(int B, int Hkv, int L, int d);
+size_t attn_fwd_tc_workspace(const Geom& geo, int d);
 int launch_attn_fwd_tc(IndexPtrs idx, const void* q, const void* k, const void* v, void* o,
-                       float* lse, int B, int Hq, int Hkv, int L, int d, float scale,
-                       uint64_t full_groups, void* ws, int* status, void* stream);
+                       float* lse, const Geom& geo, int d, float scale, uint64_t full_groups,
+                       void* ws, int* status, void* stream);
 
 namespace {
 
@@ -74,13 +74,14 @@ SEP_API sep_status sep_attn_fwd_static(const void* index_buf, const void* q, con
     return SEP_ERR_INVALID_ARG;
   // Checked in double first so that huge shapes cannot wrap size_t.
   if ((double)B * Hkv * L * d * 4.0 > (double)SEP_STATIC_SCRATCH_BYTES) return SEP_ERR_TOO_LARGE;
-  if (attn_fwd_tc_workspace(B, Hkv, L, d) > SEP_STATIC_SCRATCH_BYTES) return SEP_ERR_TOO_LARGE;
+  const Geom geo = make_geom(B, Hq, Hkv, L, L, 0);
+  if (attn_fwd_tc_workspace(geo, d) > SEP_STATIC_SCRATCH_BYTES) return SEP_ERR_TOO_LARGE;
   if (!(scale > 0.f)) scale = 1.0f / sqrtf(static_cast<float>(d));
   void* ws = scratch_address();
   int* st = device_status_ptr();
   if (!ws || !st) return SEP_ERR_CUDA;
   const IndexPtrs idx = index_ptrs(const_cast<void*>(index_buf), index_layout(B, L, SEP_BLOCK_M));
-  return launch_attn_fwd_tc(idx, q, k, v, o, lse, B, Hq, Hkv, L, d, scale, 0, ws, st, stream) == 0
+  return launch_attn_fwd_tc(idx, q, k, v, o, lse, geo, d, scale, 0, ws, st, stream) == 0
              ? SEP_OK
              : SEP_ERR_CUDA;
 }

@@ -38,18 +38,25 @@ namespace {
 
 constexpr int kChunk = 128 * 128;  // bytes of a [128 rows x 64 cols] bf16 block
 
+// The index header sits at offset 0 of any index buffer: every kernel checks
+// it against the call's geometry before using the fields whose offsets
+// depend on B and L.
+__device__ __forceinline__ bool header_matches(const IndexHeader& h, const Geom& geo) {
+  return h.magic == kIndexMagic && h.B == geo.B && h.L == geo.L && h.block_m == 128 &&
+         h.packed == geo.packed && h.total == geo.R;
+}
+
 template <int D>
 __global__ void __launch_bounds__(256)
-    gather_keep_kernel(IndexPtrs idx, const uint4* __restrict__ k, const uint4* __restrict__ v,
-                       uint4* __restrict__ kk, uint4* __restrict__ vk, int B, int Hkv, int L) {
-  // the header sits at offset 0 of any index buffer: check it before using
-  // the fields whose offsets depend on B and L
+    gather_keep_kernel(IndexPtrs idx, Geom geo, const uint4* __restrict__ k,
+                       const uint4* __restrict__ v, uint4* __restrict__ kk,
+                       uint4* __restrict__ vk) {
   const IndexHeader hdr = *idx.header;
-  if (hdr.magic != kIndexMagic || hdr.B != B || hdr.L != L) return;
-  const int units = keep_units(B, Hkv, L);
+  if (!header_matches(hdr, geo)) return;
+  const int units = keep_units(geo.B, geo.Hkv, geo.L);
   const int lane = threadIdx.x & 31;
   for (int u = blockIdx.x * 8 + (threadIdx.x >> 5); u < units; u += gridDim.x * 8)
-    gather_keep_unit<D>(idx, k, v, kk, vk, nullptr, nullptr, B, Hkv, L, u, lane);
+    gather_keep_unit<D>(idx, geo, k, v, kk, vk, nullptr, nullptr, u, lane);
 }
 
 template <int D>
@@ -84,7 +91,8 @@ constexpr float kRescaleLog2 = 8.0f;
 struct PairPlan {
   int nA, loA, hiA, nB, loB, hiB;  // block records of A and B
   int b, h, tA;
-  bool hasB, valid;
+  int len, row0, tile0;  // the sequence: length, first row in its planes, first tile
+  bool hasB, valid, empty;
   int nG, nT;  // gathered tiles, total tiles
   __device__ bool active(int u, int x) const {
     if (x == 1 && !hasB) return false;
@@ -101,47 +109,72 @@ struct PairPlan {
   }
 };
 
-constexpr int kCtaItems = 64;  // items whose block records a CTA keeps in shared memory
+constexpr int kCtaItems = 64;  // items whose records a CTA keeps in shared memory
 
-// Block records (A, B) of the CTA's k-th item, from shared memory for the
-// first kCtaItems items.
-__device__ __forceinline__ void item_records(IndexPtrs idx, const int4* s_rec, int item, int B,
-                                             int Hq, int T, int4& ba, int4& bb) {
-  const int k = (item - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x);
-  if (k < kCtaItems) {
-    ba = s_rec[2 * k];
-    bb = s_rec[2 * k + 1];
-    return;
-  }
-  const int P = (T + 1) >> 1, BH = B * Hq;
-  const int b = (item % BH) / Hq, tA = 2 * (P - 1 - item / BH);
-  ba = *reinterpret_cast<const int4*>(idx.blocks + ((size_t)b * T + tA) * 4);
-  bb = tA + 1 < T ? *reinterpret_cast<const int4*>(idx.blocks + ((size_t)b * T + tA + 1) * 4) : ba;
+// Records of one item: block records of tiles A and B, and the sequence's.
+__device__ __forceinline__ void read_item_records(IndexPtrs idx, const Geom& geo, int item,
+                                                  int4& ba, int4& bb, int4& sq) {
+  const int P = (geo.T + 1) >> 1, BH = geo.B * geo.Hq;
+  const int b = (item % BH) / geo.Hq, tA = 2 * (P - 1 - item / BH);
+  ba = *reinterpret_cast<const int4*>(idx.blocks + ((size_t)b * geo.T + tA) * 4);
+  bb = tA + 1 < geo.T
+           ? *reinterpret_cast<const int4*>(idx.blocks + ((size_t)b * geo.T + tA + 1) * 4)
+           : ba;
+  sq = *reinterpret_cast<const int4*>(idx.seq + b);
 }
 
+// Records of the CTA's k-th item, from shared memory for the first
+// kCtaItems items.
+__device__ __forceinline__ void item_records(IndexPtrs idx, const int4* s_rec, int item,
+                                             const Geom& geo, int4& ba, int4& bb, int4& sq) {
+  const int k = (item - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x);
+  if (k < kCtaItems) {
+    ba = s_rec[3 * k];
+    bb = s_rec[3 * k + 1];
+    sq = s_rec[3 * k + 2];
+    return;
+  }
+  read_item_records(idx, geo, item, ba, bb, sq);
+}
+
+// The plan of one item.  Items whose pair of tiles starts past the end of
+// their sequence are empty (a pack's shorter sequences) and are skipped by
+// every role; items with inconsistent records are invalid (reported by the
+// TMA producer, skipped by every role).
 __device__ __forceinline__ PairPlan load_plan(IndexPtrs idx, const int4* s_rec, int item,
-                                              int n_items, int B, int Hq, int L, int T,
+                                              int n_items, const Geom& geo,
                                               uint64_t full_groups, int grp) {
   PairPlan pl;
   pl.valid = false;
+  pl.empty = true;
   pl.nT = 0;
   if (item >= n_items) return pl;
-  const int P = (T + 1) >> 1, BH = B * Hq;
+  const int P = (geo.T + 1) >> 1, BH = geo.B * geo.Hq;
   const int pair = P - 1 - item / BH, bh = item % BH;
-  pl.b = bh / Hq;
-  pl.h = bh % Hq;
+  pl.b = bh / geo.Hq;
+  pl.h = bh % geo.Hq;
   pl.tA = 2 * pair;
-  pl.hasB = pl.tA + 1 < T;
-  int4 ba, bb;
-  item_records(idx, s_rec, item, B, Hq, T, ba, bb);
+  int4 ba, bb, sq;
+  item_records(idx, s_rec, item, geo, ba, bb, sq);
+  SeqRec sr;
+  sr.len = sq.x; sr.row0 = sq.y; sr.tile0 = sq.z; sr.pad = 0;
+  pl.len = sr.len; pl.row0 = sr.row0; pl.tile0 = sr.tile0;
+  if (!seq_ok(sr, geo)) {
+    pl.empty = false;  // invalid, not empty: reported
+    return pl;
+  }
+  if (pl.tA * 128 >= pl.len) return pl;  // empty
+  pl.empty = false;
+  const int len = pl.len;
+  pl.hasB = pl.tA * 128 + 128 < len;
   if (group_full(full_groups, pl.h / grp)) {
-    ba = full_block_record(pl.tA, L);
-    bb = full_block_record(pl.tA + 1, L);
+    ba = full_block_record(pl.tA, len);
+    bb = full_block_record(pl.tA + 1, len);
   }
   pl.nA = ba.x; pl.loA = ba.y; pl.hiA = ba.z;
   pl.nB = bb.x; pl.loB = bb.y; pl.hiB = bb.z;
   auto bad = [&](int4 r, int q0) {
-    return r.x < 0 || r.x > r.y || r.y < 0 || r.y > q0 || r.z <= q0 || r.z > L;
+    return r.x < 0 || r.x > r.y || r.y < 0 || r.y > q0 || r.z <= q0 || r.z > len;
   };
   pl.valid = !(bad(ba, pl.tA * 128) ||
                (pl.hasB && (bad(bb, pl.tA * 128 + 128) || bb.x < ba.x || bb.y < ba.y)));
@@ -159,8 +192,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tm_v,
                        const __grid_constant__ CUtensorMap tm_kk,
                        const __grid_constant__ CUtensorMap tm_vk, IndexPtrs idx,
-                       __nv_bfloat16* __restrict__ o, float* __restrict__ lse, int B, int Hq,
-                       int Hkv, int L, float scale_log2, uint64_t full_groups, int* status) {
+                       __nv_bfloat16* __restrict__ o, float* __restrict__ lse, Geom geo,
+                       float scale_log2, uint64_t full_groups, int* status) {
   using C = FwdCfg<D>;
   constexpr int QB = C::QB, NST = C::NST;
   extern __shared__ uint8_t smem_raw[];
@@ -171,29 +204,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint32_t tmem_slot;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int T = (L + 127) >> 7;
-  const int n_items = B * Hq * ((T + 1) >> 1);
+  const int T = geo.T;
+  const int Hq = geo.Hq;
+  const int n_items = geo.B * Hq * ((T + 1) >> 1);
   const int G = gridDim.x;
-  const int grp = Hq / Hkv;
+  const int grp = Hq / geo.Hkv;
 
   const IndexHeader hdr = *idx.header;
-  if (hdr.magic != kIndexMagic || hdr.B != B || hdr.L != L || hdr.block_m != 128) {
+  if (!header_matches(hdr, geo)) {
     if (threadIdx.x == 0) report(status, SEP_ERR_DEVICE_BOUNDS);
     return;
   }
   const int n_win = hdr.n;
-  // block records of this CTA's items (item = blockIdx.x + k * G), read once
-  __shared__ int4 s_rec[2 * kCtaItems];
+  // records of this CTA's items (item = blockIdx.x + k * G), read once
+  __shared__ int4 s_rec[3 * kCtaItems];
   for (int x = threadIdx.x; x < kCtaItems; x += blockDim.x) {
     const int item = static_cast<int>(blockIdx.x) + x * G;
-    if (item < n_items) {
-      const int P = (T + 1) >> 1, BH = B * Hq;
-      const int b = (item % BH) / Hq, tA = 2 * (P - 1 - item / BH);
-      const int4 ra = *reinterpret_cast<const int4*>(idx.blocks + ((size_t)b * T + tA) * 4);
-      s_rec[2 * x] = ra;
-      s_rec[2 * x + 1] =
-          tA + 1 < T ? *reinterpret_cast<const int4*>(idx.blocks + ((size_t)b * T + tA + 1) * 4) : ra;
-    }
+    if (item < n_items) read_item_records(idx, geo, item, s_rec[3 * x], s_rec[3 * x + 1],
+                                          s_rec[3 * x + 2]);
   }
 
   if (threadIdx.x == 0) {
@@ -233,9 +261,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int n = 0, kq = 0;  // K/V stages and query pairs loaded
       bool ok = true;
       for (int it = blockIdx.x; ok && it < n_items; it += G) {
-        const PairPlan pl = load_plan(idx, s_rec, it, n_items, B, Hq, L, T, full_groups, grp);
+        const PairPlan pl = load_plan(idx, s_rec, it, n_items, geo, full_groups, grp);
         if (!pl.valid) {
-          report(status, SEP_ERR_DEVICE_BOUNDS);
+          if (!pl.empty) report(status, SEP_ERR_DEVICE_BOUNDS);
           continue;
         }
         const int qs = kq % QB;
@@ -243,12 +271,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        const int plane_q = pl.b * Hq + pl.h, plane_kv = pl.b * Hkv + pl.h / grp;
+        const int g = pl.h / grp;
+        const int plane_q = geo.qplane(pl.b, pl.h), plane_kv = geo.kvplane(pl.b, g);
         mbar_arrive_expect_tx(&q_full[qs], (pl.hasB ? 2 : 1) * C::TILE);
         for (int x = 0; x < (pl.hasB ? 2 : 1); ++x)
           for (int c = 0; c < C::DCH; ++c)
             tma_load_3d(smem + C::OFF_Q + (qs * 2 + x) * C::TILE + c * kChunk, &tm_q, &q_full[qs],
-                        64 * c, (pl.tA + x) * 128, plane_q);
+                        64 * c, pl.row0 + (pl.tA + x) * 128, plane_q);
         ++kq;
         for (int u = 0; u < pl.nT; ++u) {
           if (!pl.any(u)) continue;
@@ -260,13 +289,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool gat = u < pl.nG;
           const CUtensorMap* mk = gat ? &tm_kk : &tm_k;
           const CUtensorMap* mv = gat ? &tm_vk : &tm_v;
-          const int row = gat ? 128 * u : pl.loA + 128 * (u - pl.nG);
+          // gathered tiles: the sequence's keep rows in plane g of the
+          // workspace; band tiles: rows of the sequence in its kv plane
+          const int row = gat ? 128 * (pl.tile0 + u) : pl.row0 + pl.loA + 128 * (u - pl.nG);
+          const int plane = gat ? g : plane_kv;
           mbar_arrive_expect_tx(&kv_full[st], 2 * C::TILE);
           for (int c = 0; c < C::DCH; ++c) {
             tma_load_3d(smem + C::OFF_K + st * C::TILE + c * kChunk, mk, &kv_full[st], 64 * c,
-                        row, plane_kv);
+                        row, plane);
             tma_load_3d(smem + C::OFF_V + st * C::TILE + c * kChunk, mv, &kv_full[st], 64 * c,
-                        row, plane_kv);
+                        row, plane);
           }
           ++n;
         }
@@ -329,16 +361,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       bool ok = true;
       int it = blockIdx.x;
-      PairPlan pc = load_plan(idx, s_rec, it, n_items, B, Hq, L, T, full_groups, grp);
+      PairPlan pc = load_plan(idx, s_rec, it, n_items, geo, full_groups, grp);
       while (it < n_items && !pc.valid) {
         it += G;
-        pc = load_plan(idx, s_rec, it, n_items, B, Hq, L, T, full_groups, grp);
+        pc = load_plan(idx, s_rec, it, n_items, geo, full_groups, grp);
       }
       if (it < n_items) {
         int kq = 0, qs = 0, n = 0;  // current item's index and Q buffer; K/V stage count
         int u = pc.next(-1);
         int itn = it + G;
-        PairPlan pn = load_plan(idx, s_rec, itn, n_items, B, Hq, L, T, full_groups, grp);  // prefetched
+        PairPlan pn = load_plan(idx, s_rec, itn, n_items, geo, full_groups, grp);  // prefetched
         ok = mbar_wait_warp(&q_full[0], 0, status) && mbar_wait_warp(&kv_full[0], 0, status);
         tc_fence_after();
         if (ok) {
@@ -353,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!same) {
             while (itn < n_items && !pn.valid) {
               itn += G;
-              pn = load_plan(idx, s_rec, itn, n_items, B, Hq, L, T, full_groups, grp);
+              pn = load_plan(idx, s_rec, itn, n_items, geo, full_groups, grp);
             }
             if (itn < n_items) un = pn.next(-1);
           }
@@ -384,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             qs = qsn;
             ci0 = ci1 = 0;
             itn = it + G;
-            pn = load_plan(idx, s_rec, itn, n_items, B, Hq, L, T, full_groups, grp);
+            pn = load_plan(idx, s_rec, itn, n_items, geo, full_groups, grp);
           }
           u = un;
         }
@@ -404,17 +436,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nwords = hdr.nwords;
     int cnt = 0, ko = 0;  // S tiles and items finished by this query tile
     bool ok = true;
-    PairPlan pn = load_plan(idx, s_rec, blockIdx.x, n_items, B, Hq, L, T, full_groups, grp);
+    PairPlan pn = load_plan(idx, s_rec, blockIdx.x, n_items, geo, full_groups, grp);
     for (int it = blockIdx.x; ok && it < n_items; it += G) {
       const PairPlan pl = pn;
-      pn = load_plan(idx, s_rec, it + G, n_items, B, Hq, L, T, full_groups, grp);  // prefetch the next item
+      pn = load_plan(idx, s_rec, it + G, n_items, geo, full_groups, grp);  // prefetch the next item
       if (!pl.valid || (x == 1 && !pl.hasB)) continue;
       const int b = pl.b, h = pl.h;
       const int i = (pl.tA + x) * 128 + r;
       const uint32_t* kbits = idx.keep_bits + (size_t)b * nwords;
       const int n_gath = x ? pl.nB : pl.nA;
       const int lo_x = x ? pl.loB : pl.loA;
-      const int n_w = group_full(full_groups, h / grp) ? L : n_win;  // full groups: no window
+      const int n_w = group_full(full_groups, h / grp) ? pl.len : n_win;  // full groups: no window
+      const int len = pl.len;
+      const size_t orow0 = (size_t)geo.qplane(b, h) * geo.R + pl.row0;  // row 0 of the sequence
       float m_used = -INFINITY, l = 0.f;
       int ci = 0;
       for (int u = 0; u < pl.nT; ++u) {
@@ -529,12 +563,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float inv_l = 1.f / l;
       uint32_t ob[32];
-      __nv_bfloat16* orow = o + (((size_t)b * Hq + h) * L + i) * D;
+      __nv_bfloat16* orow = o + (orow0 + i) * D;
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         tmem_ld32(tO + c0, ob);
         tmem_ld_wait();
-        if (i < L) {
+        if (i < len) {
 #pragma unroll
           for (int q = 0; q < 32; q += 8) {
             uint4 pk;
@@ -549,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (i < L) lse[((size_t)b * Hq + h) * L + i] = (m_used + __log2f(l)) * 0.69314718055994531f;
+      if (i < len) lse[orow0 + i] = (m_used + __log2f(l)) * 0.69314718055994531f;
       tc_fence_before();
     }
   }
@@ -562,34 +596,37 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D>
 int launch_fwd_impl(IndexPtrs idx, const void* q, const void* k, const void* v, void* o, float* lse,
-                    int B, int Hq, int Hkv, int L, float scale, uint64_t full_groups, void* ws,
-                    int* status, cudaStream_t s) {
+                    const Geom& geo, float scale, uint64_t full_groups, void* ws, int* status,
+                    cudaStream_t s) {
   using C = FwdCfg<D>;
-  const size_t plane_elems = (size_t)L * D;
   uint8_t* kk = static_cast<uint8_t*>(ws);
-  uint8_t* vk = kk + align_up((size_t)B * Hkv * plane_elems * 2, 256);
+  uint8_t* vk = kk + align_up((size_t)geo.Hkv * geo.TT * 128 * D * 2, 256);
   const int sms = num_sms();
   profile_mark(0, s);
-  gather_keep_kernel<D><<<keep_pass_ctas(keep_units(B, Hkv, L), sms), 256, 0, s>>>(
-      idx, static_cast<const uint4*>(k), static_cast<const uint4*>(v),
-      reinterpret_cast<uint4*>(kk), reinterpret_cast<uint4*>(vk), B, Hkv, L);
+  gather_keep_kernel<D><<<keep_pass_ctas(keep_units(geo.B, geo.Hkv, geo.L), sms), 256, 0, s>>>(
+      idx, geo, static_cast<const uint4*>(k), static_cast<const uint4*>(v),
+      reinterpret_cast<uint4*>(kk), reinterpret_cast<uint4*>(vk));
+  // head planes of q / k / v: (sequence, head) planes of L rows, or one plane
+  // per head of a pack; the gathered keep rows: one plane per kv head over
+  // the tile space
+  const uint64_t pq = geo.packed ? geo.Hq : (uint64_t)geo.B * geo.Hq;
+  const uint64_t pkv = geo.packed ? geo.Hkv : (uint64_t)geo.B * geo.Hkv;
+  const uint64_t rk = (uint64_t)geo.TT * 128;
   CUtensorMap mq, mk, mv, mkk, mvk;
-  if (!make_bf16_map(&mq, q, (uint64_t)B * Hq, L, D, 128) ||
-      !make_bf16_map(&mk, k, (uint64_t)B * Hkv, L, D, 128) ||
-      !make_bf16_map(&mv, v, (uint64_t)B * Hkv, L, D, 128) ||
-      !make_bf16_map(&mkk, kk, (uint64_t)B * Hkv, L, D, 128) ||
-      !make_bf16_map(&mvk, vk, (uint64_t)B * Hkv, L, D, 128))
+  if (!make_bf16_map(&mq, q, pq, geo.R, D, 128) || !make_bf16_map(&mk, k, pkv, geo.R, D, 128) ||
+      !make_bf16_map(&mv, v, pkv, geo.R, D, 128) ||
+      !make_bf16_map(&mkk, kk, geo.Hkv, rk, D, 128) ||
+      !make_bf16_map(&mvk, vk, geo.Hkv, rk, D, 128))
     return static_cast<int>(cudaErrorInvalidValue);
   auto kern = attn_fwd_tc_kernel<D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return static_cast<int>(e);
   const float scale_log2 = scale * 1.4426950408889634f;
-  const int T = (L + 127) / 128;
-  const long long items = (long long)B * Hq * ((T + 1) / 2);
+  const long long items = (long long)geo.B * geo.Hq * ((geo.T + 1) / 2);
   const int grid = static_cast<int>(items < sms ? items : sms);  // persistent: one CTA per SM
   profile_mark(1, s);
   kern<<<grid, kThreads, C::SMEM, s>>>(mq, mk, mv, mkk, mvk, idx, static_cast<__nv_bfloat16*>(o),
-                                       lse, B, Hq, Hkv, L, scale_log2, full_groups, status);
+                                       lse, geo, scale_log2, full_groups, status);
   const cudaError_t err = cudaGetLastError();
   profile_mark(2, s);
   return static_cast<int>(err);
@@ -597,19 +634,17 @@ int launch_fwd_impl(IndexPtrs idx, const void* q, const void* k, const void* v, 
 
 }  // namespace
 
-size_t attn_fwd_tc_workspace(int B, int Hkv, int L, int d) {
-  return 2 * align_up((size_t)B * Hkv * L * d * 2, 256);
+size_t attn_fwd_tc_workspace(const Geom& geo, int d) {
+  return 2 * align_up((size_t)geo.Hkv * geo.TT * 128 * d * 2, 256);
 }
 
 int launch_attn_fwd_tc(IndexPtrs idx, const void* q, const void* k, const void* v, void* o,
-                       float* lse, int B, int Hq, int Hkv, int L, int d, float scale,
-                       uint64_t full_groups, void* ws, int* status, void* stream) {
+                       float* lse, const Geom& geo, int d, float scale, uint64_t full_groups,
+                       void* ws, int* status, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (d == 64)
-    return launch_fwd_impl<64>(idx, q, k, v, o, lse, B, Hq, Hkv, L, scale, full_groups, ws, status,
-                               s);
-  return launch_fwd_impl<128>(idx, q, k, v, o, lse, B, Hq, Hkv, L, scale, full_groups, ws, status,
-                              s);
+    return launch_fwd_impl<64>(idx, q, k, v, o, lse, geo, scale, full_groups, ws, status, s);
+  return launch_fwd_impl<128>(idx, q, k, v, o, lse, geo, scale, full_groups, ws, status, s);
 }
 
 }  // namespace sep

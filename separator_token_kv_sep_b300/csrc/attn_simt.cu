@@ -30,7 +30,7 @@ __global__ void __launch_bounds__(kWarps * 32)
   const int i = blockIdx.x * kWarps + warp;
   const int h = blockIdx.y, b = blockIdx.z;
   const IndexHeader hdr = *idx.header;
-  if (hdr.magic != kIndexMagic || hdr.B != B || hdr.L != L) {
+  if (hdr.magic != kIndexMagic || hdr.B != B || hdr.L != L || hdr.packed != 0) {
     if (threadIdx.x == 0) report(status, SEP_ERR_DEVICE_BOUNDS);
     return;
   }

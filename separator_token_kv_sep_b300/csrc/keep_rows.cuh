@@ -3,15 +3,16 @@
 //
 // The tokens every query sees before its window (the first a tokens and the
 // separators: anthology record lit-748, Key takeaways, "The mask") are read by
-// every query tile.  Gathering them once into K_keep[b, g, r] =
-// K[b, g, keep_pos[b][r]] (r < keep_count[b], zero rows up to the next
-// multiple of 128) turns them into full 128-row tiles that TMA can load.
+// every query tile.  Gathering them once into dense rows -- keep token r of
+// sequence b, kv head g at row 128 * tile0_b + r of plane g of K_keep /
+// V_keep, zero rows up to the next multiple of 128 -- turns them into full
+// 128-row tiles that TMA can load.
 //
-// Work is cut into units of 16 rows of one (batch, kv head) plane and one
-// warp takes a unit.  Units are numbered chunk-major (unit = chunk * planes
-// + plane), so the units that hold rows come first and the kernels below use
-// a grid of a few CTAs per SM that strides over them; a unit past its plane's
-// padded keep count costs one cached load.
+// Work is cut into units of 16 rows of one (sequence, kv head) pair and one
+// warp takes a unit.  Units are numbered chunk-major (unit = chunk * pairs
+// + pair), so the units that hold rows come first and the kernels below use
+// a grid of a few CTAs per SM that strides over them; a unit past its pair's
+// padded keep count costs two cached loads.
 #pragma once
 
 #include <atomic>
@@ -30,22 +31,26 @@ __host__ __device__ inline int keep_units(int B, int Hkv, int L) {
 // Copies the keep rows of one unit (and, if dk_keep is set, zeroes the same
 // rows of the fp32 gradient accumulators dk_keep / dv_keep).
 template <int D>
-__device__ __forceinline__ void gather_keep_unit(IndexPtrs idx, const uint4* __restrict__ k,
+__device__ __forceinline__ void gather_keep_unit(IndexPtrs idx, const Geom& geo,
+                                                 const uint4* __restrict__ k,
                                                  const uint4* __restrict__ v,
                                                  uint4* __restrict__ kk, uint4* __restrict__ vk,
                                                  float4* __restrict__ dk_keep,
-                                                 float4* __restrict__ dv_keep, int B, int Hkv,
-                                                 int L, int unit, int lane) {
+                                                 float4* __restrict__ dv_keep, int unit,
+                                                 int lane) {
   constexpr int U = D / 8;                         // 16-byte units of a bf16 row
   constexpr int PER = kKeepUnitRows * U / 32;      // per lane
-  const int planes = B * Hkv;
-  const int plane = unit % planes, row0 = (unit / planes) * kKeepUnitRows;
-  const int b = plane / Hkv;
-  const int count = min(max(idx.keep_count[b], 0), L);
-  const int end = min(L, (count + 127) / 128 * 128);
+  const int pairs = geo.B * geo.Hkv;
+  const int pair = unit % pairs, row0 = (unit / pairs) * kKeepUnitRows;
+  const int b = pair / geo.Hkv, g = pair % geo.Hkv;
+  const SeqRec sr = idx.seq[b];
+  if (!seq_ok(sr, geo)) return;
+  const int count = min(max(idx.keep_count[b], 0), sr.len);
+  const int end = (count + 127) / 128 * 128;
   if (row0 >= end) return;
-  const int32_t* kpos = idx.keep_pos + (size_t)b * L;
-  const size_t base = (size_t)plane * L * U;
+  const int32_t* kpos = idx.keep_pos + (size_t)b * geo.L;
+  const size_t src_base = ((size_t)geo.kvplane(b, g) * geo.R + sr.row0) * U;
+  const size_t dst_base = ((size_t)g * geo.TT + sr.tile0) * 128 * U;
   uint4 kv[PER], vv[PER];
 #pragma unroll
   for (int x = 0; x < PER; ++x) {
@@ -54,9 +59,9 @@ __device__ __forceinline__ void gather_keep_unit(IndexPtrs idx, const uint4* __r
     const int src = row < count ? kpos[row] : -1;
     kv[x] = make_uint4(0, 0, 0, 0);
     vv[x] = make_uint4(0, 0, 0, 0);
-    if (src >= 0 && src < L) {
-      kv[x] = k[base + (size_t)src * U + u];
-      vv[x] = v[base + (size_t)src * U + u];
+    if (src >= 0 && src < sr.len) {
+      kv[x] = k[src_base + (size_t)src * U + u];
+      vv[x] = v[src_base + (size_t)src * U + u];
     }
   }
 #pragma unroll
@@ -64,14 +69,14 @@ __device__ __forceinline__ void gather_keep_unit(IndexPtrs idx, const uint4* __r
     const int e = x * 32 + lane;
     const int row = row0 + e / U, u = e % U;
     if (row < end) {
-      kk[base + (size_t)row * U + u] = kv[x];
-      vk[base + (size_t)row * U + u] = vv[x];
+      kk[dst_base + (size_t)row * U + u] = kv[x];
+      vk[dst_base + (size_t)row * U + u] = vv[x];
     }
   }
   if (dk_keep) {
     constexpr int U4 = D / 4;  // float4 of an fp32 row
     const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-    const size_t base4 = (size_t)plane * L * U4;
+    const size_t base4 = ((size_t)g * geo.TT + sr.tile0) * 128 * U4;
 #pragma unroll
     for (int x = 0; x < 2 * PER; ++x) {
       const int e = x * 32 + lane;
@@ -87,20 +92,24 @@ __device__ __forceinline__ void gather_keep_unit(IndexPtrs idx, const uint4* __r
 // dK / dV rows of the keep tokens of one unit, from the fp32 accumulators
 // (dK times the softmax scale), rounded to bf16 once.
 template <int D>
-__device__ __forceinline__ void scatter_keep_unit(IndexPtrs idx, const float4* __restrict__ dk_keep,
+__device__ __forceinline__ void scatter_keep_unit(IndexPtrs idx, const Geom& geo,
+                                                  const float4* __restrict__ dk_keep,
                                                   const float4* __restrict__ dv_keep,
                                                   __nv_bfloat16* __restrict__ dk,
-                                                  __nv_bfloat16* __restrict__ dv, int B, int Hkv,
-                                                  int L, float scale, int unit, int lane) {
+                                                  __nv_bfloat16* __restrict__ dv, float scale,
+                                                  int unit, int lane) {
   constexpr int U4 = D / 4;
   constexpr int PER = kKeepUnitRows * U4 / 32;
-  const int planes = B * Hkv;
-  const int plane = unit % planes, row0 = (unit / planes) * kKeepUnitRows;
-  const int b = plane / Hkv;
-  const int count = min(max(idx.keep_count[b], 0), L);
+  const int pairs = geo.B * geo.Hkv;
+  const int pair = unit % pairs, row0 = (unit / pairs) * kKeepUnitRows;
+  const int b = pair / geo.Hkv, g = pair % geo.Hkv;
+  const SeqRec sr = idx.seq[b];
+  if (!seq_ok(sr, geo)) return;
+  const int count = min(max(idx.keep_count[b], 0), sr.len);
   if (row0 >= count) return;
-  const int32_t* kpos = idx.keep_pos + (size_t)b * L;
-  const size_t base4 = (size_t)plane * L * U4;
+  const int32_t* kpos = idx.keep_pos + (size_t)b * geo.L;
+  const size_t base4 = ((size_t)g * geo.TT + sr.tile0) * 128 * U4;
+  const size_t out_base = ((size_t)geo.kvplane(b, g) * geo.R + sr.row0) * D;
   float4 a[PER], c[PER];
 #pragma unroll
   for (int x = 0; x < PER; ++x) {
@@ -119,13 +128,13 @@ __device__ __forceinline__ void scatter_keep_unit(IndexPtrs idx, const float4* _
     const int row = row0 + e / U4, u = e % U4;
     if (row >= count) continue;
     const int j = kpos[row];
-    if (j < 0 || j >= L) continue;
+    if (j < 0 || j >= sr.len) continue;
     uint2 ko, vo;
     ko.x = pack_bf16x2(a[x].x * scale, a[x].y * scale);
     ko.y = pack_bf16x2(a[x].z * scale, a[x].w * scale);
     vo.x = pack_bf16x2(c[x].x, c[x].y);
     vo.y = pack_bf16x2(c[x].z, c[x].w);
-    const size_t dst = ((size_t)plane * L + j) * D + 4 * u;
+    const size_t dst = out_base + (size_t)j * D + 4 * u;
     *reinterpret_cast<uint2*>(dk + dst) = ko;
     *reinterpret_cast<uint2*>(dv + dst) = vo;
   }

@@ -73,3 +73,17 @@ def test_decode_cache_lengths_match_the_oracle_cache(a, s, w, c, p):
         for t in range(T):
             cache.insert(z, z, bool(sep[t, seq]))
             assert got[t, seq] == cache.total(), (seq, t)
+
+
+def test_packed_pairs_match_packed_oracle_mask():
+    """The packed variant's work count: per-document visited pairs summed
+    equal the unmasked entries of the oracle's packed mask."""
+    from oracle import varlen as V
+    lengths = bench.pack_lengths(700, 16, 300, 5)
+    assert sum(lengths) == 700 and min(lengths) >= 1
+    cu = np.concatenate([[0], np.cumsum(lengths)])
+    rng = np.random.default_rng(12)
+    ids = synth.token_ids(rng, (700,), 0.1)
+    got = sum(bench.visited_pairs_per_head(ids[None, cu[b]:cu[b + 1]], 4, 37)
+              for b in range(len(lengths)))
+    assert got == int(V.packed_mask(ids, cu, synth.SEP_IDS, 4, 37).sum())
