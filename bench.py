@@ -4,7 +4,7 @@
 One timed step = sep_build_index + sep_attn_fwd + sep_attn_bwd on the
 Pythia-160M-shaped training workload (B8 H12 L2048 d64, a=4, n=128,
 separator probability 0.10), replayed from a CUDA graph with L2 flushed
-(256 MiB write) between steps and device time taken from CUDA events.
+(a 256 MiB write, then a 256 MiB read) between steps and device time taken from CUDA events.
 Also measured, in sub-objects of the same JSON line: streaming decode on the
 Llama-3-8B-shaped workload (64 sequences, c = 324, 2048 prompt tokens then
 4096 decode steps; tokens/s against HBM bandwidth) and forward-only prefill
@@ -46,6 +46,25 @@ DRAM_TRAFFIC_BYTES = {"bwd_kv": 143.985408e6 + 23.182080e6, "fwd_attn": 81.94304
                       "bwd_dq": 108.658176e6 + 9.982976e6}
 DECODE_DRAM_TRAFFIC_BYTES = 81.577216e6 + 2.098432e6
 L2_FLUSH_BYTES = 256 << 20
+
+
+class L2Flush:
+    """Evicts L2 between timed steps: writes one 256 MiB buffer (twice the
+    126 MB L2), then reads another 256 MiB buffer, so the lines left in L2
+    are clean and the write-back of the flush's dirty lines happens here,
+    not inside the next timed step."""
+
+    def __init__(self, device):
+        import torch
+        self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+        self.r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=device)
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.sum()
+
+
+L2_NOTE = "flushed between steps (256 MiB write, then a 256 MiB read)"
 
 
 def load_peaks():
@@ -190,7 +209,7 @@ def run_ours(args, rank, world, device):
 
     torch.cuda.set_device(device)
     peaks = load_peaks()
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flush = L2Flush(device)
     stream = torch.cuda.current_stream()
 
     # ---------------------------------------------------------- train step
@@ -248,7 +267,7 @@ def run_ours(args, rank, world, device):
     with torch.cuda.graph(graph):
         train_step(mark=True)
     for _ in range(max(3, args.warmup)):
-        flush.zero_()
+        flush()
         graph.replay()
     torch.cuda.synchronize()
 
@@ -267,7 +286,7 @@ def run_ours(args, rank, world, device):
             torch.distributed.barrier()
         torch.cuda.synchronize()
         for _ in range(args.steps):
-            flush.zero_()
+            flush()
             graph.replay()
             torch.cuda.synchronize()
             t_step.append(step_ev[0].elapsed_time(step_ev[1]))
@@ -320,7 +339,7 @@ def run_ours(args, rank, world, device):
                    " = sep_build_index + sep_attn_fwd + sep_attn_bwd (CUDA graph replay)",
                    "visited_pairs_per_head": pairs, "visited_over_causal":
                        round(pairs / (B * L * (L + 1) / 2), 4),
-                   "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas x{world}"},
+                   "l2": L2_NOTE, "parallelism": f"replicas x{world}"},
         "phases_ms": {"fwd": round(fwd_ms, 5), "bwd": round(bwd_ms, 5),
                       "fwd_tflops": round(fwd_tf, 2), "bwd_tflops": round(bwd_tf, 2)},
         "kernels": kernels,
@@ -494,7 +513,7 @@ def run_decode(args, rank, device, flush, peaks):
     with torch.cuda.graph(graph):
         for j in range(n_dec):
             t = cfg.prompt + j
-            flush.zero_()
+            flush()
             ev_a[j].record()
             api.sep_cache_step(p, buf, dq[t % P], dk[t % P], dv[t % P], dids[t], synth.SEP_IDS,
                                out=out)
@@ -517,7 +536,7 @@ def run_decode(args, rank, device, flush, peaks):
     return {"workload": "llama3_8b_stream_decode " + cfg.describe(),
             "value": round(tok_s, 1), "unit": "tok/s", "ms_per_step": round(total_ms / n_dec, 5),
             "mean_cache_entries": round(float(lens.mean()), 2), "gqa_group": G,
-            "l2": "flushed before every decode step (256 MiB write)",
+            "l2": L2_NOTE + ", before every decode step",
             "roofline": {"bound": "hbm", "kernel": "cache_step_kernel (one launch per step)",
                          "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(gbs / peaks["hbm_gbs"], 4),
@@ -593,7 +612,7 @@ def run_variants(args, rank, device, flush, peaks):
             step()
         times = []
         for it in range(steps + 3):
-            flush.zero_()
+            flush()
             e0.record()
             graph.replay()
             e1.record()
@@ -678,7 +697,7 @@ def run_packed_variant(q, k, v, dout, ids_np, cfg, steps, device, flush, peaks, 
     e1 = torch.cuda.Event(enable_timing=True)
     times = []
     for it in range(steps + 3):
-        flush.zero_()
+        flush()
         e0.record()
         graph.replay()
         e1.record()
@@ -713,7 +732,7 @@ def run_index_scaling(args, rank, device, flush):
     e1 = torch.cuda.Event(enable_timing=True)
     times = []
     for it in range(13):
-        flush.zero_()
+        flush()
         e0.record()
         api.sep_build_index(ids, synth.SEP_IDS, a, n, index_buf=idx_buf)
         e1.record()
@@ -755,7 +774,7 @@ def run_prefill(args, rank, device, flush, peaks):
         e1 = torch.cuda.Event(enable_timing=True)
         times = []
         for it in range(reps + 2):
-            flush.zero_()
+            flush()
             e0.record()
             api.sep_attn_fwd(idx_buf, q, k, v, o=o, lse=lse, ws=ws)
             e1.record()
@@ -868,7 +887,7 @@ def main(argv=None):
         dist.init_process_group("nccl", device_id=device)
     if args.only == "decode":
         torch.cuda.set_device(device)
-        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+        flush = L2Flush(device)
         line = run_decode(args, rank, device, flush, load_peaks())
     else:
         line = run_ours(args, rank, world, device)

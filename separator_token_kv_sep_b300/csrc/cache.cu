@@ -49,7 +49,7 @@ namespace sep {
 namespace {
 
 constexpr int kCacheMagic = 0x43504553;  // 'SEPC'
-constexpr int kConsumerWarps = 4;        // score / softmax / P.V warps
+constexpr int kConsumerWarps = 2;        // score / softmax / P.V warps
 constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one TMA producer warp
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxC = 1024;              // survivor list is kept in shared memory
@@ -60,7 +60,7 @@ constexpr int kTargetCtas = 296;         // CTAs per step the split aims at (2 p
 
 struct CacheLayout {
   int S, Hkv, d, a, s, w, c, NSL, rope_rows;
-  size_t meta, rope, pos, issep, k, v, total;
+  size_t meta, rope, invf, pos, issep, k, v, total;
 };
 
 // Counters of one (sequence, kv head) (int32 x 8 in device memory).  Every
@@ -85,6 +85,8 @@ CacheLayout cache_layout(const sep_cache_params* p) {
   off = align_up(off + sizeof(Meta) * (size_t)l.S * l.Hkv, 256);
   l.rope = off;
   off = align_up(off + sizeof(float2) * (size_t)l.rope_rows * (l.d / 2), 256);
+  l.invf = off;  // inv_freq_i = theta^(-2i/d), float32 [d/2]
+  off = align_up(off + sizeof(float) * (size_t)(l.d / 2), 256);
   l.pos = off;
   off = align_up(off + sizeof(int32_t) * (size_t)l.S * l.NSL, 256);
   l.issep = off;
@@ -100,6 +102,7 @@ CacheLayout cache_layout(const sep_cache_params* p) {
 struct CachePtrs {
   Meta* meta;
   const float2* rope;
+  const float* invf;
   int32_t* pos;
   uint8_t* issep;
   uint16_t* k;
@@ -111,6 +114,7 @@ CachePtrs cache_ptrs(void* buf, const CacheLayout& l) {
   CachePtrs p;
   p.meta = reinterpret_cast<Meta*>(b + l.meta);
   p.rope = reinterpret_cast<const float2*>(b + l.rope);
+  p.invf = reinterpret_cast<const float*>(b + l.invf);
   p.pos = reinterpret_cast<int32_t*>(b + l.pos);
   p.issep = reinterpret_cast<uint8_t*>(b + l.issep);
   p.k = reinterpret_cast<uint16_t*>(b + l.k);
@@ -143,14 +147,6 @@ __device__ __forceinline__ float dsmem_ld(uint32_t addr) {
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
   return v;
 }
-__device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float* f) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(w[i] << 16);
-    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-  }
-}
 
 // The layout after this step's update, expressed through where each entry
 // sits before it:
@@ -165,46 +161,102 @@ struct StepPlan {
   int sk0, pw0;
 };
 
-// Streaming shape of the decode attention: a chunk is the entries the four
-// consumer warps score in one pass (LPE lanes per entry), and NST chunks
-// of K and V rows are in flight through the TMA ring.
+// Streaming shape of the decode attention.  A chunk is 16 entries per
+// consumer warp; NST chunks of K and V rows are in flight.  The producer
+// warp copies them 16 bytes at a time (cp.async) into rows of PU 16-byte
+// units (one more than a row holds), unit u of row r at position u ^ ((r >>
+// 1) & 7): with that pitch and swizzle the consumers' fragment loads (16-byte
+// reads of eight rows at once) touch all 32 banks without conflict.
 template <int D>
 struct StreamShape {
   static constexpr int HALF = D / 2;
-  static constexpr int CPR = D / 8;          // 16-byte pieces per row
-  static constexpr int LPE = CPR / 2;        // lanes per entry when scoring
-  static constexpr int EPW = 32 / LPE;       // entries per warp per chunk
-  static constexpr int CH = kConsumerWarps * EPW;  // entries per chunk
-  static constexpr int DPL = D / 32;         // output dims per lane
-  static constexpr int NST = 4;              // ring stages
-  static constexpr int STAGE = 2 * CH * D * 2;  // bytes: K rows then V rows
+  static constexpr int CPR = D / 8;               // 16-byte units of a K / V row
+  static constexpr int CH = kConsumerWarps * 16;  // entries per chunk
+  static constexpr int PU = CPR + 1;              // units per staged row
+  static constexpr int NST = 3;                   // ring stages
+  static constexpr int OFF_V = CH * PU * 16;
+  static constexpr int STAGE = 2 * CH * PU * 16;  // bytes: K rows, V rows
+  static constexpr int NSLAB = D / 16;            // 16-wide k slabs of a row
+  static constexpr int NLO = D / 32;              // slabs of the first half
+  static constexpr int LD = D / 8;                // dims of each half a lane holds
+  static constexpr int MT = D / 16;               // 16-dim m-tiles of the output
 };
+
+// Byte offset of unit u of staged row r.
+__device__ __forceinline__ int staged_unit(int r, int u, int pu) {
+  return (r * pu + (u ^ ((r >> 1) & 7))) * 16;
+}
+
+// 16-byte global -> shared copy (cp.async, L2 only) and the arrive on an
+// mbarrier once every cp.async this thread issued so far has landed (the
+// arrive counts toward the barrier's expected arrivals).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
 
 // Dynamic shared memory of the step kernel (byte offsets, 16-byte aligned).
 struct StepSmem {
-  int ring, q, wstate, part, pw, surv, total;
+  int ring, q, wstate, part, surv, slots, total;
 };
 
 template <int D, int G>
-__host__ __device__ inline StepSmem step_smem(int s_cap) {
+__host__ __device__ inline StepSmem step_smem(int s_cap, int c_cap) {
   using SS = StreamShape<D>;
   auto al = [](int x) { return (x + 15) / 16 * 16; };
   StepSmem m;
   int off = 0;
   m.ring = off;
   off += SS::NST * SS::STAGE;
+  // the merge state overlays the ring: it is written only once every chunk
+  // has been consumed
+  m.wstate = 0;  // per consumer warp: acc[G][D], m[G], l[G]
+  m.part = al(kConsumerWarps * G * (D + 2) * 4);  // merged partial: acc[G][D], m[G], l[G]
   m.q = off;
   off += al(G * D * 4);
-  m.wstate = off;  // per consumer warp: acc[G][D], m[G], l[G]
-  off += al(kConsumerWarps * G * (D + 2) * 4);
-  m.part = off;    // this CTA's merged partial: acc[G][D], m[G], l[G]
-  off += al(G * (D + 2) * 4);
-  m.pw = off;      // per consumer warp: p[EPW][G] and alpha[G] of the current chunk
-  off += al(kConsumerWarps * (SS::EPW * G + G) * 4);
   m.surv = off;    // surviving separators: window slot, text position
   off += al(2 * (s_cap > 0 ? s_cap : 1) * 4);
+  m.slots = off;   // slot of each entry of this CTA's share (-1: the new token)
+  off += al(c_cap * 4);
   m.total = off;
   return m;
+}
+
+static_assert(kConsumerWarps * 8 * (128 + 2) * 4 + 8 * (128 + 2) * 4 <=
+                  StreamShape<64>::NST * StreamShape<64>::STAGE,
+              "merge state fits in the ring");
+
+
+// D (fp32 16x8) += A (bf16 16x16, row) * B (bf16 16x8, col): the warp-level
+// tensor-core product.  Fragments (g = lane / 4, t = lane % 4): a0 = A[g][2t,
+// 2t+1], a1 = A[g+8][2t, 2t+1], a2 = A[g][2t+8, 2t+9], a3 = A[g+8][2t+8, 2t+9];
+// b0 = B[2t, 2t+1][g], b1 = B[2t+8, 2t+9][g]; d0 = D[g][2t], d1 = D[g][2t+1],
+// d2 = D[g+8][2t], d3 = D[g+8][2t+1].  Lower index in the low 16 bits.
+__device__ __forceinline__ void mma_bf16_16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Transpose of an 8x8 b16 matrix held as one b16x2 per lane (row lane / 4,
+// columns 2 (lane % 4), +1).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+__device__ __forceinline__ uint32_t word_of(const uint4& u, int i) {
+  return i == 0 ? u.x : i == 1 ? u.y : i == 2 ? u.z : u.w;
 }
 
 __device__ __forceinline__ void consumer_sync() {
@@ -221,8 +273,7 @@ __global__ void __launch_bounds__(kThreads, 4)
                       const int32_t* __restrict__ ids_new, uint16_t* __restrict__ out,
                       int* status) {
   using SS = StreamShape<D>;
-  constexpr int HALF = SS::HALF, CPR = SS::CPR, LPE = SS::LPE, EPW = SS::EPW, CH = SS::CH,
-                DPL = SS::DPL, NST = SS::NST;
+  constexpr int HALF = SS::HALF, CPR = SS::CPR, CH = SS::CH, NST = SS::NST;
   extern __shared__ __align__(128) uint8_t dsm[];
   __shared__ int warp_cnt[kWarps];
   __shared__ __align__(8) uint64_t full_bar[NST], empty_bar[NST];
@@ -233,13 +284,12 @@ __global__ void __launch_bounds__(kThreads, 4)
   const int a = args.a, s = args.s, w = args.w, c = args.c, NSL = args.NSL;
   const int ring = c - a;
   const bool attend = q != nullptr && out != nullptr;
-  const StepSmem L = step_smem<D, G>(s);
+  const StepSmem L = step_smem<D, G>(s, c);
   float* sQ = reinterpret_cast<float*>(dsm + L.q);
   float* sW = reinterpret_cast<float*>(dsm + L.wstate);
   float* sAcc = reinterpret_cast<float*>(dsm + L.part);
   float* sM = sAcc + G * D;
   float* sL = sM + G;
-  float* sPx = reinterpret_cast<float*>(dsm + L.pw);
   int* surv_src = reinterpret_cast<int*>(dsm + L.surv);
   int* surv_pos = surv_src + (s > 0 ? s : 1);
 
@@ -319,6 +369,14 @@ __global__ void __launch_bounds__(kThreads, 4)
     nm.t = m.t + 1;
   }
   pl.N = pl.I0 + pl.SK + pl.SV + pl.W0 + 1;
+  // CTA 0 writes the new token's rows at the end: fetch them now
+  uint4 nk = make_uint4(0u, 0u, 0u, 0u), nvv = nk;
+  int32_t new_id = 0;
+  if (rank == 0 && ok && tid < CPR) {
+    nk = *reinterpret_cast<const uint4*>(k_new + mh * D + 8 * tid);
+    nvv = *reinterpret_cast<const uint4*>(v_new + mh * D + 8 * tid);
+    new_id = ids_new[sq];
+  }
 
   // ---- attention over this CTA's share [k0, k1) of the new layout, streamed
   // in chunks of CH entries through an NST-stage ring of TMA bulk copies
@@ -330,9 +388,31 @@ __global__ void __launch_bounds__(kThreads, 4)
     const int k1 = (int)(((long long)N * (rank + 1)) / split);
     const int ne = ok ? k1 - k0 : 0;
     const int n_chunks = (ne + CH - 1) / CH;
+    // where each entry of the share sits before the update
+    {
+      int* slots = reinterpret_cast<int*>(dsm + L.slots);
+      const int rS = pl.I0, rV = rS + pl.SK, rW = rV + pl.SV, rN = N - 1;
+      for (int e = k0 + tid; e < k0 + ne; e += kThreads) {
+        int slot;
+        if (e == rN) {
+          slot = -1;
+        } else if (e < rS) {
+          slot = e;
+        } else if (e < rV) {
+          int x = pl.sk0 + (e - rS);  // < 2 s
+          slot = a + (x >= s ? x - s : x);
+        } else if (e < rW) {
+          slot = surv_src[e - rV];
+        } else {
+          int x = pl.pw0 + (e - rW);  // < 2 ring
+          slot = a + s + (x >= ring ? x - ring : x);
+        }
+        slots[e - k0] = slot;
+      }
+    }
     if (tid == 0) {
       for (int st = 0; st < NST; ++st) {
-        mbar_init(&full_bar[st], 1);
+        mbar_init(&full_bar[st], 32);  // the producer lanes' cp.async arrivals
         mbar_init(&empty_bar[st], kConsumerWarps);
       }
       fence_mbar_init();
@@ -341,49 +421,48 @@ __global__ void __launch_bounds__(kThreads, 4)
 
     if (warp == kConsumerWarps) {
       // ------------------------------------------------------------ producer
-      if (lane == 0 && ne > 0) {
+      // Chunk ch holds entries [c0, c0 + n): each lane copies 16-byte units
+      // of their K and V rows, from the slot an entry has before the update
+      // or from the caller's new token.
+      if (ne > 0) {
         const uint16_t* kh = cp.k + head_off;
         const uint16_t* vh = cp.v + head_off;
         const size_t new_off = mh * D;  // [S][Hkv][D] inputs
-        const int rS = pl.I0, rV = rS + pl.SK, rW = rV + pl.SV, rN = pl.N - 1;
         for (int ch = 0; ch < n_chunks; ++ch) {
           const int st = ch % NST;
-          if (ch >= NST && !mbar_wait(&empty_bar[st], ((ch / NST) - 1) & 1, status)) break;
-          const int c0 = k0 + ch * CH, c1 = min(k1, c0 + CH);
-          uint16_t* dK = reinterpret_cast<uint16_t*>(dsm + L.ring + st * SS::STAGE);
-          uint16_t* dV = dK + CH * D;
-          mbar_arrive_expect_tx(&full_bar[st], (uint32_t)((c1 - c0) * D * 2 * 2));
-          // runs of consecutive slots: slots slot0 .. slot0 + (hi - lo) - 1
-          auto run = [&](int lo, int hi, int slot0) {
-            if (hi <= lo) return;
-            const uint32_t bytes = (uint32_t)((hi - lo) * D * 2);
-            bulk_g2s(dK + (size_t)(lo - c0) * D, kh + (size_t)slot0 * D, bytes, &full_bar[st]);
-            bulk_g2s(dV + (size_t)(lo - c0) * D, vh + (size_t)slot0 * D, bytes, &full_bar[st]);
-          };
-          auto ring_run = [&](int r_lo, int r_hi, int base_slot, int head, int size) {
-            const int lo = max(r_lo, c0), hi = min(r_hi, c1);
-            if (hi <= lo) return;
-            const int p0 = (head + (lo - r_lo)) % size;
-            const int n1 = min(hi - lo, size - p0);
-            run(lo, lo + n1, base_slot + p0);
-            run(lo + n1, hi, base_slot);
-          };
-          run(c0, min(rS, c1), c0);
-          if (s > 0) ring_run(rS, rV, a, pl.sk0, s);
-          for (int k = max(rV, c0); k < min(rW, c1); ++k) run(k, k + 1, surv_src[k - rV]);
-          ring_run(rW, rN, a + s, pl.pw0, ring);
-          if (c0 <= rN && rN < c1) {
-            bulk_g2s(dK + (size_t)(rN - c0) * D, k_new + new_off, D * 2, &full_bar[st]);
-            bulk_g2s(dV + (size_t)(rN - c0) * D, v_new + new_off, D * 2, &full_bar[st]);
+          if (ch >= NST && !mbar_wait_warp(&empty_bar[st], ((ch / NST) - 1) & 1, status)) break;
+          const int c0 = k0 + ch * CH, n = min(k1, c0 + CH) - c0;
+          uint8_t* stg = dsm + L.ring + st * SS::STAGE;
+          const int* sl_c = reinterpret_cast<const int*>(dsm + L.slots) + (c0 - k0);
+          for (int x = lane; x < n * CPR; x += 32) {
+            const int r = x / CPR, u = x % CPR;  // CPR is a power of two
+            const int slot = sl_c[r];
+            const uint16_t* bk = slot < 0 ? k_new + new_off : kh + (size_t)slot * D;
+            const uint16_t* bv = slot < 0 ? v_new + new_off : vh + (size_t)slot * D;
+            const int du = staged_unit(r, u, SS::PU);
+            cp_async16(stg + du, bk + 8 * u);
+            cp_async16(stg + SS::OFF_V + du, bv + 8 * u);
           }
+          cp_async_arrive(&full_bar[st]);
         }
+        // nothing this lane copies may land after the CTA is gone
+        asm volatile("cp.async.wait_all;" ::: "memory");
       }
     } else {
       // ------------------------------------------------------------ consumers
-      // Rotated queries of the G heads at position N-1, stored so that the
-      // LPE lanes scoring one entry read 16 consecutive bytes each, lane
-      // after lane (no bank conflicts): sQ[h][j][l][4] holds, for lane l,
-      // q[8l + 4j .. +4) (j = 0, 1) and q[HALF + 8l + 4(j-2) .. +4) (j = 2, 3).
+      // Warp w owns entries [16w, 16w + 16) of every chunk.  Per chunk:
+      //   S^T = Krot Q^T on the tensor cores (m = 16 entries, n = 8 heads,
+      //   k = d), Krot = K rotated by RoPE at the entry's rank, in registers;
+      //   online softmax per head (lazy rescale);
+      //   O^T += V^T P^T (m = 16 dims, n = 8 heads, k = 16 entries), P^T by
+      //   an in-register transpose of the S^T fragments.
+      // Lane (g, t) = (lane / 4, lane % 4).  In the QK product its k columns
+      // {2t, 2t+1, 2t+8, 2t+9} of slab s are dims LD t + 4s + {0..3} of the
+      // first half (slabs s < NLO) or the same dims + HALF (slabs NLO + s):
+      // the pairs RoPE rotates together stay in one lane.  In the PV product
+      // its m rows g, g+8 of m-tile mt are dims LD g + mt and LD g + MT + mt.
+      constexpr int LD = SS::LD, NLO = SS::NLO, MT = SS::MT;
+      // rotated queries of the G heads at position N-1 into sQ[h][D] (fp32)
       if (ok) {
         const float2* cs_row = cp.rope + (size_t)(N - 1) * HALF;
         for (int e = tid; e < G * HALF; e += kConsumerWarps * 32) {
@@ -392,216 +471,220 @@ __global__ void __launch_bounds__(kThreads, 4)
           const float2 cs = cs_row[i];
           const float x1 = __uint_as_float((uint32_t)qr[i] << 16);
           const float x2 = __uint_as_float((uint32_t)qr[i + HALF] << 16);
-          const int l = i / 8, j = (i % 8) / 4, x = i % 4;
-          float* qh = sQ + hh * D + l * 4 + x;
-          qh[j * (4 * LPE)] = x1 * cs.x - x2 * cs.y;
-          qh[(j + 2) * (4 * LPE)] = x2 * cs.x + x1 * cs.y;
+          sQ[hh * D + i] = x1 * cs.x - x2 * cs.y;
+          sQ[hh * D + i + HALF] = x2 * cs.x + x1 * cs.y;
         }
       }
       consumer_sync();
-      constexpr int HPL = G > LPE ? G / LPE : 1;  // heads a lane keeps after the reduce-scatter
-      const int sub = lane / LPE, l8 = lane % LPE;
-      const int i0 = 8 * l8;  // this lane's first frequency index when scoring
-      const int e_w = warp * EPW + sub;  // entry of this lane within a chunk
-      float* sPw = sPx + warp * (EPW * G + G);  // this warp's p[EPW][G], then alpha[G]
-      // heads this lane holds after the reduce-scatter, and whether it is
-      // the lowest lane of its entry holding them (it publishes p)
-      int hbase = 0;
-      {
-        int cur = G, off = LPE / 2;
-        for (; off > 0 && cur > 1; off >>= 1) {
-          cur >>= 1;
-          if (l8 & off) hbase += cur;
+      const int gq = lane >> 2, tq = lane & 3;
+      // Q^T fragments (B operand): b0 = q[gq][dims +0, +1], b1 = q[gq][+2, +3]
+      uint32_t qf[SS::NSLAB][2];
+#pragma unroll
+      for (int sl = 0; sl < SS::NSLAB; ++sl) {
+        const int dim = (sl < NLO ? 0 : HALF) + LD * tq + 4 * (sl % NLO);
+        if (gq < G) {
+          const float* qrow = sQ + gq * D + dim;
+          qf[sl][0] = pack_bf16x2(qrow[0], qrow[1]);
+          qf[sl][1] = pack_bf16x2(qrow[2], qrow[3]);
+        } else {
+          qf[sl][0] = qf[sl][1] = 0u;
         }
       }
-      const int plain_mask = (G >= LPE) ? 0 : (LPE / G) - 1;  // lanes repeating a head
-      const bool publisher = (l8 & plain_mask) == 0;
-      // (cos, sin) of the lane's 8 frequencies at its first position, and the
-      // rotation by CH positions that advances it chunk to chunk
-      float cz[8], sz[8], cst[8], sst[8];
-      {
-        const float2* r0 = cp.rope + (size_t)min(k0 + e_w, c - 1) * HALF + i0;
-        const float2* rs = cp.rope + (size_t)CH * HALF + i0;
+      const bool hv0 = 2 * tq < G, hv1 = 2 * tq + 1 < G;  // heads 2t, 2t+1 exist
+      // inv_freq of the lane's frequencies LD t .. LD t + LD - 1
+      float ifr[LD];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float2 t0 = r0[j], ts = rs[j];
-          cz[j] = t0.x; sz[j] = t0.y; cst[j] = ts.x; sst[j] = ts.y;
-        }
-      }
-      // running max (log2 units; moved only when a score exceeds it by more
-      // than kLazyRescale, so p <= 2^kLazyRescale) and sum for the held heads
-      float mrun[HPL], lrun[HPL];
+      for (int j = 0; j < LD; ++j) ifr[j] = cp.invf[LD * tq + j];
+      float acc[MT][4];
 #pragma unroll
-      for (int x = 0; x < HPL; ++x) {
-        mrun[x] = -INFINITY;
-        lrun[x] = 0.f;
-      }
-      float acc[G][DPL];
-#pragma unroll
-      for (int hh = 0; hh < G; ++hh)
-#pragma unroll
-        for (int x = 0; x < DPL; ++x) acc[hh][x] = 0.f;
+      for (int mt = 0; mt < MT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+      float mrun0 = -INFINITY, mrun1 = -INFINITY, lrun0 = 0.f, lrun1 = 0.f;
       for (int ch = 0; ch < n_chunks; ++ch) {
         const int st = ch % NST;
+        const int c0 = k0 + ch * CH;
+        const int nv = min(k1, c0 + CH) - c0;  // live entries of the chunk
+        const int e0 = 16 * warp;             // this warp's first chunk row
+        const int rg = e0 + gq, rg8 = rg + 8;
+        const bool live_g = rg < nv, live_g8 = rg8 < nv;
         if (!mbar_wait(&full_bar[st], (ch / NST) & 1, status)) {
           att_ok = false;
           break;
         }
-        const uint16_t* sK = reinterpret_cast<const uint16_t*>(dsm + L.ring + st * SS::STAGE);
-        const uint16_t* sV = sK + CH * D;
-        const bool live = ch * CH + e_w < ne;
-        // ---- partial dot products of the rotated key with the G queries
-        float part[G];
+        const uint8_t* sK = dsm + L.ring + st * SS::STAGE;
+        const uint8_t* sV = sK + SS::OFF_V;
+        const float pos_g = static_cast<float>(c0 + rg);
+        // ---- S^T = Krot Q^T
+        // two accumulators (first / second half slabs) halve the MMA chain
+        float sacc[4] = {0.f, 0.f, 0.f, 0.f}, sacc2[4] = {0.f, 0.f, 0.f, 0.f};
         {
-          float lo[8], hi[8];
-          const uint16_t* row = sK + (size_t)(live ? e_w : 0) * D;
-          bf16x8_to_f32(*reinterpret_cast<const uint4*>(row + i0), lo);
-          bf16x8_to_f32(*reinterpret_cast<const uint4*>(row + i0 + HALF), hi);
-          float rl[8], rh[8];
+          // K units of the lane's dims: first half units (LD / 8) t + u,
+          // second half HALF / 8 + (LD / 8) t + u (rows of dead entries hold
+          // stale values; their scores are masked)
+          uint4 klo[2][LD / 8], khi[2][LD / 8];
 #pragma unroll
-          for (int j = 0; j < 8; j += 2) {
-            float t0, t1;
-            fmul2(t0, t1, hi[j], hi[j + 1], sz[j], sz[j + 1]);
-            ffma2(rl[j], rl[j + 1], lo[j], lo[j + 1], cz[j], cz[j + 1], -t0, -t1);
-            fmul2(t0, t1, lo[j], lo[j + 1], sz[j], sz[j + 1]);
-            ffma2(rh[j], rh[j + 1], hi[j], hi[j + 1], cz[j], cz[j + 1], t0, t1);
-          }
+          for (int x = 0; x < 2; ++x) {
+            const int r = x ? rg8 : rg;
 #pragma unroll
-          for (int hh = 0; hh < G; ++hh) {
-            const float4* qv = reinterpret_cast<const float4*>(sQ + hh * D + l8 * 4);
-            const float4 a0 = qv[0], a1 = qv[LPE], b0 = qv[2 * LPE], b1 = qv[3 * LPE];
-            float u0, u1;
-            fmul2(u0, u1, rl[0], rl[1], a0.x, a0.y);
-            ffma2(u0, u1, rl[2], rl[3], a0.z, a0.w, u0, u1);
-            ffma2(u0, u1, rl[4], rl[5], a1.x, a1.y, u0, u1);
-            ffma2(u0, u1, rl[6], rl[7], a1.z, a1.w, u0, u1);
-            ffma2(u0, u1, rh[0], rh[1], b0.x, b0.y, u0, u1);
-            ffma2(u0, u1, rh[2], rh[3], b0.z, b0.w, u0, u1);
-            ffma2(u0, u1, rh[4], rh[5], b1.x, b1.y, u0, u1);
-            ffma2(u0, u1, rh[6], rh[7], b1.z, b1.w, u0, u1);
-            part[hh] = u0 + u1;
-          }
-        }
-        // ---- reduce-scatter over the entry's LPE lanes: each lane ends up
-        // with the full scores of HPL heads (hbase ..)
-        float sc[HPL];
-        {
-          float cur[G];
-#pragma unroll
-          for (int hh = 0; hh < G; ++hh) cur[hh] = part[hh];
-          int n = G;
-#pragma unroll
-          for (int off = LPE / 2; off > 0; off >>= 1) {
-            if (n > HPL) {
-              const int half = n / 2;
-              const bool up = (l8 & off) != 0;
-#pragma unroll
-              for (int x = 0; x < G / 2; ++x) {
-                if (x < half) {
-                  const float send = up ? cur[x] : cur[x + half];
-                  const float keep = up ? cur[x + half] : cur[x];
-                  cur[x] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-                }
-              }
-              n = half;
-            } else {
-#pragma unroll
-              for (int x = 0; x < HPL; ++x) cur[x] += __shfl_xor_sync(0xffffffffu, cur[x], off);
+            for (int u = 0; u < LD / 8; ++u) {
+              klo[x][u] = *reinterpret_cast<const uint4*>(
+                  sK + staged_unit(r, (LD / 8) * tq + u, SS::PU));
+              khi[x][u] = *reinterpret_cast<const uint4*>(
+                  sK + staged_unit(r, HALF / 8 + (LD / 8) * tq + u, SS::PU));
             }
           }
 #pragma unroll
-          for (int x = 0; x < HPL; ++x) sc[x] = live ? cur[x] * args.scale_log2 : -INFINITY;
-        }
-        // ---- online softmax over the warp's EPW entries, per held head
+          for (int sl = 0; sl < NLO; ++sl) {
+            uint32_t alo[2][2], ahi[2][2];  // [entry g / g+8][dims +0/+1, +2/+3]
 #pragma unroll
-        for (int x = 0; x < HPL; ++x) {
-          float cm = sc[x];
+            // (cos, sin) of freqs LD t + 4 sl + 0..3 at entry g's rank, and
+            // at entry g+8's (8 ranks on: the angle-addition formulas with
+            // (cos, sin)(8 theta_i), row 8 of the table)
+            float4 cg01, cg23, cq01, cq23;
+            __sincosf(pos_g * ifr[4 * sl], &cg01.y, &cg01.x);
+            __sincosf(pos_g * ifr[4 * sl + 1], &cg01.w, &cg01.z);
+            __sincosf(pos_g * ifr[4 * sl + 2], &cg23.y, &cg23.x);
+            __sincosf(pos_g * ifr[4 * sl + 3], &cg23.w, &cg23.z);
+            {
+              const float4* r8 = reinterpret_cast<const float4*>(cp.rope + 8 * HALF + LD * tq + 4 * sl);
+              const float4 e01 = r8[0], e23 = r8[1];  // (cos, sin) of 8 theta, two freqs each
+              float t0, t1;
+              fmul2(t0, t1, cg01.y, cg01.w, e01.y, e01.w);
+              ffma2(cq01.x, cq01.z, cg01.x, cg01.z, e01.x, e01.z, -t0, -t1);
+              fmul2(t0, t1, cg01.x, cg01.z, e01.y, e01.w);
+              ffma2(cq01.y, cq01.w, cg01.y, cg01.w, e01.x, e01.z, t0, t1);
+              fmul2(t0, t1, cg23.y, cg23.w, e23.y, e23.w);
+              ffma2(cq23.x, cq23.z, cg23.x, cg23.z, e23.x, e23.z, -t0, -t1);
+              fmul2(t0, t1, cg23.x, cg23.z, e23.y, e23.w);
+              ffma2(cq23.y, cq23.w, cg23.y, cg23.w, e23.x, e23.z, t0, t1);
+            }
 #pragma unroll
-          for (int off = LPE; off < 32; off <<= 1)
-            cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, off));
-          float alpha = 1.f;
-          if (cm > mrun[x] + kLazyRescale) {  // uniform across the lanes holding the head
-            alpha = mrun[x] == -INFINITY ? 0.f : exp2f(mrun[x] - cm);
-            mrun[x] = cm;
+            for (int x = 0; x < 2; ++x) {
+              const float4 c01 = x ? cq01 : cg01, c23 = x ? cq23 : cg23;
+              const uint32_t l01 = word_of(klo[x][sl / 2], 2 * (sl % 2));
+              const uint32_t l23 = word_of(klo[x][sl / 2], 2 * (sl % 2) + 1);
+              const uint32_t h01 = word_of(khi[x][sl / 2], 2 * (sl % 2));
+              const uint32_t h23 = word_of(khi[x][sl / 2], 2 * (sl % 2) + 1);
+              float rl0, rl1, rl2, rl3, rh0, rh1, rh2, rh3, t0, t1;
+              // rl = lo cos - hi sin; rh = hi cos + lo sin
+              fmul2(t0, t1, bf_lo(h01), bf_hi(h01), c01.y, c01.w);
+              ffma2(rl0, rl1, bf_lo(l01), bf_hi(l01), c01.x, c01.z, -t0, -t1);
+              fmul2(t0, t1, bf_lo(l01), bf_hi(l01), c01.y, c01.w);
+              ffma2(rh0, rh1, bf_lo(h01), bf_hi(h01), c01.x, c01.z, t0, t1);
+              fmul2(t0, t1, bf_lo(h23), bf_hi(h23), c23.y, c23.w);
+              ffma2(rl2, rl3, bf_lo(l23), bf_hi(l23), c23.x, c23.z, -t0, -t1);
+              fmul2(t0, t1, bf_lo(l23), bf_hi(l23), c23.y, c23.w);
+              ffma2(rh2, rh3, bf_lo(h23), bf_hi(h23), c23.x, c23.z, t0, t1);
+              alo[x][0] = pack_bf16x2(rl0, rl1);
+              alo[x][1] = pack_bf16x2(rl2, rl3);
+              ahi[x][0] = pack_bf16x2(rh0, rh1);
+              ahi[x][1] = pack_bf16x2(rh2, rh3);
+            }
+            mma_bf16_16816(sacc, alo[0][0], alo[1][0], alo[0][1], alo[1][1], qf[sl][0],
+                           qf[sl][1]);
+            mma_bf16_16816(sacc2, ahi[0][0], ahi[1][0], ahi[0][1], ahi[1][1], qf[NLO + sl][0],
+                           qf[NLO + sl][1]);
           }
-          const float pe = live ? exp2f(sc[x] - mrun[x]) : 0.f;
-          float ps = pe;
 #pragma unroll
-          for (int off = LPE; off < 32; off <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
-          lrun[x] = lrun[x] * alpha + ps;
-          if (publisher) {
-            sPw[sub * G + hbase + x] = pe;
-            if (sub == 0) sPw[EPW * G + hbase + x] = alpha;
-          }
+          for (int x = 0; x < 4; ++x) sacc[x] += sacc2[x];
         }
-        __syncwarp();
-        // ---- P V: lane owns output dims [DPL*lane, DPL*lane + DPL)
+        // ---- online softmax per head (heads 2t, 2t+1; entries g, g+8)
+        const float sl2 = args.scale_log2;
+        const float s00 = (live_g && hv0) ? sacc[0] * sl2 : -INFINITY;
+        const float s01 = (live_g && hv1) ? sacc[1] * sl2 : -INFINITY;
+        const float s10 = (live_g8 && hv0) ? sacc[2] * sl2 : -INFINITY;
+        const float s11 = (live_g8 && hv1) ? sacc[3] * sl2 : -INFINITY;
+        float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        // lazy rescale: the running max moves only when a score exceeds it by
+        // more than kLazyRescale (uniform over the lanes holding the head)
+        float al0 = 1.f, al1 = 1.f;
+        if (mx0 > mrun0 + kLazyRescale) {
+          al0 = mrun0 == -INFINITY ? 0.f : exp2f(mrun0 - mx0);
+          mrun0 = mx0;
+        }
+        if (mx1 > mrun1 + kLazyRescale) {
+          al1 = mrun1 == -INFINITY ? 0.f : exp2f(mrun1 - mx1);
+          mrun1 = mx1;
+        }
+        if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            acc[mt][0] *= al0;
+            acc[mt][2] *= al0;
+            acc[mt][1] *= al1;
+            acc[mt][3] *= al1;
+          }
+          lrun0 *= al0;
+          lrun1 *= al1;
+        }
+        const float p00 = s00 == -INFINITY ? 0.f : exp2f(s00 - mrun0);
+        const float p01 = s01 == -INFINITY ? 0.f : exp2f(s01 - mrun1);
+        const float p10 = s10 == -INFINITY ? 0.f : exp2f(s10 - mrun0);
+        const float p11 = s11 == -INFINITY ? 0.f : exp2f(s11 - mrun1);
+        lrun0 += p00 + p10;  // this lane's entries; summed over lanes at the end
+        lrun1 += p01 + p11;
+        // P^T fragments: rows of P^T(entries x heads) transposed in registers
+        const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p00, p01));
+        const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p10, p11));
+        // ---- O^T += V^T P^T; dead entries' rows read as zero
         {
-          const float* al = sPw + EPW * G;
-          bool rescale = false;
+          constexpr int VW = LD / 2;  // words of a lane's dims in one V row
+          uint32_t vr[4][VW];         // entries 2t, 2t+1, 2t+8, 2t+9
 #pragma unroll
-          for (int hh = 0; hh < G; ++hh) rescale |= al[hh] != 1.f;
-          if (rescale) {
+          for (int x = 0; x < 4; ++x) {
+            const int r = e0 + 2 * tq + (x & 1) + 8 * (x >> 1);
+            const bool live = r < nv;
 #pragma unroll
-            for (int hh = 0; hh < G; ++hh) {
-              const float f = al[hh];
-#pragma unroll
-              for (int x = 0; x < DPL; ++x) acc[hh][x] *= f;
+            for (int u = 0; u < VW / 4; ++u) {
+              const uint4 w = live ? *reinterpret_cast<const uint4*>(
+                                         sV + staged_unit(r, (LD / 8) * gq + u, SS::PU))
+                                   : make_uint4(0u, 0u, 0u, 0u);
+              vr[x][4 * u] = w.x;
+              vr[x][4 * u + 1] = w.y;
+              vr[x][4 * u + 2] = w.z;
+              vr[x][4 * u + 3] = w.w;
             }
           }
-        }
 #pragma unroll
-        for (int e = 0; e < EPW; ++e) {
-          if (ch * CH + warp * EPW + e >= ne) break;  // rows past the chunk hold stale data
-          float v[DPL];
-          const uint16_t* vr = sV + (size_t)(warp * EPW + e) * D + DPL * lane;
-          if (DPL == 4) {
-            const uint2 u = *reinterpret_cast<const uint2*>(vr);
-            v[0] = __uint_as_float(u.x << 16);
-            v[1] = __uint_as_float(u.x & 0xffff0000u);
-            v[2] = __uint_as_float(u.y << 16);
-            v[3] = __uint_as_float(u.y & 0xffff0000u);
-          } else {
-            const uint32_t u = *reinterpret_cast<const uint32_t*>(vr);
-            v[0] = __uint_as_float(u << 16);
-            v[1] = __uint_as_float(u & 0xffff0000u);
-          }
-          const float* pr = sPw + e * G;
-#pragma unroll
-          for (int hh = 0; hh < G; ++hh) {
-            const float pe = pr[hh];
-#pragma unroll
-            for (int x = 0; x < DPL; x += 2)
-              ffma2(acc[hh][x], acc[hh][x + 1], pe, pe, v[x], v[x + 1], acc[hh][x], acc[hh][x + 1]);
+          for (int mt = 0; mt < MT; ++mt) {
+            const uint32_t sel = (mt & 1) ? 0x7632u : 0x5410u;
+            const int wa = mt / 2, wb = (MT + mt) / 2;
+            const uint32_t a0 = __byte_perm(vr[0][wa], vr[1][wa], sel);
+            const uint32_t a1 = __byte_perm(vr[0][wb], vr[1][wb], sel);
+            const uint32_t a2 = __byte_perm(vr[2][wa], vr[3][wa], sel);
+            const uint32_t a3 = __byte_perm(vr[2][wb], vr[3][wb], sel);
+            mma_bf16_16816(acc[mt], a0, a1, a2, a3, pb0, pb1);
           }
         }
-        __syncwarp();  // p / alpha of this chunk are read before the next chunk rewrites them
+        __syncwarp();  // every lane has read the stage
         if (lane == 0) mbar_arrive(&empty_bar[st]);
-        // advance the angles by CH positions
-#pragma unroll
-        for (int j = 0; j < 8; j += 2) {
-          float c0, c1, s0, s1;
-          fmul2(c0, c1, sz[j], sz[j + 1], sst[j], sst[j + 1]);
-          ffma2(c0, c1, cz[j], cz[j + 1], cst[j], cst[j + 1], -c0, -c1);
-          fmul2(s0, s1, cz[j], cz[j + 1], sst[j], sst[j + 1]);
-          ffma2(s0, s1, sz[j], sz[j + 1], cst[j], cst[j + 1], s0, s1);
-          cz[j] = c0; cz[j + 1] = c1; sz[j] = s0; sz[j + 1] = s1;
-        }
       }
-      // merge the four warps' states into this CTA's partial: the lanes
-      // holding a head publish its running max and sum
+      // this warp's state into sW[warp][head]: acc (dims), running max, sum
+      // (sW overlays the ring: both warps are past their last chunk first)
 #pragma unroll
-      for (int hh = 0; hh < G; ++hh) {
-        float* ws = sW + (warp * G + hh) * (D + 2);
-#pragma unroll
-        for (int x = 0; x < DPL; ++x) ws[DPL * lane + x] = acc[hh][x];
+      for (int off = 4; off < 32; off <<= 1) {
+        lrun0 += __shfl_xor_sync(0xffffffffu, lrun0, off);
+        lrun1 += __shfl_xor_sync(0xffffffffu, lrun1, off);
       }
-      if (sub == 0 && publisher) {
+      consumer_sync();
 #pragma unroll
-        for (int x = 0; x < HPL; ++x) {
-          float* ws = sW + (warp * G + hbase + x) * (D + 2);
-          ws[D] = mrun[x];
-          ws[D + 1] = lrun[x];
+      for (int x = 0; x < 2; ++x) {
+        const int hh = 2 * tq + x;
+        if (hh < G) {
+          float* ws = sW + (warp * G + hh) * (D + 2);
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            ws[LD * gq + mt] = acc[mt][x];
+            ws[LD * gq + MT + mt] = acc[mt][2 + x];
+          }
+          if (gq == 0) {
+            ws[D] = x ? mrun1 : mrun0;
+            ws[D + 1] = x ? lrun1 : lrun0;
+          }
         }
       }
       consumer_sync();
@@ -620,10 +703,18 @@ __global__ void __launch_bounds__(kThreads, 4)
             den = fmaf(f, ws[D + 1], den);
           }
         }
-        sAcc[e] = num;
-        if (x == 0) {
-          sM[hh] = M;
-          sL[hh] = den;
+        if (split == 1) {  // the whole cache is this CTA's: the output is final
+          if (att_ok) {
+            const __nv_bfloat16 bv = __float2bfloat16_rn(num / den);
+            out[(((size_t)sq * args.Hq) + g * G + hh) * D + x] =
+                *reinterpret_cast<const uint16_t*>(&bv);
+          }
+        } else {
+          sAcc[e] = num;
+          if (x == 0) {
+            sM[hh] = M;
+            sL[hh] = den;
+          }
         }
       }
     }
@@ -631,10 +722,13 @@ __global__ void __launch_bounds__(kThreads, 4)
   }
 
   // ---- merge the cluster's partial states (each CTA a slice of the outputs),
-  // then CTA 0 writes the update once every CTA has finished reading
-  cluster_arrive();
-  cluster_wait();
-  if (attend && att_ok) {
+  // then CTA 0 writes the update once every CTA has finished reading (a
+  // cluster of one CTA needs no cluster barrier)
+  if (split > 1) {
+    cluster_arrive();
+    cluster_wait();
+  }
+  if (attend && att_ok && split > 1) {
     const int per = (G * D + split - 1) / split;
     const int e_lo = rank * per, e_hi = min(G * D, e_lo + per);
     for (int e = e_lo + tid; e < e_hi; e += kThreads) {
@@ -692,14 +786,11 @@ __global__ void __launch_bounds__(kThreads, 4)
         if (g == 0) posw[dst] = surv_pos[r];
       }
       __syncthreads();
-      const int32_t new_id = ids_new[sq];
-      bool new_is_sep = false;
+      bool new_is_sep = false;  // thread 0 (tid < CPR) holds the id
       for (int x = 0; x < args.sids.n; ++x) new_is_sep |= (new_id == args.sids.ids[x]);
-      for (int u = tid; u < CPR; u += kThreads) {
-        *reinterpret_cast<uint4*>(kh + (size_t)new_slot * D + 8 * u) =
-            *reinterpret_cast<const uint4*>(k_new + mh * D + 8 * u);
-        *reinterpret_cast<uint4*>(vh + (size_t)new_slot * D + 8 * u) =
-            *reinterpret_cast<const uint4*>(v_new + mh * D + 8 * u);
+      if (tid < CPR) {
+        *reinterpret_cast<uint4*>(kh + (size_t)new_slot * D + 8 * tid) = nk;
+        *reinterpret_cast<uint4*>(vh + (size_t)new_slot * D + 8 * tid) = nvv;
       }
       if (tid == 0) {
         sepw[new_slot] = new_is_sep ? 1 : 0;
@@ -709,8 +800,10 @@ __global__ void __launch_bounds__(kThreads, 4)
     }
   }
   // every CTA has read the partials it needs before any shared memory goes away
-  cluster_arrive();
-  cluster_wait();
+  if (split > 1) {
+    cluster_arrive();
+    cluster_wait();
+  }
 }
 
 int pick_split(int S, int Hkv, int c) {
@@ -725,11 +818,17 @@ template <int D, int G>
 cudaError_t launch_step_t(const CachePtrs& cp, StepArgs args, const void* q, const void* k_new,
                           const void* v_new, const int32_t* ids_new, void* out, int* status,
                           cudaStream_t stream) {
-  const size_t smem = step_smem<D, G>(args.s).total;
+  const size_t smem = step_smem<D, G>(args.s, args.c).total;
   if (smem > 48 * 1024) {
     const cudaError_t e = cudaFuncSetAttribute(
         cache_step_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+  }
+  if (args.split == 1) {  // one CTA per (sequence, kv head): no cluster
+    cache_step_kernel<D, G><<<dim3(1, args.Hkv, args.S), kThreads, smem, stream>>>(
+        cp, args, static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k_new),
+        static_cast<const uint16_t*>(v_new), ids_new, static_cast<uint16_t*>(out), status);
+    return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(args.split, args.Hkv, args.S);
@@ -923,6 +1022,16 @@ std::vector<float2> rope_table(const sep_cache_params* p, int rows) {
   return t;
 }
 
+// inv_freq_i = theta^(-2i/d) as float32, the per-frequency rate the decode
+// kernel turns into (cos, sin) at each entry's rank.
+std::vector<float> inv_freqs(const sep_cache_params* p) {
+  std::vector<float> f(p->d / 2);
+  for (int i = 0; i < p->d / 2; ++i)
+    f[i] = static_cast<float>(pow((double)theta_of(p), -2.0 * i / p->d));
+  return f;
+}
+
+
 size_t export_bytes(const sep_cache_params* p) {
   return sizeof(int32_t) * 8 + (size_t)p->S * sizeof(int32_t) * 8 +
          (size_t)p->S * p->c * sizeof(int32_t) + (size_t)p->S * p->c +
@@ -950,8 +1059,11 @@ SEP_API sep_status sep_cache_init(const sep_cache_params* p, void* cache_buf, si
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const std::vector<float2> tab = rope_table(p, l.rope_rows);
   if (cudaMemsetAsync(cache_buf, 0, l.total, s) != cudaSuccess) return SEP_ERR_CUDA;
+  const std::vector<float> invf = inv_freqs(p);
   if (cudaMemcpyAsync(static_cast<char*>(cache_buf) + l.rope, tab.data(),
-                      tab.size() * sizeof(float2), cudaMemcpyHostToDevice, s) != cudaSuccess)
+                      tab.size() * sizeof(float2), cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(static_cast<char*>(cache_buf) + l.invf, invf.data(),
+                      invf.size() * sizeof(float), cudaMemcpyHostToDevice, s) != cudaSuccess)
     return SEP_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return SEP_ERR_CUDA;
   return SEP_OK;
@@ -1142,6 +1254,8 @@ SEP_API sep_status sep_cache_import(const sep_cache_params* p, void* cache_buf,
   hc.raw.assign(hc.l.total, 0);
   const std::vector<float2> tab = rope_table(p, hc.l.rope_rows);
   memcpy(hc.raw.data() + hc.l.rope, tab.data(), tab.size() * sizeof(float2));
+  const std::vector<float> invf = inv_freqs(p);
+  memcpy(hc.raw.data() + hc.l.invf, invf.data(), invf.size() * sizeof(float));
   const int ring = p->c - p->a, NSL = hc.l.NSL, HD = p->Hkv * p->d;
   for (int sq = 0; sq < p->S; ++sq) {
     const int32_t* cnt = im.counts + 8 * sq;
