@@ -39,9 +39,12 @@ struct SeqRec {
   int len, row0, tile0, pad;
 };
 
+// Tokens of one scan tile of the index kernel (one CTA per tile).
+constexpr int kScanTile = 8192;
+
 struct IndexLayout {
-  size_t header, seq, keep_prefix, keep_pos, keep_count, blocks, keep_bits, total;
-  int T, nwords;
+  size_t header, seq, keep_prefix, keep_pos, keep_count, blocks, keep_bits, scan, total;
+  int T, nwords, ntiles;
 };
 
 inline IndexLayout index_layout(int B, int L, int block_m) {
@@ -63,6 +66,11 @@ inline IndexLayout index_layout(int B, int L, int block_m) {
   off = align_up(off + sizeof(int32_t) * (size_t)B * l.T * 4, 256);
   l.keep_bits = off;
   off = align_up(off + sizeof(uint32_t) * (size_t)B * l.nwords, 256);
+  // scratch of the index kernel's scan: a tile ticket (first 256 bytes),
+  // then one status word per (sequence, scan tile); zeroed before each build
+  l.ntiles = (L + kScanTile - 1) / kScanTile;
+  l.scan = off;
+  off = align_up(off + 256 + sizeof(unsigned long long) * (size_t)B * l.ntiles, 256);
   l.total = off;
   return l;
 }
@@ -75,6 +83,8 @@ struct IndexPtrs {
   int32_t* keep_count;
   int32_t* blocks;
   uint32_t* keep_bits;
+  unsigned int* scan_ticket;
+  unsigned long long* scan_state;
 };
 
 inline IndexPtrs index_ptrs(void* buf, const IndexLayout& l) {
@@ -87,6 +97,8 @@ inline IndexPtrs index_ptrs(void* buf, const IndexLayout& l) {
   r.keep_count = reinterpret_cast<int32_t*>(p + l.keep_count);
   r.blocks = reinterpret_cast<int32_t*>(p + l.blocks);
   r.keep_bits = reinterpret_cast<uint32_t*>(p + l.keep_bits);
+  r.scan_ticket = reinterpret_cast<unsigned int*>(p + l.scan);
+  r.scan_state = reinterpret_cast<unsigned long long*>(p + l.scan + 256);
   return r;
 }
 
