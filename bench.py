@@ -877,9 +877,10 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["all", "train", "decode"], default="all",
+    ap.add_argument("--only", choices=["all", "train", "decode", "prefill", "index"],
+                    default="all",
                     help="train: the training step alone (no e2e, decode or prefill legs); "
-                         "decode: the streaming-decode leg alone")
+                         "decode / prefill / index: that leg alone (profiling runs)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
     rank = int(os.environ.get("RANK", "0"))
@@ -896,10 +897,15 @@ def main(argv=None):
         import torch.distributed as dist
         torch.cuda.set_device(device)
         dist.init_process_group("nccl", device_id=device)
-    if args.only == "decode":
+    if args.only in ("decode", "prefill", "index"):
         torch.cuda.set_device(device)
         flush = L2Flush(device)
-        line = run_decode(args, rank, device, flush, load_peaks())
+        if args.only == "decode":
+            line = run_decode(args, rank, device, flush, load_peaks())
+        elif args.only == "prefill":
+            line = run_prefill(args, rank, device, flush, load_peaks())
+        else:
+            line = run_index_scaling(args, rank, device, flush)
     else:
         line = run_ours(args, rank, world, device)
     if rank == 0:

@@ -535,7 +535,6 @@ __global__ void __launch_bounds__(kThreads, 4)
 #pragma unroll
           for (int sl = 0; sl < NLO; ++sl) {
             uint32_t alo[2][2], ahi[2][2];  // [entry g / g+8][dims +0/+1, +2/+3]
-#pragma unroll
             // (cos, sin) of freqs LD t + 4 sl + 0..3 at entry g's rank, and
             // at entry g+8's (8 ranks on: the angle-addition formulas with
             // (cos, sin)(8 theta_i), row 8 of the table)
