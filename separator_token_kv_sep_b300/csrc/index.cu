@@ -42,8 +42,7 @@ namespace sep {
 namespace {
 
 constexpr int kThreads = 512;
-constexpr int kPerThread = 16;
-static_assert(kThreads * kPerThread == kScanTile, "16 tokens per thread");
+static_assert(kThreads * 16 == kScanTile, "16 tokens per thread in a full scan tile");
 
 // status word of a (sequence, scan tile): flag in bits 62-63, count below
 constexpr unsigned long long kAggregate = 1ull << 62, kInclusive = 2ull << 62;
@@ -58,13 +57,19 @@ __device__ __forceinline__ unsigned long long ld_acquire(const unsigned long lon
   return v;
 }
 
+// PER tokens per thread: 16 for rows longer than 2048 tokens (scan tiles of
+// kScanTile), 4 for rows of at most 2048 (one tile, four times the active
+// threads).
+template <int PER>
 __global__ void __launch_bounds__(kThreads)
     build_index_kernel(const int32_t* __restrict__ ids, const int32_t* __restrict__ cu,
                        int total, int B, int L, SepIdList sids, int a, int n, int block_m,
                        int fix_delta, IndexPtrs ptrs, int* status) {
   // rows of at most one scan tile need no ticket, no look-back and no
   // scratch: tile (b, 0) is block b
-  const bool multi = L > kScanTile;
+  constexpr int kPerThread = PER;
+  static_assert(32 % PER == 0 && PER % 4 == 0, "whole words of keep bits per lane group");
+  const bool multi = L > kScanTile;  // (only with PER == 16: the launch guarantees it)
   __shared__ int warp_sums[kThreads / 32];
   __shared__ int tile_total, prefix_sh, tiles_before;
   __shared__ unsigned int ticket;
@@ -223,15 +228,38 @@ __global__ void __launch_bounds__(kThreads)
   // the warp's 512, whose owner thread and bit come by shuffle), so each
   // store covers 128 contiguous bytes; keep positions go through shared
   // memory and leave in order.
+  // The block record of query tile t needs keep_prefix at its window start
+  // W(t) = max(0, 128 t - n + 1): the lane that computes keep_prefix of a
+  // token that is some W(t) writes that record (token 0 those of every tile
+  // whose window starts at 0).
+  const int Tb = (len + block_m - 1) / block_m;
+  int32_t* blk = ptrs.blocks + (size_t)b * T * 4;
+  auto record = [&](int t, int W, int kv) {
+    int4 rec;
+    rec.x = kv;
+    rec.y = W;
+    rec.z = min(len, t * block_m + block_m);
+    rec.w = (W < a) ? 1 : 0;
+    *reinterpret_cast<int4*>(blk + 4 * t) = rec;
+  };
   {
     const int wbase = base + warp * 32 * kPerThread;  // the warp's first token
 #pragma unroll 4
     for (int m = 0; m < kPerThread; ++m) {
-      const int owner = 2 * m + (lane >> 4), bit = lane & 15;
+      const int owner = (32 * m + lane) / PER, bit = (32 * m + lane) % PER;
       const uint32_t onib = __shfl_sync(0xffffffffu, nib, owner);
       const int olpos = __shfl_sync(0xffffffffu, lpos, owner);
       const int j = wbase + 32 * m + lane;
-      if (j < len) kp[j] = prefix + olpos + __popc(onib & ((1u << bit) - 1u));
+      if (j < len) {
+        const int kv = prefix + olpos + __popc(onib & ((1u << bit) - 1u));
+        kp[j] = kv;
+        if (j == 0) {
+          for (int t = 0; t < Tb && (long long)t * block_m - n + 1 <= 0; ++t) record(t, 0, kv);
+        } else if (((long long)j + n - 1) % block_m == 0) {
+          const long long t = ((long long)j + n - 1) / block_m;
+          if (t < Tb) record(static_cast<int>(t), j, kv);
+        }
+      }
     }
   }
 #pragma unroll
@@ -239,33 +267,15 @@ __global__ void __launch_bounds__(kThreads)
     if ((nib >> e) & 1u) kposbuf[lpos] = j0 + e;
     lpos += (nib >> e) & 1u;
   }
-  // 2 lanes x 16 tokens = one word of the keep bitmask
-  const uint32_t word = nib | (__shfl_xor_sync(0xffffffffu, nib, 1) << 16);
+  // 32 / PER lanes x PER tokens = one word of the keep bitmask
+  constexpr int LPW = 32 / PER;
+  uint32_t word = nib << (PER * (lane % LPW));
+#pragma unroll
+  for (int off = 1; off < LPW; off <<= 1) word |= __shfl_xor_sync(0xffffffffu, word, off);
   const int widx = j0 >> 5;
-  if ((lane & 1) == 0 && widx < nwords) bits_out[widx] = word;
-  __syncthreads();  // kposbuf and this tile's keep_prefix are complete
+  if (lane % LPW == 0 && widx < nwords) bits_out[widx] = word;
+  __syncthreads();  // kposbuf is complete
   for (int i = tid; i < tile_total; i += kThreads) kpos[prefix + i] = kposbuf[i];
-
-  // ---- block records of the query tiles whose window start lies in this
-  // tile (W(t) = max(0, 128 t - n + 1)); tiles past the sequence are empty
-  const int Tb = (len + block_m - 1) / block_m;
-  int32_t* blk = ptrs.blocks + (size_t)b * T * 4;
-  {
-    const long long lo = k == 0 ? 0 : ((long long)base + n - 1 + block_m - 1) / block_m;
-    const long long hi = ((long long)base + kScanTile + n - 1 + block_m - 1) / block_m;
-    const int t_lo = static_cast<int>(lo < Tb ? lo : Tb);
-    const int t_hi = static_cast<int>(hi < Tb ? hi : Tb);
-    for (int t = t_lo + tid; t < t_hi; t += kThreads) {
-      const int i0 = t * block_m;
-      const int W = max(0, i0 - n + 1);
-      int4 rec;
-      rec.x = kp[W];  // written above by this CTA (W lies in its tile)
-      rec.y = W;
-      rec.z = min(len, i0 + block_m);
-      rec.w = (W < a) ? 1 : 0;
-      *reinterpret_cast<int4*>(blk + 4 * t) = rec;
-    }
-  }
 
   // ---- per sequence: the last tile writes the count and the padding; the
   // first one the sequence record (and the header, for sequence 0)
@@ -310,8 +320,12 @@ int launch_build_index(const int32_t* ids, const int32_t* cu, int total, int B, 
       e = cudaMemsetAsync(ptrs.keep_pos, 0xff, sizeof(int32_t) * (size_t)B * L, s);
     if (e != cudaSuccess) return static_cast<int>(e);
   }
-  build_index_kernel<<<B * ntiles, kThreads, 0, s>>>(ids, cu, total, B, L, sids, a, n, block_m,
-                                                     fix_delta, ptrs, status);
+  if (L <= kThreads * 4)
+    build_index_kernel<4><<<B, kThreads, 0, s>>>(ids, cu, total, B, L, sids, a, n, block_m,
+                                                 fix_delta, ptrs, status);
+  else
+    build_index_kernel<16><<<B * ntiles, kThreads, 0, s>>>(ids, cu, total, B, L, sids, a, n,
+                                                           block_m, fix_delta, ptrs, status);
   return static_cast<int>(cudaGetLastError());
 }
 
