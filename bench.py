@@ -240,12 +240,12 @@ def run_ours(args, rank, world, device):
     lse = torch.empty((B, Hq, L), dtype=torch.float32, device=device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     # step boundaries, and the per-kernel marks the library records through
-    # sep_profile_events (fwd: gather | attention; bwd: prep | dK/dV | dQ |
-    # scatter)
+    # sep_profile_events (fwd: gather | attention; bwd: prep | dK/dV | dQ
+    # with the keep-row dK/dV writes)
     Ev = lambda: torch.cuda.Event(enable_timing=True, external=True)  # noqa: E731
     step_ev = [Ev(), Ev()]
     fwd_ev = [Ev() for _ in range(3)]
-    bwd_ev = [Ev() for _ in range(5)]
+    bwd_ev = [Ev() for _ in range(4)]
     for e in step_ev + fwd_ev + bwd_ev:  # create the CUDA events outside the capture
         e.record()
     torch.cuda.synchronize()
@@ -268,21 +268,28 @@ def run_ours(args, rank, world, device):
         train_step()
     torch.cuda.synchronize()
     assert api.sep_get_device_status() == 0
+    # the timed graph holds the step's launches only; a second graph with the
+    # per-kernel marks gives the breakdown (event nodes between the kernels
+    # would lengthen the timed step)
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
+        train_step()
+    graph_m = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_m):
         train_step(mark=True)
     for _ in range(max(3, args.warmup)):
         flush()
         graph.replay()
+        flush()
+        graph_m.replay()
     torch.cuda.synchronize()
 
-    kern_names = ["index", "fwd_gather", "fwd_attn", "bwd_prep", "bwd_kv", "bwd_dq",
-                  "bwd_scatter"]
+    kern_names = ["index", "fwd_gather", "fwd_attn", "bwd_prep", "bwd_kv", "bwd_dq"]
     marks = [step_ev[0], fwd_ev[0], fwd_ev[1], fwd_ev[2], bwd_ev[0], bwd_ev[1], bwd_ev[2],
-             bwd_ev[3], bwd_ev[4]]
+             bwd_ev[3]]
     # index: step start -> fwd gather; fwd attn end -> bwd prep is launch glue
     spans = {"index": (0, 1), "fwd_gather": (1, 2), "fwd_attn": (2, 3), "bwd_prep": (4, 5),
-             "bwd_kv": (5, 6), "bwd_dq": (6, 7), "bwd_scatter": (7, 8)}
+             "bwd_kv": (5, 6), "bwd_dq": (6, 7)}
     sampler = ClockSampler(device.index if device.index is not None else 0)
     t_step = []
     t_kern = {n: [] for n in kern_names}
@@ -290,19 +297,28 @@ def run_ours(args, rank, world, device):
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize()
+        stream = torch.cuda.current_stream()
         for _ in range(args.steps):
             flush()
+            step_ev[0].record(stream)
             graph.replay()
+            step_ev[1].record(stream)
             torch.cuda.synchronize()
             t_step.append(step_ev[0].elapsed_time(step_ev[1]))
-            for n in kern_names:
-                a_, b_ = spans[n]
-                t_kern[n].append(marks[a_].elapsed_time(marks[b_]))
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
         total_ms = sum(t_step)
         total_ms = max_over_ranks(total_ms, world)
+        t_marked = []
+        for _ in range(args.steps):  # the breakdown, outside the timed steps
+            flush()
+            graph_m.replay()
+            torch.cuda.synchronize()
+            t_marked.append(step_ev[0].elapsed_time(step_ev[1]))
+            for n in kern_names:
+                a_, b_ = spans[n]
+                t_kern[n].append(marks[a_].elapsed_time(marks[b_]))
         decode = run_decode(args, rank, device, flush, peaks) if args.only == "all" else None
         prefill = run_prefill(args, rank, device, flush, peaks) if args.only == "all" else None
         variants = run_variants(args, rank, device, flush, peaks) if args.only == "all" else None
@@ -316,7 +332,7 @@ def run_ours(args, rank, world, device):
     mean = lambda xs: sum(xs) / len(xs)  # noqa: E731
     kern_ms = {n: mean(t_kern[n]) for n in kern_names}
     fwd_ms = kern_ms["fwd_gather"] + kern_ms["fwd_attn"]
-    bwd_ms = sum(kern_ms[n] for n in ("bwd_prep", "bwd_kv", "bwd_dq", "bwd_scatter"))
+    bwd_ms = sum(kern_ms[n] for n in ("bwd_prep", "bwd_kv", "bwd_dq"))
     fwd_tf = fwd_flops / (fwd_ms * 1e-3) / 1e12
     bwd_tf = bwd_flops / (bwd_ms * 1e-3) / 1e12
     # Algorithmic FLOPs of each tensor-core kernel over the visited pairs it
@@ -345,6 +361,7 @@ def run_ours(args, rank, world, device):
                    "visited_pairs_per_head": pairs, "visited_over_causal":
                        round(pairs / (B * L * (L + 1) / 2), 4),
                    "l2": L2_NOTE, "parallelism": f"replicas x{world}"},
+        "ms_per_step_with_marks": round(sum(t_marked) / len(t_marked), 5),
         "phases_ms": {"fwd": round(fwd_ms, 5), "bwd": round(bwd_ms, 5),
                       "fwd_tflops": round(fwd_tf, 2), "bwd_tflops": round(bwd_tf, 2)},
         "kernels": kernels,
@@ -355,13 +372,15 @@ def run_ours(args, rank, world, device):
             "frac_of_sustained": round(dom_tf / peaks["bf16_tflops_sustained"], 4)
             if peaks.get("bf16_tflops_sustained") else None,
             "peak_source": peaks["source"] + " (burst bf16; of measured)",
-            "timing": "CUDA events recorded around the kernel inside the timed graph",
+            "timing": "CUDA events recorded around the kernel inside a replay of the same "
+                      "step captured with per-kernel event nodes",
             "traffic": DRAM_TRAFFIC_BYTES.get(dom),
             "traffic_unit": "bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum, "
                             "one ncu capture of this kernel at this workload)"},
         "e2e": e2e,
         "clocks": clocks,
-        "gpu_launches": 7 * args.steps,
+        # index, keep gather, forward; prep, dK/dV, dQ (with the keep rows)
+        "gpu_launches": 6 * args.steps,
         "decode": decode,
         "prefill": prefill,
         "mask_variants": variants,

@@ -11,7 +11,7 @@
 //
 // Every visible pair (i, j) belongs to exactly one of the forward's two key
 // sources (gathered keep tokens before the query tile's window, or the dense
-// band), and the backward keeps that split.  Four launches:
+// band), and the backward keeps that split.  Three launches:
 //   bwd_prep_kernel     the keep-token K/V gather, zeroed fp32 keep-token
 //                       gradient accumulators, the per-row stats
 //                       (-LSE log2 e, -Delta) and, in CTA 0, the dK/dV work
@@ -28,9 +28,10 @@
 //                       written as bf16 at once.
 //   bwd_dq_persistent   query-major dQ, one CTA per SM: the forward's
 //                       traversal, S = Q K^T and dP = dO V^T into TMEM, dS to
-//                       shared memory, dQ += dS K.
-//   bwd_keep_scatter_kernel  the keep tokens' dK / dV rows from the
-//                       accumulators.
+//                       shared memory, dQ += dS K.  Its elementwise warps
+//                       first write the keep tokens' dK / dV rows from the
+//                       finished accumulators, while the first item's copies
+//                       and products are in flight.
 // The MMA issuers run warp-uniform, with one elected lane issuing.
 // All waits are bounded; on expiry a kernel records SEP_ERR_TIMEOUT, drains
 // its copies and MMAs, frees TMEM and returns.
@@ -82,7 +83,7 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
 constexpr int kItemKeep = 0, kItemDense = 1;
 
 struct BwdSchedule {  // header of the schedule region; int4 items follow
-  int n_items, n_keep, pad0, pad1;
+  int n_items, n_keep, max_count, pad;  // max_count: the largest keep count
 };
 
 __host__ __device__ inline size_t bwd_max_items(int B, int Hkv, int T) {
@@ -136,8 +137,15 @@ __device__ __forceinline__ bool header_matches(const IndexHeader& h, const Geom&
 __device__ void build_bwd_schedule(IndexPtrs idx, const Geom& geo, uint64_t full_groups,
                                    BwdSchedule* sched, int4* items) {
   __shared__ int sh[33];
+  __shared__ int s_maxc;
   const int B = geo.B, Hkv = geo.Hkv, T = geo.T;
   int total = 0;
+  if (threadIdx.x == 0) s_maxc = 0;
+  __syncthreads();
+  for (int b = threadIdx.x; b < B; b += blockDim.x) {
+    const SeqRec sr = idx.seq[b];
+    if (seq_ok(sr, geo)) atomicMax(&s_maxc, min(max(idx.keep_count[b], 0), sr.len));
+  }
   // kv groups with full causal attention have no keep items, and every
   // query tile from the key tile on sees their dense key tiles
   int nsep = 0;
@@ -211,9 +219,11 @@ __device__ void build_bwd_schedule(IndexPtrs idx, const Geom& geo, uint64_t full
     }
     total += sum * Hkv;
   }
+  __syncthreads();
   if (threadIdx.x == 0) {
     sched->n_items = total;
     sched->n_keep = n_keep;
+    sched->max_count = s_maxc;
   }
 }
 
@@ -326,7 +336,7 @@ struct KvCfg {
   // +64); accumulator buffer b: dV at TM_ACC + 2bD, dK at TM_ACC + 2bD + D
   static constexpr int TM_ACC = 256;
   static constexpr int TM_COLS = 512;
-  static_assert(SMEM + 16 * kCtaItems + 256 <= 227 * 1024, "shared memory");
+  static_assert(SMEM + 68 * kCtaItems + 256 <= 227 * 1024, "shared memory");
   static_assert(TM_ACC + ACB * 2 * D <= TM_COLS, "tensor memory");
 };
 
@@ -368,12 +378,49 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
   const int n_win = hdr.n;
-  // this CTA's items (i = blockIdx.x + k * gridDim.x), read once; items past
-  // kCtaItems are read from global memory
+  // this CTA's items (i = blockIdx.x + k * gridDim.x) and what every role
+  // needs of them, read once: the sequence record with its keep count, the
+  // block record of the first query tile and, for a dense key tile, its 128
+  // keep bits and the keep prefix at its first key.  Items past kCtaItems
+  // read the same from global memory when they start.
   __shared__ int4 s_items[kCtaItems];
+  __shared__ int4 s_seq[kCtaItems];     // {len, row0, tile0, keep count}
+  __shared__ int4 s_blk0[kCtaItems];
+  __shared__ uint4 s_kbits[kCtaItems];
+  __shared__ int s_kpre[kCtaItems];
+  auto item_seq = [&](int4 it) -> int4 {
+    const int b = it.y / Hkv;
+    const SeqRec sr = idx.seq[b];
+    return make_int4(sr.len, sr.row0, sr.tile0, min(max(idx.keep_count[b], 0), sr.len));
+  };
+  auto item_blk0 = [&](int4 it, int len) -> int4 {
+    const int b = it.y / Hkv, g = it.y % Hkv, t0 = it.w >> 16;
+    return group_full(full_groups, g)
+               ? full_block_record(t0, len)
+               : *reinterpret_cast<const int4*>(idx.blocks + ((size_t)b * T + t0) * 4);
+  };
   for (int x = threadIdx.x; x < kCtaItems; x += blockDim.x) {
     const int i = static_cast<int>(blockIdx.x) + x * static_cast<int>(gridDim.x);
-    if (i < n_items) s_items[x] = items[i];
+    if (i < n_items) {
+      const int4 it = items[i];
+      const int4 sq = item_seq(it);
+      s_items[x] = it;
+      s_seq[x] = sq;
+      s_blk0[x] = item_blk0(it, sq.x);
+      uint4 kb = make_uint4(0u, 0u, 0u, 0u);
+      int kpre = 0;
+      if (it.x == kItemDense) {
+        const int b = it.y / Hkv, w0 = it.z >> 5;
+        const uint32_t* bw = idx.keep_bits + (size_t)b * hdr.nwords;
+        kb.x = w0 < hdr.nwords ? bw[w0] : 0u;
+        kb.y = w0 + 1 < hdr.nwords ? bw[w0 + 1] : 0u;
+        kb.z = w0 + 2 < hdr.nwords ? bw[w0 + 2] : 0u;
+        kb.w = w0 + 3 < hdr.nwords ? bw[w0 + 3] : 0u;
+        kpre = idx.keep_prefix[(size_t)b * (L + 1) + it.z];
+      }
+      s_kbits[x] = kb;
+      s_kpre[x] = kpre;
+    }
   }
 
   if (threadIdx.x == 0) {
@@ -409,10 +456,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // sequences only, whose records {len, row0, tile0} are read here
   struct Item {
     int kind, b, g, row0, t0, nt;
-    int len, srow0, tile0;
+    int len, srow0, tile0, count;
   };
   auto item_at = [&](int i, int k) -> Item {  // item i, the k-th of this CTA
     const int4 it = k < kCtaItems ? s_items[k] : items[i];
+    const int4 sq = k < kCtaItems ? s_seq[k] : item_seq(it);
     Item r;
     r.kind = it.x;
     r.b = it.y / Hkv;
@@ -420,10 +468,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     r.row0 = it.z;
     r.t0 = it.w >> 16;
     r.nt = (it.w & 0xffff) - r.t0;
-    const SeqRec sr = idx.seq[r.b];
-    r.len = sr.len;
-    r.srow0 = sr.row0;
-    r.tile0 = sr.tile0;
+    r.len = sq.x;
+    r.srow0 = sq.y;
+    r.tile0 = sq.z;
+    r.count = sq.w;
     return r;
   };
 
@@ -668,16 +716,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Item it = item_at(i, k);
       const bool keep = it.kind == kItemKeep;
       const int len = it.len;
-      const int count = min(max(idx.keep_count[it.b], 0), len);
+      const int count = it.count;
       const int32_t* blocks = idx.blocks + (size_t)it.b * T * 4;
       const int j = it.row0 + r;  // KEEP: keep index; DENSE: key position
-      // a dense row's keep bit and keep prefix, loaded together
+      // a dense row's keep bit and keep prefix (from the staged keep bits of
+      // the key tile when the item is staged)
       const bool dense_row = !keep && j < len;
-      const uint32_t kbw = dense_row ? idx.keep_bits[(size_t)it.b * hdr.nwords + (j >> 5)] : 0u;
-      const int kpre = dense_row ? idx.keep_prefix[(size_t)it.b * (L + 1) + j] : 0;
+      uint32_t kbw = 0u;
+      int kpre = 0;
+      if (dense_row) {
+        if (k < kCtaItems) {
+          const uint32_t* wb = reinterpret_cast<const uint32_t*>(&s_kbits[k]);
+          kpre = s_kpre[k];
+#pragma unroll
+          for (int q = 0; q < 3; ++q)
+            if (q < (r >> 5)) kpre += __popc(wb[q]);
+          kbw = wb[r >> 5];
+          kpre += __popc(kbw & ((1u << (j & 31)) - 1u));
+        } else {
+          kbw = idx.keep_bits[(size_t)it.b * hdr.nwords + (j >> 5)];
+          kpre = idx.keep_prefix[(size_t)it.b * (L + 1) + j];
+        }
+      }
       const bool keep_j = (kbw >> (j & 31)) & 1u;
       // this item's epilogue: KEEP rows and DENSE keep tokens add into the
-      // fp32 keep accumulators (written to dK/dV by the scatter kernel);
+      // fp32 keep accumulators (written to dK/dV by the dQ kernel);
       // other DENSE rows are final
       Epi e;
       e.k = k;
@@ -696,7 +759,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto record = [&](int t2) {
         return full ? full_block_record(t2, len) : *reinterpret_cast<const int4*>(blocks + 4 * t2);
       };
-      int4 blk_next = record(it.t0);
+      int4 blk_next = k < kCtaItems ? s_blk0[k] : record(it.t0);
       for (int u = 0; u < nU; ++u) {
         const int ugl = ug + u;
         const int t = it.t0 + u % it.nt;
@@ -785,20 +848,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, C::TM_COLS);
 }
 
-// dK / dV rows of keep tokens from the fp32 accumulators (dK scaled).
-template <int D>
-__global__ void __launch_bounds__(256)
-    bwd_keep_scatter_kernel(IndexPtrs idx, const float4* __restrict__ dk_keep,
-                            const float4* __restrict__ dv_keep, __nv_bfloat16* __restrict__ dk,
-                            __nv_bfloat16* __restrict__ dv, Geom geo, float scale) {
-  const IndexHeader hdr = *idx.header;
-  if (!header_matches(hdr, geo)) return;
-  const int units = keep_units(geo.B, geo.Hkv, geo.L);
-  const int lane = threadIdx.x & 31;
-  for (int u = blockIdx.x * 8 + (threadIdx.x >> 5); u < units; u += gridDim.x * 8)
-    scatter_keep_unit<D>(idx, geo, dk_keep, dv_keep, dk, dv, scale, u, lane);
-}
-
 // ---------------------------------------------------------------------------
 // Query-major dQ, persistent: items are (batch, q head, query tile), longest
 // query tiles first, taken round-robin by one CTA per SM.
@@ -831,8 +880,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_kk,
                       const __grid_constant__ CUtensorMap tm_vk, IndexPtrs idx,
-                      const float2* __restrict__ stats,
-                      __nv_bfloat16* __restrict__ dq, Geom geo, float scale,
+                      const float2* __restrict__ stats, const BwdSchedule* __restrict__ sched,
+                      const float4* __restrict__ dk_keep, const float4* __restrict__ dv_keep,
+                      __nv_bfloat16* __restrict__ dq, __nv_bfloat16* __restrict__ dk,
+                      __nv_bfloat16* __restrict__ dv, Geom geo, float scale,
                       float scale_log2, uint64_t full_groups, int* status) {
   using C = DqCfg<D>;
   constexpr int QB = C::QB, NST = C::NST;
@@ -1089,6 +1140,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------------------------------------------------- elementwise
+    // First the keep tokens' dK / dV rows from the fp32 accumulators, which
+    // the dK/dV kernel has finished: one warp per 16-row unit over every
+    // elementwise warp of the grid, only the units below the largest keep
+    // count, while the first item's copies and products are in flight.
+    {
+      const int max_count = min(max(sched->max_count, 0), geo.L);
+      const int units = geo.B * Hkv * ((max_count + kKeepUnitRows - 1) / kKeepUnitRows);
+      const int nw = static_cast<int>(gridDim.x) * (kEwThreads / 32);
+      for (int u = static_cast<int>(blockIdx.x) * (kEwThreads / 32) + (warp - 2); u < units;
+           u += nw)
+        scatter_keep_unit<D>(idx, geo, dk_keep, dv_keep, dk, dv, scale, u, lane);
+    }
     // Two warpgroups share every tile: warps 2-5 take key columns 0-63 and
     // warps 6-9 columns 64-127 of the same 128 query rows; in the epilogue
     // each writes half of the dQ columns.
@@ -1298,16 +1361,14 @@ int launch_bwd_impl(IndexPtrs idx, const void* q, const void* k, const void* v, 
                                        w.stats, w.dk_keep, w.dv_keep, dkb, dvb, geo, scale,
                                        scale_log2, full_groups, status);
   profile_mark(2, s);
+  // the dQ kernel also writes the keep tokens' dK / dV rows
   const int dq_items = geo.B * geo.Hq * geo.T;
   dq_k<<<dq_items < sms ? dq_items : sms, kThreads, QC::SMEM, s>>>(
-      mq, mdo, mk, mv, mkk, mvk, idx, w.stats, static_cast<__nv_bfloat16*>(dq), geo, scale,
-      scale_log2, full_groups, status);
-  profile_mark(3, s);
-  bwd_keep_scatter_kernel<D><<<keep_pass_ctas(keep_units(geo.B, geo.Hkv, geo.L), sms), 256, 0, s>>>(
-      idx, reinterpret_cast<const float4*>(w.dk_keep), reinterpret_cast<const float4*>(w.dv_keep),
-      dkb, dvb, geo, scale);
+      mq, mdo, mk, mv, mkk, mvk, idx, w.stats, w.sched,
+      reinterpret_cast<const float4*>(w.dk_keep), reinterpret_cast<const float4*>(w.dv_keep),
+      static_cast<__nv_bfloat16*>(dq), dkb, dvb, geo, scale, scale_log2, full_groups, status);
   const cudaError_t err = cudaGetLastError();
-  profile_mark(4, s);
+  profile_mark(3, s);
   return static_cast<int>(err);
 }
 
