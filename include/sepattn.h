@@ -82,14 +82,15 @@ size_t sep_index_bytes(int B, int L, int block_m);
  *   n          neighbour window, >= 1; row i's window is [i-n+1, i].
  *   block_m    query-tile height of the block lists; must be SEP_BLOCK_M.
  *   index_buf  device buffer of index_bytes >= sep_index_bytes(B, L, block_m),
- *              256-byte aligned, written entirely by this call.  Its fields
+ *              256-byte aligned, written by this call (every field below
+ *              but the keep_pos entries past each count).  Its fields
  *              are reached with sep_index_views(); the attention calls read
  *              a, n, B and L from it.
  *
  * Fields (all int32 unless stated):
  *   keep_prefix [B, L+1]   number of keep tokens in [0, j)
- *   keep_pos    [B, L]     ascending positions of keep tokens, entries
- *                          >= keep_count[b] set to -1
+ *   keep_pos    [B, L]     ascending positions of keep tokens; only the
+ *                          entries below keep_count[b] are written
  *   keep_count  [B]
  *   blocks      [B, T, 4]  T = ceil(L / block_m); for tile t with first row
  *                          i0 = t*block_m and W = max(0, i0-n+1):
@@ -137,8 +138,8 @@ sep_status sep_build_index_fixed(int B, int L, int a, int n, int delta, int bloc
  *   other arguments as sep_build_index.
  * The fields (sep_index_views with L = max_len) hold, for each sequence, what
  * sep_build_index gives for that sequence alone in local positions, padded:
- * keep_prefix[b][j] = keep_count[b] for j >= len_b, keep_pos -1 past the
- * count, empty block records {0, 0, 0, 0} for tiles at or past len_b, zero
+ * keep_prefix[b][j] = keep_count[b] for j >= len_b, keep_pos written below
+ * the count only, empty block records {0, 0, 0, 0} for tiles at or past len_b, zero
  * keep bits past len_b.
  * Errors: SEP_ERR_INVALID_ARG, SEP_ERR_UNSUPPORTED, SEP_ERR_WORKSPACE,
  * SEP_ERR_CUDA; device: SEP_ERR_DEVICE_BOUNDS if cu_seqlens is not a valid
@@ -434,8 +435,8 @@ sep_status sep_get_device_status(void);
  *                        attention kernel, [2] after it.
  *   sep_attn_bwd:        [0] before the prep kernel (keep gather, Delta and
  *                        the dK/dV work schedule), [1] before the dK/dV
- *                        kernel, [2] before the dQ kernel, [3] before the
- *                        keep-row scatter, [4] after it.
+ *                        kernel, [2] before the dQ kernel (which also writes
+ *                        the keep tokens' dK / dV rows), [3] after it.
  * Indices past n_events are skipped.  The handles stay owned by the caller
  * and must outlive their registration.
  * Errors: SEP_ERR_INVALID_ARG (n_events out of range, or events NULL with

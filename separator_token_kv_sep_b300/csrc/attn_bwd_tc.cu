@@ -297,6 +297,7 @@ __global__ void __launch_bounds__(kPrepThreads)
                     float4* __restrict__ dk_keep, float4* __restrict__ dv_keep,
                     uint64_t full_groups, BwdSchedule* __restrict__ sched,
                     int4* __restrict__ items) {
+  grid_dep_wait();
   const IndexHeader hdr = *idx.header;
   if (!header_matches(hdr, geo)) return;
   if (blockIdx.x == 0) {
@@ -327,14 +328,17 @@ struct KvCfg {
   static constexpr int KVB = D == 64 ? 2 : 1;   // K/V tile buffers
   static constexpr int NST = D == 64 ? 3 : 2;   // Q/dO ring stages
   static constexpr int ACB = D == 64 ? 2 : 1;   // dK/dV accumulator buffers in TMEM
+  // half-tile buffers in TMEM (three with one accumulator buffer at d = 64
+  // was measured slower: the epilogue then waits for the item's last MMAs)
+  static constexpr int NHB = 2;
   static constexpr int OFF_KV = 0;              // [KVB][K, V]
   static constexpr int OFF_Q = OFF_KV + KVB * 2 * TILE;
   static constexpr int OFF_DO = OFF_Q + NST * TILE;
   static constexpr int OFF_STAT = OFF_DO + NST * TILE;  // [NST][128] (-LSE log2, -Delta)
   static constexpr int SMEM = OFF_STAT + NST * 128 * 8 + 1024;
-  // TMEM: half-tile buffers h = 0, 1 at 128h (S^T / P^T, then dP^T / dS^T at
+  // TMEM: half-tile buffers x < NHB at 128x (S^T / P^T, then dP^T / dS^T at
   // +64); accumulator buffer b: dV at TM_ACC + 2bD, dK at TM_ACC + 2bD + D
-  static constexpr int TM_ACC = 256;
+  static constexpr int TM_ACC = 128 * NHB;
   static constexpr int TM_COLS = 512;
   static_assert(SMEM + 68 * kCtaItems + 256 <= 227 * 1024, "shared memory");
   static_assert(TM_ACC + ACB * 2 * D <= TM_COLS, "tensor memory");
@@ -354,12 +358,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                       __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, Geom geo,
                       float scale, float scale_log2, uint64_t full_groups, int* status) {
   using C = KvCfg<D>;
-  constexpr int KVB = C::KVB, NST = C::NST, ACB = C::ACB;
+  constexpr int KVB = C::KVB, NST = C::NST, ACB = C::ACB, NHB = C::NHB;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   __shared__ __align__(8) uint64_t kv_full[KVB], kv_empty[KVB], qd_full[NST], qd_empty[NST];
-  __shared__ __align__(8) uint64_t sd_full[2], ps_full[2], acc_full[ACB], acc_empty[ACB],
+  __shared__ __align__(8) uint64_t sd_full[NHB], ps_full[NHB], acc_full[ACB], acc_empty[ACB],
       mma_final;
   __shared__ uint32_t tmem_slot;
 
@@ -367,14 +371,41 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int T = geo.T, Hq = geo.Hq, Hkv = geo.Hkv, L = geo.L;
   const int G = Hq / Hkv;
 
-  const IndexHeader hdr = *idx.header;
-  if (!header_matches(hdr, geo)) {
-    if (threadIdx.x == 0) report(status, SEP_ERR_DEVICE_BOUNDS);
-    return;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < KVB; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+    }
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(&qd_full[i], 1);
+      mbar_init(&qd_empty[i], 1);
+    }
+    for (int i = 0; i < ACB; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], kEwThreads);
+    }
+    for (int x = 0; x < NHB; ++x) {
+      mbar_init(&sd_full[x], 1);
+      mbar_init(&ps_full[x], 128);
+    }
+    mbar_init(&mma_final, 1);
+    fence_mbar_init();
   }
+  if (warp == 1) {
+    tmem_alloc(&tmem_slot, C::TM_COLS);
+    tmem_relinquish();
+  }
+  // barriers and tensor memory are set up before waiting for the prep kernel
+  grid_dep_wait();
+  const IndexHeader hdr = *idx.header;
   const int n_items = sched->n_items;
-  if (n_items < 0 || (size_t)n_items > bwd_max_items(geo.B, Hkv, T)) {
+  if (!header_matches(hdr, geo) || n_items < 0 ||
+      (size_t)n_items > bwd_max_items(geo.B, Hkv, T)) {
     if (threadIdx.x == 0) report(status, SEP_ERR_DEVICE_BOUNDS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_slot, C::TM_COLS);
     return;
   }
   const int n_win = hdr.n;
@@ -423,30 +454,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < KVB; ++i) {
-      mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
-    }
-    for (int i = 0; i < NST; ++i) {
-      mbar_init(&qd_full[i], 1);
-      mbar_init(&qd_empty[i], 1);
-    }
-    for (int i = 0; i < ACB; ++i) {
-      mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], kEwThreads);
-    }
-    for (int x = 0; x < 2; ++x) {
-      mbar_init(&sd_full[x], 1);
-      mbar_init(&ps_full[x], 128);
-    }
-    mbar_init(&mma_final, 1);
-    fence_mbar_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(&tmem_slot, C::TM_COLS);
-    tmem_relinquish();
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -534,12 +541,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     // The unit of work is a half-tile: the 64 query columns h of one query
-    // tile u against the item's 128 keys.  Half h lives in TMEM buffer h:
-    // S^T at columns [128h, 128h+64), dP^T at [128h+64, 128h+128); the
-    // elementwise warpgroup h overwrites them with P^T and dS^T (packed
-    // bf16), which the dV / dK products then read from TMEM.  Order:
-    // S/dP(u,0), S/dP(u,1), then per half-tile j: dV/dK(j), S/dP(j+2) --
-    // the two warpgroups' chains interleave on the tensor pipe.
+    // tile u against the item's 128 keys, half-tile j = 2u + h of the CTA.
+    // It lives in TMEM buffer x = j % NHB: S^T at columns [128x, 128x+64),
+    // dP^T at [128x+64, 128x+128); the elementwise warpgroup h overwrites
+    // them with P^T and dS^T (packed bf16), which the dV / dK products then
+    // read from TMEM.  Order: S/dP of the first NHB half-tiles, then per
+    // half-tile j: dV/dK(j), S/dP(j+NHB) -- the two warpgroups' chains
+    // interleave on the tensor pipe.
     // The whole warp runs this loop; the elected lane issues.
     {
       const bool leader = elect_one();
@@ -586,7 +594,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t dk = dsc_kv + ((kb * 2 * C::TILE) >> 4), dv = dk + (C::TILE >> 4);
         const uint64_t qo = (st * C::TILE + 8192 * c.h) >> 4;  // query rows 64h .. 64h+63
         const uint64_t dq = dsc_q + qo, ddo = dsc_do + qo;
-        const uint32_t tb = tmem + 128 * c.h;
+        const int hb = (2 * c.ug + c.h) % NHB;  // the half-tile's TMEM buffer
+        const uint32_t tb = tmem + 128 * hb;
         if (leader) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
@@ -598,7 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t off = ((kk >> 2) * kChunk + (kk & 3) * 32) >> 4;
             umma_bf16_ss(tb + 64, dv + off, ddo + off, idesc_sd, kk > 0);
           }
-          umma_commit(&sd_full[c.h]);
+          umma_commit(&sd_full[hb]);
         }
         __syncwarp();
         return true;
@@ -607,11 +616,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       cur_load(cs);
       Cur ca = cs;  // next dV/dK to issue
       bool ok = true;
-      // S/dP run up to two half-tiles ahead of dV/dK, but not into an item
+      // S/dP run up to NHB half-tiles ahead of dV/dK, but not into an item
       // whose K/V buffer the current item still holds
       int ahead = 0;
       auto top_up = [&]() -> bool {
-        while (ahead < 2 && cs.i < n_items && cs.k < ca.k + KVB) {
+        while (ahead < NHB && cs.i < n_items && cs.k < ca.k + KVB) {
           if (!issue_sd(cs)) return false;
           cur_next(cs);
           ++ahead;
@@ -625,9 +634,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           // the epilogue has drained this accumulator buffer
           if (!(ok = mbar_wait_warp(&acc_empty[ab], ((ca.k / ACB) - 1) & 1, status))) break;
         }
-        if (!(ok = mbar_wait_warp(&ps_full[ca.h], ca.ug & 1, status))) break;
+        const int ja = 2 * ca.ug + ca.h, hb = ja % NHB;
+        if (!(ok = mbar_wait_warp(&ps_full[hb], (ja / NHB) & 1, status))) break;
         tc_fence_after();
-        const uint32_t tb = tmem + 128 * ca.h;
+        const uint32_t tb = tmem + 128 * hb;
         const uint32_t tm_dv = tmem + C::TM_ACC + ab * 2 * D, tm_dk = tm_dv + D;
         const uint64_t qo = (st * C::TILE + 8192 * ca.h) >> 4;
         const uint64_t ddo = dsc_do_mn + qo, dq = dsc_q_mn + qo;
@@ -665,7 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int half = (warp - 2) >> 2;
     const int r = quad * 32 + lane;  // key row of the tile
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t tb = tmem + lane_base + 128 * half;
+    const uint32_t tl = tmem + lane_base;
     // accumulators of item k -> global memory (half 0 dV, half 1 dK)
     struct Epi {
       int k;
@@ -780,7 +790,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           vm[0] = range_bits(c_lo, c_hi, 2 * half);
           vm[1] = range_bits(c_lo, c_hi, 2 * half + 1);
         }
-        if (!mbar_wait(&sd_full[half], ugl & 1, status)) {
+        const int jh = 2 * ugl + half, hb = jh % NHB;  // this half-tile's TMEM buffer
+        const uint32_t tb = tl + 128 * hb;
+        if (!mbar_wait(&sd_full[hb], (jh / NHB) & 1, status)) {
           ok = false;
           break;
         }
@@ -825,7 +837,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&ps_full[half]);
+        mbar_arrive(&ps_full[hb]);
       }
       if (!ok) break;
       ug += nU;
@@ -899,13 +911,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int T = geo.T, B = geo.B, Hq = geo.Hq, Hkv = geo.Hkv;
   const int n_items = B * Hq * T;
 
-  const IndexHeader hdr = *idx.header;
-  if (!header_matches(hdr, geo)) {
-    if (threadIdx.x == 0) report(status, SEP_ERR_DEVICE_BOUNDS);
-    return;
-  }
-  const int n_win = hdr.n;
-
   if (threadIdx.x == 0) {
     for (int i = 0; i < QB; ++i) {
       mbar_init(&qd_full[i], 1);
@@ -926,6 +931,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&mma_final, 1);
     fence_mbar_init();
   }
+  if (warp == 1) {
+    tmem_alloc(&tmem_slot, C::TM_COLS);
+    tmem_relinquish();
+  }
+  // barriers and tensor memory are set up before waiting for the dK/dV kernel
+  grid_dep_wait();
+  const IndexHeader hdr = *idx.header;
+  if (!header_matches(hdr, geo)) {
+    if (threadIdx.x == 0) report(status, SEP_ERR_DEVICE_BOUNDS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_slot, C::TM_COLS);
+    return;
+  }
+  const int n_win = hdr.n;
   // block and sequence records of this CTA's items (i = blockIdx.x + x *
   // gridDim.x), read once; items past C::ITEMS read theirs from global memory
   __shared__ int4 s_blk[C::ITEMS], s_seq[C::ITEMS];
@@ -937,10 +958,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                 ((size_t)(bh / Hq) * T + (T - 1 - i / (B * Hq))) * 4);
       s_seq[x] = *reinterpret_cast<const int4*>(idx.seq + bh / Hq);
     }
-  }
-  if (warp == 1) {
-    tmem_alloc(&tmem_slot, C::TM_COLS);
-    tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
@@ -1328,12 +1345,14 @@ int launch_bwd_impl(IndexPtrs idx, const void* q, const void* k, const void* v, 
                          (size_t)geo.B * geo.Hq * geo.T * 128 / kPrepRows;
     const size_t want = (units + kPrepThreads / 32 - 1) / (kPrepThreads / 32);
     const int ctas = static_cast<int>(want < (size_t)8 * sms ? want : (size_t)8 * sms);
-    bwd_prep_kernel<D><<<ctas + 1, kPrepThreads, 0, s>>>(
-        idx, geo, static_cast<const uint4*>(k), static_cast<const uint4*>(v),
+    const cudaError_t e = launch_dependent(
+        bwd_prep_kernel<D>, dim3(ctas + 1), dim3(kPrepThreads), 0, s, idx, geo,
+        static_cast<const uint4*>(k), static_cast<const uint4*>(v),
         reinterpret_cast<uint4*>(w.kk), reinterpret_cast<uint4*>(w.vk),
         static_cast<const uint4*>(o), static_cast<const uint4*>(dout), lse, w.stats,
         reinterpret_cast<float4*>(w.dk_keep), reinterpret_cast<float4*>(w.dv_keep), full_groups,
         w.sched, w.items);
+    if (e != cudaSuccess) return static_cast<int>(e);
   }
   const uint64_t pq = geo.packed ? geo.Hq : (uint64_t)geo.B * geo.Hq;
   const uint64_t pkv = geo.packed ? geo.Hkv : (uint64_t)geo.B * geo.Hkv;
@@ -1357,17 +1376,21 @@ int launch_bwd_impl(IndexPtrs idx, const void* q, const void* k, const void* v, 
   __nv_bfloat16* dkb = static_cast<__nv_bfloat16*>(dk);
   __nv_bfloat16* dvb = static_cast<__nv_bfloat16*>(dv);
   profile_mark(1, s);
-  kv_k<<<sms, kThreads, KC::SMEM, s>>>(mkk, mvk, mk, mv, mq, mdo, idx, w.sched, w.items,
-                                       w.stats, w.dk_keep, w.dv_keep, dkb, dvb, geo, scale,
-                                       scale_log2, full_groups, status);
+  e = launch_dependent(kv_k, dim3(sms), dim3(kThreads), KC::SMEM, s, mkk, mvk, mk, mv, mq, mdo,
+                       idx, static_cast<const BwdSchedule*>(w.sched),
+                       static_cast<const int4*>(w.items), static_cast<const float2*>(w.stats),
+                       w.dk_keep, w.dv_keep, dkb, dvb, geo, scale, scale_log2, full_groups,
+                       status);
+  if (e != cudaSuccess) return static_cast<int>(e);
   profile_mark(2, s);
   // the dQ kernel also writes the keep tokens' dK / dV rows
   const int dq_items = geo.B * geo.Hq * geo.T;
-  dq_k<<<dq_items < sms ? dq_items : sms, kThreads, QC::SMEM, s>>>(
-      mq, mdo, mk, mv, mkk, mvk, idx, w.stats, w.sched,
-      reinterpret_cast<const float4*>(w.dk_keep), reinterpret_cast<const float4*>(w.dv_keep),
-      static_cast<__nv_bfloat16*>(dq), dkb, dvb, geo, scale, scale_log2, full_groups, status);
-  const cudaError_t err = cudaGetLastError();
+  const cudaError_t err = launch_dependent(
+      dq_k, dim3(dq_items < sms ? dq_items : sms), dim3(kThreads), QC::SMEM, s, mq, mdo, mk, mv,
+      mkk, mvk, idx, static_cast<const float2*>(w.stats),
+      static_cast<const BwdSchedule*>(w.sched), reinterpret_cast<const float4*>(w.dk_keep),
+      reinterpret_cast<const float4*>(w.dv_keep), static_cast<__nv_bfloat16*>(dq), dkb, dvb, geo,
+      scale, scale_log2, full_groups, status);
   profile_mark(3, s);
   return static_cast<int>(err);
 }

@@ -51,6 +51,7 @@ __global__ void __launch_bounds__(256)
     gather_keep_kernel(IndexPtrs idx, Geom geo, const uint4* __restrict__ k,
                        const uint4* __restrict__ v, uint4* __restrict__ kk,
                        uint4* __restrict__ vk) {
+  grid_dep_wait();
   const IndexHeader hdr = *idx.header;
   if (!header_matches(hdr, geo)) return;
   const int units = keep_units(geo.B, geo.Hkv, geo.L);
@@ -210,20 +211,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int G = gridDim.x;
   const int grp = Hq / geo.Hkv;
 
-  const IndexHeader hdr = *idx.header;
-  if (!header_matches(hdr, geo)) {
-    if (threadIdx.x == 0) report(status, SEP_ERR_DEVICE_BOUNDS);
-    return;
-  }
-  const int n_win = hdr.n;
-  // records of this CTA's items (item = blockIdx.x + k * G), read once
-  __shared__ int4 s_rec[3 * kCtaItems];
-  for (int x = threadIdx.x; x < kCtaItems; x += blockDim.x) {
-    const int item = static_cast<int>(blockIdx.x) + x * G;
-    if (item < n_items) read_item_records(idx, geo, item, s_rec[3 * x], s_rec[3 * x + 1],
-                                          s_rec[3 * x + 2]);
-  }
-
   if (threadIdx.x == 0) {
     for (int s = 0; s < QB; ++s) {
       mbar_init(&q_full[s], 1);
@@ -244,6 +231,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     tmem_alloc(&tmem_slot, C::TM_COLS);
     tmem_relinquish();
+  }
+  // barriers and tensor memory are set up before waiting for the keep gather
+  grid_dep_wait();
+  const IndexHeader hdr = *idx.header;
+  if (!header_matches(hdr, geo)) {
+    if (threadIdx.x == 0) report(status, SEP_ERR_DEVICE_BOUNDS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_slot, C::TM_COLS);
+    return;
+  }
+  const int n_win = hdr.n;
+  // records of this CTA's items (item = blockIdx.x + k * G), read once
+  __shared__ int4 s_rec[3 * kCtaItems];
+  for (int x = threadIdx.x; x < kCtaItems; x += blockDim.x) {
+    const int item = static_cast<int>(blockIdx.x) + x * G;
+    if (item < n_items) read_item_records(idx, geo, item, s_rec[3 * x], s_rec[3 * x + 1],
+                                          s_rec[3 * x + 2]);
   }
   tc_fence_before();
   __syncthreads();
@@ -603,9 +609,11 @@ int launch_fwd_impl(IndexPtrs idx, const void* q, const void* k, const void* v, 
   uint8_t* vk = kk + align_up((size_t)geo.Hkv * geo.TT * 128 * D * 2, 256);
   const int sms = num_sms();
   profile_mark(0, s);
-  gather_keep_kernel<D><<<keep_pass_ctas(keep_units(geo.B, geo.Hkv, geo.L), sms), 256, 0, s>>>(
-      idx, geo, static_cast<const uint4*>(k), static_cast<const uint4*>(v),
+  cudaError_t e = launch_dependent(
+      gather_keep_kernel<D>, dim3(keep_pass_ctas(keep_units(geo.B, geo.Hkv, geo.L), sms)),
+      dim3(256), 0, s, idx, geo, static_cast<const uint4*>(k), static_cast<const uint4*>(v),
       reinterpret_cast<uint4*>(kk), reinterpret_cast<uint4*>(vk));
+  if (e != cudaSuccess) return static_cast<int>(e);
   // head planes of q / k / v: (sequence, head) planes of L rows, or one plane
   // per head of a pack; the gathered keep rows: one plane per kv head over
   // the tile space
@@ -619,15 +627,15 @@ int launch_fwd_impl(IndexPtrs idx, const void* q, const void* k, const void* v, 
       !make_bf16_map(&mvk, vk, geo.Hkv, rk, D, 128))
     return static_cast<int>(cudaErrorInvalidValue);
   auto kern = attn_fwd_tc_kernel<D>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return static_cast<int>(e);
   const float scale_log2 = scale * 1.4426950408889634f;
   const long long items = (long long)geo.B * geo.Hq * ((geo.T + 1) / 2);
   const int grid = static_cast<int>(items < sms ? items : sms);  // persistent: one CTA per SM
   profile_mark(1, s);
-  kern<<<grid, kThreads, C::SMEM, s>>>(mq, mk, mv, mkk, mvk, idx, static_cast<__nv_bfloat16*>(o),
-                                       lse, geo, scale_log2, full_groups, status);
-  const cudaError_t err = cudaGetLastError();
+  const cudaError_t err =
+      launch_dependent(kern, dim3(grid), dim3(kThreads), C::SMEM, s, mq, mk, mv, mkk, mvk, idx,
+                       static_cast<__nv_bfloat16*>(o), lse, geo, scale_log2, full_groups, status);
   profile_mark(2, s);
   return static_cast<int>(err);
 }

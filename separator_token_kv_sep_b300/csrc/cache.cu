@@ -28,8 +28,11 @@
 // cache will have after this step's update; it then attends over its share
 // of the entries in that layout, reading each entry from where it sits
 // *before* the update (a separator that moves this step is read from its
-// window slot, the new token from the caller's k_new / v_new).  The rows
-// arrive by TMA bulk copies into shared memory.  The partial softmax states
+// window slot, the new token from the caller's k_new / v_new).  A producer
+// warp stages the rows in shared memory with 16-byte asynchronous copies;
+// two consumer warps score them and accumulate P.V on the tensor cores
+// (mma.sync, bf16 in, fp32 out), rotating keys by RoPE in registers at
+// their cache rank.  The partial softmax states
 // merge over distributed shared memory, and only after the whole cluster has
 // finished reading does CTA 0 write the update (moves, new row, flags,
 // counters).  Counters and flags are kept per (sequence, kv head), so no
@@ -50,7 +53,7 @@ namespace {
 
 constexpr int kCacheMagic = 0x43504553;  // 'SEPC'
 constexpr int kConsumerWarps = 2;        // score / softmax / P.V warps
-constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one TMA producer warp
+constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one copy producer warp
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxC = 1024;              // survivor list is kept in shared memory
 constexpr int kMaxHkv = 64;
@@ -379,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 4)
   }
 
   // ---- attention over this CTA's share [k0, k1) of the new layout, streamed
-  // in chunks of CH entries through an NST-stage ring of TMA bulk copies
+  // in chunks of CH entries through an NST-stage ring of asynchronous copies
   bool att_ok = ok && attend;
   const size_t head_off = mh * (size_t)NSL * D;
   if (attend) {

@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/sepattn.h"
 
 namespace sep {
@@ -332,6 +334,35 @@ __host__ __device__ __forceinline__ bool group_full(uint64_t full_groups, int g)
 // window n >= L (no gathered keys, the band from key 0 to the tile's last row).
 __device__ __forceinline__ int4 full_block_record(int t, int L) {
   return make_int4(0, 0, min(L, 128 * t + 128), 1);
+}
+
+// Programmatic dependent launch.  A kernel started by launch_dependent() is
+// launched as soon as the kernel before it on the stream exits, without the
+// gap of an ordinary launch, and may be resident while that kernel's last
+// CTAs drain: it does only local setup (barriers, tensor memory) until
+// grid_dep_wait() returns, which is after that kernel has finished and its
+// writes are visible.  Every such kernel waits before its first global
+// memory access, so stream order holds for all of them.  (None signals its
+// dependents early: letting the next grid's CTAs wait beside a running
+// kernel was measured slower.)
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block,
+                                    size_t smem, cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {

@@ -26,14 +26,15 @@
 // inclusive prefix ends the walk).  A CTA only ever waits on tiles claimed
 // before its own, by CTAs already running, so the walk always ends; it is
 // also bounded in time.  Pairs of lanes join their 16 keep bits into one
-// 32-bit word of the keep bitmask.  Separator ids are tested through a
-// 1024-bit filter first and exactly only when its bit is set.  keep_pos is
-// set to -1 by a memset before the launch, so only its valid entries are
-// written here.  Each CTA writes the block records of
-// the query tiles whose window start falls in its tile; the last tile of a
-// sequence writes the count and the padding.  The ticket and the status
-// words live in a scratch region of the index buffer that the host zeroes
-// before the launch.
+// 32-bit word of the keep bitmask.  Separator ids are looked up in a
+// direct-mapped table of 1024 slots (slot = id & 1023): one shared-memory
+// load and a compare per token, and a loop over the ids only for a slot
+// that two separator ids share.  Only keep_pos entries below the count are
+// written.  Each CTA writes the block records of the query tiles whose
+// window start falls in its tile (the thread owning that token); the last
+// tile of a sequence writes the count and the padding.  The ticket and the
+// status words live in a scratch region of the index buffer that the host
+// zeroes before the launch.
 #include "common.cuh"
 #include "layout.h"
 
@@ -42,7 +43,14 @@ namespace sep {
 namespace {
 
 constexpr int kThreads = 512;
+constexpr int kBM = SEP_BLOCK_M;  // query-tile height of the block records
 static_assert(kThreads * 16 == kScanTile, "16 tokens per thread in a full scan tile");
+static_assert((kBM & (kBM - 1)) == 0, "block records assume a power-of-two tile height");
+
+// separator table: slot s = id & 1023 holds the separator id of that slot,
+// s ^ 1 when no separator id maps there (never equal to an id of slot s) or
+// s ^ 2 when several do (then the ids are compared one by one)
+constexpr int kSlots = 1024;
 
 // status word of a (sequence, scan tile): flag in bits 62-63, count below
 constexpr unsigned long long kAggregate = 1ull << 62, kInclusive = 2ull << 62;
@@ -61,10 +69,11 @@ __device__ __forceinline__ unsigned long long ld_acquire(const unsigned long lon
 // kScanTile), 4 for rows of at most 2048 (one tile, four times the active
 // threads).
 template <int PER>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 4)
     build_index_kernel(const int32_t* __restrict__ ids, const int32_t* __restrict__ cu,
-                       int total, int B, int L, SepIdList sids, int a, int n, int block_m,
+                       int total, int B, int L, SepIdList sids, int a, int n,
                        int fix_delta, IndexPtrs ptrs, int* status) {
+  constexpr int block_m = kBM;
   // rows of at most one scan tile need no ticket, no look-back and no
   // scratch: tile (b, 0) is block b
   constexpr int kPerThread = PER;
@@ -74,24 +83,24 @@ __global__ void __launch_bounds__(kThreads)
   __shared__ int tile_total, prefix_sh, tiles_before;
   __shared__ unsigned int ticket;
   __shared__ int sep_ids[SEP_MAX_SEP_IDS];
-  // a 1024-bit filter of the separator ids (bit id & 1023): a token whose
-  // bit is clear is no separator, one whose bit is set is checked exactly
-  __shared__ uint32_t sep_filter[32];
-  __shared__ int kposbuf[kScanTile];  // this tile's keep positions, in order
+  __shared__ int sep_slot[kSlots];
+  __shared__ __align__(16) int stage[kThreads * PER];  // keep_prefix values, per warp
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n_sep = sids.n;
   const int T = (L + block_m - 1) / block_m;
   const int ntiles = (L + kScanTile - 1) / kScanTile;
-  if (tid < 32) sep_filter[tid] = 0u;
+  for (int s = tid; s < kSlots; s += kThreads) sep_slot[s] = s ^ 1;
+  grid_dep_wait();
   if (tid == 0) {
     tiles_before = 0;
     ticket = multi ? atomicAdd(ptrs.scan_ticket, 1u) : blockIdx.x;
   }
   __syncthreads();
   if (tid < n_sep) {
-    const int id = sids.ids[tid];
+    const int id = sids.ids[tid], s = id & (kSlots - 1);
     sep_ids[tid] = id;
-    atomicOr(&sep_filter[(id >> 5) & 31], 1u << (id & 31));
+    const int old = atomicCAS(&sep_slot[s], s ^ 1, id);
+    if (old != (s ^ 1) && old != id) sep_slot[s] = s ^ 2;  // shared slot
   }
   __syncthreads();
   const int tau = static_cast<int>(ticket);
@@ -139,22 +148,33 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
     for (int e = 0; e < kPerThread; ++e) v[e] = (by_ids && j0 + e < len) ? row[j0 + e] : 0;
   }
-  uint32_t nib = 0;  // keep bits of the thread's 16 tokens
+  uint32_t nib = 0;  // keep bits of the thread's tokens
+  if (by_ids) {
+    uint32_t shared_slot = 0;  // tokens whose slot several separator ids share
 #pragma unroll
-  for (int e = 0; e < kPerThread; ++e) {
-    const int j = j0 + e;
-    bool keep = false;
-    if (j < len) {
-      keep = j < a;
-      if (by_ids) {
-        if ((sep_filter[(v[e] >> 5) & 31] >> (v[e] & 31)) & 1u)
-          for (int q = 0; q < n_sep; ++q) keep |= (v[e] == sep_ids[q]);
-      } else {
-        keep |= (j + 1) % fix_delta == 0;
+    for (int e = 0; e < kPerThread; ++e) {
+      const int t = sep_slot[v[e] & (kSlots - 1)];
+      nib |= (t == v[e] ? 1u : 0u) << e;
+      shared_slot |= (((t ^ v[e]) & (kSlots - 1)) == 2 ? 1u : 0u) << e;
+    }
+    if (__any_sync(0xffffffffu, shared_slot != 0u)) {
+#pragma unroll
+      for (int e = 0; e < kPerThread; ++e) {
+        if (!((shared_slot >> e) & 1u)) continue;
+        bool hit = false;
+        for (int q = 0; q < n_sep; ++q) hit |= (v[e] == sep_ids[q]);
+        nib |= (hit ? 1u : 0u) << e;
       }
     }
-    nib |= (keep ? 1u : 0u) << e;
+  } else {
+#pragma unroll
+    for (int e = 0; e < kPerThread; ++e) nib |= ((j0 + e + 1) % fix_delta == 0 ? 1u : 0u) << e;
   }
+  if (j0 < a)  // the sinks
+#pragma unroll
+    for (int e = 0; e < kPerThread; ++e) nib |= (j0 + e < a ? 1u : 0u) << e;
+  if (j0 + kPerThread > len)  // past the sequence's end
+    nib &= len > j0 ? (1u << (len - j0)) - 1u : 0u;
   const int cnt = __popc(nib);
   int incl = cnt;
 #pragma unroll
@@ -223,15 +243,12 @@ __global__ void __launch_bounds__(kThreads)
   __syncthreads();
   const int prefix = prefix_sh;
 
-  // ---- keep_prefix, keep_pos and the keep bits of the tile.  keep_prefix
-  // is written token-major across the warp (lane l writes token 32 m + l of
-  // the warp's 512, whose owner thread and bit come by shuffle), so each
-  // store covers 128 contiguous bytes; keep positions go through shared
-  // memory and leave in order.
+  // ---- block records, keep_prefix, keep_pos and the keep bits of the tile.
   // The block record of query tile t needs keep_prefix at its window start
-  // W(t) = max(0, 128 t - n + 1): the lane that computes keep_prefix of a
-  // token that is some W(t) writes that record (token 0 those of every tile
-  // whose window starts at 0).
+  // W(t) = max(0, 128 t - n + 1).  A window start above 0 is a token j with
+  // j = 1 - n (mod 128); the thread owning it writes the record (at most one
+  // per thread).  Tile 0's CTA writes the records of every tile whose window
+  // starts at 0.
   const int Tb = (len + block_m - 1) / block_m;
   int32_t* blk = ptrs.blocks + (size_t)b * T * 4;
   auto record = [&](int t, int W, int kv) {
@@ -243,29 +260,49 @@ __global__ void __launch_bounds__(kThreads)
     *reinterpret_cast<int4*>(blk + 4 * t) = rec;
   };
   {
+    const int resid = static_cast<int>((1 - static_cast<long long>(n)) & (block_m - 1));
+    const int e = (resid - j0) & (block_m - 1);  // the thread's token of that residue
+    const int j = j0 + e;
+    if (e < kPerThread && j > 0 && j < len) {
+      const long long t = ((long long)j + n - 1) / block_m;
+      if (t < Tb) record(static_cast<int>(t), j, prefix + lpos + __popc(nib & ((1u << e) - 1u)));
+    }
+    if (k == 0)  // windows that start at token 0 (keep_prefix[0] = 0)
+      for (int t = tid; t < Tb && (long long)t * block_m - n + 1 <= 0; t += kThreads)
+        record(t, 0, 0);
+  }
+  {
+    // through the warp's part of the staging buffer: written thread-major,
+    // read back token-major, so each global store covers 128 contiguous bytes
+    int* wst = stage + warp * 32 * kPerThread;
+    int run = prefix + lpos;
+#pragma unroll
+    for (int q = 0; q < kPerThread / 4; ++q) {
+      int4 x;
+      x.x = run; run += (nib >> (4 * q)) & 1u;
+      x.y = run; run += (nib >> (4 * q + 1)) & 1u;
+      x.z = run; run += (nib >> (4 * q + 2)) & 1u;
+      x.w = run; run += (nib >> (4 * q + 3)) & 1u;
+      *reinterpret_cast<int4*>(wst + lane * kPerThread + 4 * q) = x;
+    }
+    __syncwarp();
     const int wbase = base + warp * 32 * kPerThread;  // the warp's first token
-#pragma unroll 4
+#pragma unroll
     for (int m = 0; m < kPerThread; ++m) {
-      const int owner = (32 * m + lane) / PER, bit = (32 * m + lane) % PER;
-      const uint32_t onib = __shfl_sync(0xffffffffu, nib, owner);
-      const int olpos = __shfl_sync(0xffffffffu, lpos, owner);
       const int j = wbase + 32 * m + lane;
-      if (j < len) {
-        const int kv = prefix + olpos + __popc(onib & ((1u << bit) - 1u));
-        kp[j] = kv;
-        if (j == 0) {
-          for (int t = 0; t < Tb && (long long)t * block_m - n + 1 <= 0; ++t) record(t, 0, kv);
-        } else if (((long long)j + n - 1) % block_m == 0) {
-          const long long t = ((long long)j + n - 1) / block_m;
-          if (t < Tb) record(static_cast<int>(t), j, kv);
-        }
-      }
+      if (j < len) kp[j] = wst[32 * m + lane];
     }
   }
-#pragma unroll
-  for (int e = 0; e < kPerThread; ++e) {
-    if ((nib >> e) & 1u) kposbuf[lpos] = j0 + e;
-    lpos += (nib >> e) & 1u;
+  // keep positions, in order: a lane's keep tokens go to consecutive
+  // entries from its prefix, and a warp's stores stay within its few
+  // hundred bytes of keep_pos
+  {
+    uint32_t rest = nib;
+    int* out = kpos + prefix + lpos;
+    while (rest) {
+      *out++ = j0 + __ffs(rest) - 1;
+      rest &= rest - 1u;
+    }
   }
   // 32 / PER lanes x PER tokens = one word of the keep bitmask
   constexpr int LPW = 32 / PER;
@@ -274,16 +311,12 @@ __global__ void __launch_bounds__(kThreads)
   for (int off = 1; off < LPW; off <<= 1) word |= __shfl_xor_sync(0xffffffffu, word, off);
   const int widx = j0 >> 5;
   if (lane % LPW == 0 && widx < nwords) bits_out[widx] = word;
-  __syncthreads();  // kposbuf is complete
-  for (int i = tid; i < tile_total; i += kThreads) kpos[prefix + i] = kposbuf[i];
 
   // ---- per sequence: the last tile writes the count and the padding; the
   // first one the sequence record (and the header, for sequence 0)
   if (k == ntiles - 1) {
     const int count = prefix + tile_total;
     for (int j = len + tid; j <= L; j += kThreads) kp[j] = count;
-    if (!multi)  // (a multi-tile row's keep_pos was set to -1 before the launch)
-      for (int j = count + tid; j < L; j += kThreads) kpos[j] = -1;
     for (int t = Tb + tid; t < T; t += kThreads)
       *reinterpret_cast<int4*>(blk + 4 * t) = make_int4(0, 0, 0, 0);
     if (tid == 0) ptrs.keep_count[b] = count;
@@ -310,23 +343,21 @@ int launch_build_index(const int32_t* ids, const int32_t* cu, int total, int B, 
                        IndexPtrs ptrs, int* status, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int ntiles = (L + kScanTile - 1) / kScanTile;
-  // the ticket and the status words start at zero; keep_pos starts at -1
-  // everywhere (the kernel writes the entries below each count)
-  // (rows of one scan tile need neither)
+  if (block_m != kBM) return static_cast<int>(cudaErrorInvalidValue);
+  // the ticket and the status words start at zero (rows of one scan tile
+  // use neither)
   if (ntiles > 1) {
-    cudaError_t e = cudaMemsetAsync(ptrs.scan_ticket, 0,
-                                    256 + sizeof(unsigned long long) * (size_t)B * ntiles, s);
-    if (e == cudaSuccess)
-      e = cudaMemsetAsync(ptrs.keep_pos, 0xff, sizeof(int32_t) * (size_t)B * L, s);
+    const cudaError_t e = cudaMemsetAsync(
+        ptrs.scan_ticket, 0, 256 + sizeof(unsigned long long) * (size_t)B * ntiles, s);
     if (e != cudaSuccess) return static_cast<int>(e);
   }
-  if (L <= kThreads * 4)
-    build_index_kernel<4><<<B, kThreads, 0, s>>>(ids, cu, total, B, L, sids, a, n, block_m,
-                                                 fix_delta, ptrs, status);
-  else
-    build_index_kernel<16><<<B * ntiles, kThreads, 0, s>>>(ids, cu, total, B, L, sids, a, n,
-                                                           block_m, fix_delta, ptrs, status);
-  return static_cast<int>(cudaGetLastError());
+  const cudaError_t e =
+      L <= kThreads * 4
+          ? launch_dependent(build_index_kernel<4>, dim3(B), dim3(kThreads), 0, s, ids, cu,
+                             total, B, L, sids, a, n, fix_delta, ptrs, status)
+          : launch_dependent(build_index_kernel<16>, dim3(B * ntiles), dim3(kThreads), 0, s,
+                             ids, cu, total, B, L, sids, a, n, fix_delta, ptrs, status);
+  return static_cast<int>(e);
 }
 
 }  // namespace sep
