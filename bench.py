@@ -491,6 +491,24 @@ def run_e2e(api, cfg, q_np, k_np, v_np, do_np, ids_np, device, args, flops, worl
     t0 = time.perf_counter()
     run(n)
     dt = max_over_ranks(time.perf_counter() - t0, world)
+    # the host link's own roofline: the step's uploads alone and its
+    # downloads alone, each timed by CUDA events on its copy stream (best of 5)
+    def link_gbs(copies, stream):
+        best = float("inf")
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for _ in range(5):
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                for dst, src in copies:
+                    dst.copy_(src, non_blocking=True)
+                e1.record(stream)
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        nbytes = sum(src.numel() * src.element_size() for _, src in copies)
+        return nbytes / (best * 1e-3) / 1e9
+    h2d_gbs = link_gbs(list(zip(dev_in[0], host_in)), s_in)
+    d2h_gbs = link_gbs(list(zip(host_out, dev_out[0])), s_out)
+    link_ms = max(h2d / h2d_gbs, d2h / d2h_gbs) * 1e-6
     # the pipelined gradients equal a plain serial call's (dQ is deterministic)
     q, k, v, dout, ids = (x.to(device) for x in host_in)
     buf = api.sep_build_index(ids, synth.SEP_IDS, cfg.a, cfg.n)
@@ -501,6 +519,12 @@ def run_e2e(api, cfg, q_np, k_np, v_np, do_np, ids_np, device, args, flops, worl
     return {"value": round(flops * world * n / dt / 1e12, 3), "unit": "TFLOP/s",
             "ms_per_step": round(dt / n * 1e3, 4), "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
+            "link": {"h2d_gbs": round(h2d_gbs, 1), "d2h_gbs": round(d2h_gbs, 1),
+                     "bound_ms_per_step": round(link_ms, 4),
+                     "frac": round(link_ms / (dt / n * 1e3), 3),
+                     "note": "pinned copies of one step's inputs (uploads) and gradients "
+                             "(downloads), each direction alone; the bound is the slower "
+                             "direction, as they overlap on separate streams"},
             "note": "public API, eager launches, pinned host buffers, wall clock; uploads, "
                     "compute and downloads of consecutive steps overlap on three streams"}
 

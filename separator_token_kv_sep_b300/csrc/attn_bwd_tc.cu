@@ -296,7 +296,7 @@ __global__ void __launch_bounds__(kPrepThreads)
                     const float* __restrict__ lse, float2* __restrict__ stats,
                     float4* __restrict__ dk_keep, float4* __restrict__ dv_keep,
                     uint64_t full_groups, BwdSchedule* __restrict__ sched,
-                    int4* __restrict__ items) {
+                    int4* __restrict__ items, int* status) {
   grid_dep_wait();
   const IndexHeader hdr = *idx.header;
   if (!header_matches(hdr, geo)) return;
@@ -312,7 +312,8 @@ __global__ void __launch_bounds__(kPrepThreads)
   const size_t sunits = (size_t)geo.B * geo.Hq * geo.T * 128 / kPrepRows;
   for (size_t u = w0; u < gunits + sunits; u += nw) {
     if (u < gunits)
-      gather_keep_unit<D>(idx, geo, k, v, kk, vk, dk_keep, dv_keep, static_cast<int>(u), lane);
+      gather_keep_unit<D>(idx, geo, k, v, kk, vk, dk_keep, dv_keep, static_cast<int>(u), lane,
+                          status);
     else
       prep_stats_unit<D>(idx, geo, o, dout, lse, stats, u - gunits, lane);
   }
@@ -1167,7 +1168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nw = static_cast<int>(gridDim.x) * (kEwThreads / 32);
       for (int u = static_cast<int>(blockIdx.x) * (kEwThreads / 32) + (warp - 2); u < units;
            u += nw)
-        scatter_keep_unit<D>(idx, geo, dk_keep, dv_keep, dk, dv, scale, u, lane);
+        scatter_keep_unit<D>(idx, geo, dk_keep, dv_keep, dk, dv, scale, u, lane, status);
     }
     // Two warpgroups share every tile: warps 2-5 take key columns 0-63 and
     // warps 6-9 columns 64-127 of the same 128 query rows; in the epilogue
@@ -1351,7 +1352,7 @@ int launch_bwd_impl(IndexPtrs idx, const void* q, const void* k, const void* v, 
         reinterpret_cast<uint4*>(w.kk), reinterpret_cast<uint4*>(w.vk),
         static_cast<const uint4*>(o), static_cast<const uint4*>(dout), lse, w.stats,
         reinterpret_cast<float4*>(w.dk_keep), reinterpret_cast<float4*>(w.dv_keep), full_groups,
-        w.sched, w.items);
+        w.sched, w.items, status);
     if (e != cudaSuccess) return static_cast<int>(e);
   }
   const uint64_t pq = geo.packed ? geo.Hq : (uint64_t)geo.B * geo.Hq;

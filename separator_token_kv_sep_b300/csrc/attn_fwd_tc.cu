@@ -50,14 +50,14 @@ template <int D>
 __global__ void __launch_bounds__(256)
     gather_keep_kernel(IndexPtrs idx, Geom geo, const uint4* __restrict__ k,
                        const uint4* __restrict__ v, uint4* __restrict__ kk,
-                       uint4* __restrict__ vk) {
+                       uint4* __restrict__ vk, int* status) {
   grid_dep_wait();
   const IndexHeader hdr = *idx.header;
   if (!header_matches(hdr, geo)) return;
   const int units = keep_units(geo.B, geo.Hkv, geo.L);
   const int lane = threadIdx.x & 31;
   for (int u = blockIdx.x * 8 + (threadIdx.x >> 5); u < units; u += gridDim.x * 8)
-    gather_keep_unit<D>(idx, geo, k, v, kk, vk, nullptr, nullptr, u, lane);
+    gather_keep_unit<D>(idx, geo, k, v, kk, vk, nullptr, nullptr, u, lane, status);
 }
 
 template <int D>
@@ -612,7 +612,7 @@ int launch_fwd_impl(IndexPtrs idx, const void* q, const void* k, const void* v, 
   cudaError_t e = launch_dependent(
       gather_keep_kernel<D>, dim3(keep_pass_ctas(keep_units(geo.B, geo.Hkv, geo.L), sms)),
       dim3(256), 0, s, idx, geo, static_cast<const uint4*>(k), static_cast<const uint4*>(v),
-      reinterpret_cast<uint4*>(kk), reinterpret_cast<uint4*>(vk));
+      reinterpret_cast<uint4*>(kk), reinterpret_cast<uint4*>(vk), status);
   if (e != cudaSuccess) return static_cast<int>(e);
   // head planes of q / k / v: (sequence, head) planes of L rows, or one plane
   // per head of a pack; the gathered keep rows: one plane per kv head over

@@ -28,8 +28,10 @@ __host__ __device__ inline int keep_units(int B, int Hkv, int L) {
   return B * Hkv * ((L + kKeepUnitRows - 1) / kKeepUnitRows);
 }
 
-// Copies the keep rows of one unit (and, if dk_keep is set, zeroes the same
-// rows of the fp32 gradient accumulators dk_keep / dv_keep).
+// Copies the keep rows of one unit (and, if dk_keep is set, zeroes the rows
+// of the fp32 gradient accumulators dk_keep / dv_keep below the keep count,
+// the only ones that are added to and read).  A keep position outside its
+// sequence is reported as SEP_ERR_DEVICE_BOUNDS and its row left zero.
 template <int D>
 __device__ __forceinline__ void gather_keep_unit(IndexPtrs idx, const Geom& geo,
                                                  const uint4* __restrict__ k,
@@ -37,7 +39,7 @@ __device__ __forceinline__ void gather_keep_unit(IndexPtrs idx, const Geom& geo,
                                                  uint4* __restrict__ kk, uint4* __restrict__ vk,
                                                  float4* __restrict__ dk_keep,
                                                  float4* __restrict__ dv_keep, int unit,
-                                                 int lane) {
+                                                 int lane, int* status) {
   constexpr int U = D / 8;                         // 16-byte units of a bf16 row
   constexpr int PER = kKeepUnitRows * U / 32;      // per lane
   const int pairs = geo.B * geo.Hkv;
@@ -62,6 +64,8 @@ __device__ __forceinline__ void gather_keep_unit(IndexPtrs idx, const Geom& geo,
     if (src >= 0 && src < sr.len) {
       kv[x] = k[src_base + (size_t)src * U + u];
       vv[x] = v[src_base + (size_t)src * U + u];
+    } else if (row < count) {
+      report(status, SEP_ERR_DEVICE_BOUNDS);
     }
   }
 #pragma unroll
@@ -81,7 +85,7 @@ __device__ __forceinline__ void gather_keep_unit(IndexPtrs idx, const Geom& geo,
     for (int x = 0; x < 2 * PER; ++x) {
       const int e = x * 32 + lane;
       const int row = row0 + e / U4;
-      if (row < end) {
+      if (row < count) {
         dk_keep[base4 + (size_t)row * U4 + e % U4] = z;
         dv_keep[base4 + (size_t)row * U4 + e % U4] = z;
       }
@@ -90,14 +94,15 @@ __device__ __forceinline__ void gather_keep_unit(IndexPtrs idx, const Geom& geo,
 }
 
 // dK / dV rows of the keep tokens of one unit, from the fp32 accumulators
-// (dK times the softmax scale), rounded to bf16 once.
+// (dK times the softmax scale), rounded to bf16 once.  A keep position
+// outside its sequence is reported and not written.
 template <int D>
 __device__ __forceinline__ void scatter_keep_unit(IndexPtrs idx, const Geom& geo,
                                                   const float4* __restrict__ dk_keep,
                                                   const float4* __restrict__ dv_keep,
                                                   __nv_bfloat16* __restrict__ dk,
                                                   __nv_bfloat16* __restrict__ dv, float scale,
-                                                  int unit, int lane) {
+                                                  int unit, int lane, int* status) {
   constexpr int U4 = D / 4;
   constexpr int PER = kKeepUnitRows * U4 / 32;
   const int pairs = geo.B * geo.Hkv;
@@ -128,7 +133,10 @@ __device__ __forceinline__ void scatter_keep_unit(IndexPtrs idx, const Geom& geo
     const int row = row0 + e / U4, u = e % U4;
     if (row >= count) continue;
     const int j = kpos[row];
-    if (j < 0 || j >= sr.len) continue;
+    if (j < 0 || j >= sr.len) {  // a keep position outside the sequence
+      report(status, SEP_ERR_DEVICE_BOUNDS);
+      continue;
+    }
     uint2 ko, vo;
     ko.x = pack_bf16x2(a[x].x * scale, a[x].y * scale);
     ko.y = pack_bf16x2(a[x].z * scale, a[x].w * scale);

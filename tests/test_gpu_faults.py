@@ -62,3 +62,26 @@ def test_inconsistent_cache_counters_are_reported():
     api.sep_cache_step(p, buf, qn, kn, kn, ids, synth.SEP_IDS)
     assert api.sep_get_device_status() == 6
     assert int(meta[3]) == c + 5  # the step did not write the corrupt stream
+
+
+def test_keep_positions_outside_the_sequence_are_reported():
+    # keep_pos entries past the row (one too far, one negative) are caught by
+    # the keep-row gather and scatter before any access; the calls report
+    # SEP_ERR_DEVICE_BOUNDS and the context keeps working
+    from separator_token_kv_sep_b300 import api
+    rng = np.random.default_rng(3)
+    B, H, L, d = 2, 2, 300, 64
+    ids = synth.token_ids(rng, (B, L), 0.3)
+    buf = api.sep_build_index(torch.from_numpy(ids).cuda(), synth.SEP_IDS, 4, 32)
+    views = api.sep_index_views(buf, B, L)
+    assert int(views["keep_count"][0]) > 10 and int(views["keep_count"][1]) > 10
+    views["keep_pos"][0, 5] = L + 1000
+    views["keep_pos"][1, 2] = -7
+    bf = torch.bfloat16
+    mk = lambda *sh: torch.randn(*sh, device="cuda").to(bf)  # noqa: E731
+    q, k, v, do = mk(B, H, L, d), mk(B, H, L, d), mk(B, H, L, d), mk(B, H, L, d)
+    o, lse = api.sep_attn_fwd(buf, q, k, v)
+    assert api.sep_get_device_status() == 6  # SEP_ERR_DEVICE_BOUNDS
+    api.sep_attn_bwd(buf, q, k, v, o, lse, do)
+    assert api.sep_get_device_status() == 6
+    assert api.sep_get_device_status() == 0
