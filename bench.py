@@ -42,9 +42,8 @@ METRIC = "Sep-Attention fwd+bwd TFLOP/s (visited pairs) & decode tok/s; % roofli
 # DRAM bytes per launch from one ncu capture of each kernel version at the
 # bench's training workload; a kernel changed since its capture has no entry
 # (its "traffic" is reported as null)
-DRAM_TRAFFIC_BYTES = {"bwd_kv": 143.985408e6 + 23.182080e6, "fwd_attn": 81.943040e6 + 4.494848e6,
-                      "bwd_dq": 108.658176e6 + 9.982976e6}
-DECODE_DRAM_TRAFFIC_BYTES = 81.577216e6 + 2.098432e6
+DRAM_TRAFFIC_BYTES = {}
+DECODE_DRAM_TRAFFIC_BYTES = 81.506560e6 + 1.981440e6
 L2_FLUSH_BYTES = 256 << 20
 
 
