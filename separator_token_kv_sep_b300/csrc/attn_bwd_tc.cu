@@ -410,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
   const int n_win = hdr.n;
-  // this CTA's items (i = blockIdx.x + k * gridDim.x) and what every role
+  // this CTA's items (i = snake_item(k, gridDim.x)) and what every role
   // needs of them, read once: the sequence record with its keep count, the
   // block record of the first query tile and, for a dense key tile, its 128
   // keep bits and the keep prefix at its first key.  Items past kCtaItems
@@ -432,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                : *reinterpret_cast<const int4*>(idx.blocks + ((size_t)b * T + t0) * 4);
   };
   for (int x = threadIdx.x; x < kCtaItems; x += blockDim.x) {
-    const int i = static_cast<int>(blockIdx.x) + x * static_cast<int>(gridDim.x);
+    const int i = snake_item(x, static_cast<int>(gridDim.x));
     if (i < n_items) {
       const int4 it = items[i];
       const int4 sq = item_seq(it);
@@ -488,7 +488,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int k = 0, ug = 0, kv_issued = 0;
       bool ok = true;
-      for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x, ++k) {
+      for (int i = blockIdx.x; ok && i < n_items;
+           ++k, i = snake_item(k, static_cast<int>(gridDim.x))) {
         const Item it = item_at(i, k);
         const int kb = k % KVB;
         if (k >= KVB && !mbar_wait(&kv_empty[kb], ((k / KVB) - 1) & 1, status)) {
@@ -573,8 +574,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++c.ug;
         if (++c.u < c.nU) return;
         c.u = 0;
-        c.i += gridDim.x;
         ++c.k;
+        c.i = snake_item(c.k, static_cast<int>(gridDim.x));
         cur_load(c);
       };
       // descriptors of the operand bases, advanced by constant offsets
@@ -723,7 +724,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool pend = false;
     int k = 0, ug = 0;
     bool ok = true;
-    for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x, ++k) {
+    for (int i = blockIdx.x; ok && i < n_items;
+         ++k, i = snake_item(k, static_cast<int>(gridDim.x))) {
       const Item it = item_at(i, k);
       const bool keep = it.kind == kItemKeep;
       const int len = it.len;
@@ -948,11 +950,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
   const int n_win = hdr.n;
-  // block and sequence records of this CTA's items (i = blockIdx.x + x *
-  // gridDim.x), read once; items past C::ITEMS read theirs from global memory
+  // block and sequence records of this CTA's items (i = snake_item(x,
+  // gridDim.x)), read once; items past C::ITEMS read theirs from global memory
   __shared__ int4 s_blk[C::ITEMS], s_seq[C::ITEMS];
   for (int x = threadIdx.x; x < C::ITEMS; x += blockDim.x) {
-    const int i = static_cast<int>(blockIdx.x) + x * static_cast<int>(gridDim.x);
+    const int i = snake_item(x, static_cast<int>(gridDim.x));
     if (i < n_items) {
       const int bh = i % (B * Hq);
       s_blk[x] = *reinterpret_cast<const int4*>(idx.blocks +
@@ -1010,7 +1012,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int k = 0, ug = 0, qd_issued = 0;  // k: live items so far
       bool ok = true;
-      for (int i = blockIdx.x, ix = 0; ok && i < n_items; i += gridDim.x, ++ix) {
+      for (int i = blockIdx.x, ix = 0; ok && i < n_items;
+           ++ix, i = snake_item(ix, static_cast<int>(gridDim.x))) {
         const Item it = item_at(i, ix);
         if (it.empty) continue;
         if (!it.ok) {
@@ -1073,7 +1076,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                      ds_base = smem_u32(smem + C::OFF_DS);
       int k = 0, ug = 0;  // k: live items so far
       bool ok = true;
-      for (int i = blockIdx.x, ix = 0; ok && i < n_items; i += gridDim.x, ++ix) {
+      for (int i = blockIdx.x, ix = 0; ok && i < n_items;
+           ++ix, i = snake_item(ix, static_cast<int>(gridDim.x))) {
         const Item it = item_at(i, ix);
         if (it.empty) continue;
         if (!it.ok) break;
@@ -1182,7 +1186,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sDS = smem + C::OFF_DS;
     int k = 0, ug = 0;  // k: live items so far
     bool ok = true;
-    for (int i = blockIdx.x, ix = 0; ok && i < n_items; i += gridDim.x, ++ix) {
+    for (int i = blockIdx.x, ix = 0; ok && i < n_items;
+           ++ix, i = snake_item(ix, static_cast<int>(gridDim.x))) {
       const Item it = item_at(i, ix);
       if (it.empty) continue;
       if (!it.ok) break;

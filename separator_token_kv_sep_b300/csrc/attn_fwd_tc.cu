@@ -82,7 +82,8 @@ constexpr float kRescaleLog2 = 8.0f;
 
 // One work item: query tiles A = 2p and B = 2p + 1 of one (batch, q head).
 // Items are numbered longest first (pair index descending, then batch and
-// head), and CTA c of a grid of G takes items c, c + G, c + 2G, ...
+// head), and CTA c of a grid of G takes one item per round of G in snake
+// order (snake_item): c, 2G - 1 - c, 2G + c, ...
 //
 // The key tiles an item visits, in order: the gathered keep tiles of the
 // longer gathered list, then the dense band from A's window start to B's
@@ -128,7 +129,7 @@ __device__ __forceinline__ void read_item_records(IndexPtrs idx, const Geom& geo
 // kCtaItems items.
 __device__ __forceinline__ void item_records(IndexPtrs idx, const int4* s_rec, int item,
                                              const Geom& geo, int4& ba, int4& bb, int4& sq) {
-  const int k = (item - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x);
+  const int k = item / static_cast<int>(gridDim.x);  // the round, = the CTA's k-th item
   if (k < kCtaItems) {
     ba = s_rec[3 * k];
     bb = s_rec[3 * k + 1];
@@ -244,10 +245,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
   const int n_win = hdr.n;
-  // records of this CTA's items (item = blockIdx.x + k * G), read once
+  // records of this CTA's items (item = snake_item(k, G)), read once
   __shared__ int4 s_rec[3 * kCtaItems];
   for (int x = threadIdx.x; x < kCtaItems; x += blockDim.x) {
-    const int item = static_cast<int>(blockIdx.x) + x * G;
+    const int item = snake_item(x, G);
     if (item < n_items) read_item_records(idx, geo, item, s_rec[3 * x], s_rec[3 * x + 1],
                                           s_rec[3 * x + 2]);
   }
@@ -266,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_vk);
       int n = 0, kq = 0;  // K/V stages and query pairs loaded
       bool ok = true;
-      for (int it = blockIdx.x; ok && it < n_items; it += G) {
+      for (int it = blockIdx.x; ok && it < n_items; it = snake_item(it / G + 1, G)) {
         const PairPlan pl = load_plan(idx, s_rec, it, n_items, geo, full_groups, grp);
         if (!pl.valid) {
           if (!pl.empty) report(status, SEP_ERR_DEVICE_BOUNDS);
@@ -369,13 +370,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = blockIdx.x;
       PairPlan pc = load_plan(idx, s_rec, it, n_items, geo, full_groups, grp);
       while (it < n_items && !pc.valid) {
-        it += G;
+        it = snake_item(it / G + 1, G);
         pc = load_plan(idx, s_rec, it, n_items, geo, full_groups, grp);
       }
       if (it < n_items) {
         int kq = 0, qs = 0, n = 0;  // current item's index and Q buffer; K/V stage count
         int u = pc.next(-1);
-        int itn = it + G;
+        int itn = snake_item(it / G + 1, G);
         PairPlan pn = load_plan(idx, s_rec, itn, n_items, geo, full_groups, grp);  // prefetched
         ok = mbar_wait_warp(&q_full[0], 0, status) && mbar_wait_warp(&kv_full[0], 0, status);
         tc_fence_after();
@@ -390,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool same = un < pc.nT;
           if (!same) {
             while (itn < n_items && !pn.valid) {
-              itn += G;
+              itn = snake_item(itn / G + 1, G);
               pn = load_plan(idx, s_rec, itn, n_items, geo, full_groups, grp);
             }
             if (itn < n_items) un = pn.next(-1);
@@ -421,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++kq;
             qs = qsn;
             ci0 = ci1 = 0;
-            itn = it + G;
+            itn = snake_item(it / G + 1, G);
             pn = load_plan(idx, s_rec, itn, n_items, geo, full_groups, grp);
           }
           u = un;
@@ -443,9 +444,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     int cnt = 0, ko = 0;  // S tiles and items finished by this query tile
     bool ok = true;
     PairPlan pn = load_plan(idx, s_rec, blockIdx.x, n_items, geo, full_groups, grp);
-    for (int it = blockIdx.x; ok && it < n_items; it += G) {
+    for (int it = blockIdx.x; ok && it < n_items; it = snake_item(it / G + 1, G)) {
       const PairPlan pl = pn;
-      pn = load_plan(idx, s_rec, it + G, n_items, geo, full_groups, grp);  // prefetch the next item
+      pn = load_plan(idx, s_rec, snake_item(it / G + 1, G), n_items, geo, full_groups,
+                     grp);  // prefetch the next item
       if (!pl.valid || (x == 1 && !pl.hasB)) continue;
       const int b = pl.b, h = pl.h;
       const int i = (pl.tA + x) * 128 + r;

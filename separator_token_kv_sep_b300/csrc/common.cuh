@@ -365,6 +365,16 @@ inline cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 bl
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// The k-th work item of a persistent CTA: items are dealt in rounds of one
+// per CTA, forwards in even rounds and backwards in odd ones, so a CTA that
+// drew one of the larger items of a round (items come longest first) draws
+// one of the smaller ones of the next.  Strictly increasing in k, and item /
+// ctas recovers k.
+__device__ __forceinline__ int snake_item(int k, int ctas) {
+  return k * ctas + ((k & 1) ? ctas - 1 - static_cast<int>(blockIdx.x)
+                             : static_cast<int>(blockIdx.x));
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
