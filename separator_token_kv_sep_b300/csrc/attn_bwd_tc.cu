@@ -308,7 +308,7 @@ __global__ void __launch_bounds__(kPrepThreads)
   const int lane = threadIdx.x & 31;
   const size_t w0 = (size_t)(blockIdx.x - 1) * WPB + (threadIdx.x >> 5);
   const size_t nw = (size_t)(gridDim.x - 1) * WPB;
-  const size_t gunits = static_cast<size_t>(keep_units(geo.B, geo.Hkv, geo.L));
+  const size_t gunits = static_cast<size_t>(live_keep_units(idx, geo, lane));
   const size_t sunits = (size_t)geo.B * geo.Hq * geo.T * 128 / kPrepRows;
   for (size_t u = w0; u < gunits + sunits; u += nw) {
     if (u < gunits)

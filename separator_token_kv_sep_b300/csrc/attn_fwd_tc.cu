@@ -54,8 +54,8 @@ __global__ void __launch_bounds__(256)
   grid_dep_wait();
   const IndexHeader hdr = *idx.header;
   if (!header_matches(hdr, geo)) return;
-  const int units = keep_units(geo.B, geo.Hkv, geo.L);
   const int lane = threadIdx.x & 31;
+  const int units = live_keep_units(idx, geo, lane);
   for (int u = blockIdx.x * 8 + (threadIdx.x >> 5); u < units; u += gridDim.x * 8)
     gather_keep_unit<D>(idx, geo, k, v, kk, vk, nullptr, nullptr, u, lane, status);
 }

@@ -28,6 +28,21 @@ __host__ __device__ inline int keep_units(int B, int Hkv, int L) {
   return B * Hkv * ((L + kKeepUnitRows - 1) / kKeepUnitRows);
 }
 
+// Units below the largest keep count of the batch rounded up to a 128-row
+// tile (units run pair-fastest, so the later ones hold neither keep rows nor
+// the zero rows that pad a sequence's last gathered tile); computed by each
+// calling warp.
+__device__ __forceinline__ int live_keep_units(IndexPtrs idx, const Geom& geo, int lane) {
+  int mc = 0;
+  for (int b = lane; b < geo.B; b += 32) {
+    const SeqRec sr = idx.seq[b];
+    if (seq_ok(sr, geo)) mc = max(mc, min(max(idx.keep_count[b], 0), sr.len));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mc = max(mc, __shfl_xor_sync(0xffffffffu, mc, off));
+  return geo.B * geo.Hkv * ((mc + 127) / 128 * (128 / kKeepUnitRows));
+}
+
 // Copies the keep rows of one unit (and, if dk_keep is set, zeroes the rows
 // of the fp32 gradient accumulators dk_keep / dv_keep below the keep count,
 // the only ones that are added to and read).  A keep position outside its
