@@ -297,6 +297,20 @@ __global__ void __launch_bounds__(kThreads, 4)
   int* surv_pos = surv_src + (s > 0 ? s : 1);
 
   const size_t mh = (size_t)sq * args.Hkv + g;  // (sequence, kv head)
+  // the G query heads' values, loaded by the consumer threads before the
+  // plan so that their latency passes while it is made
+  constexpr int QPER = (G * HALF + kConsumerWarps * 32 - 1) / (kConsumerWarps * 32);
+  float qx1[QPER], qx2[QPER];
+#pragma unroll
+  for (int j = 0; j < QPER; ++j) {
+    const int e = tid + j * kConsumerWarps * 32;
+    qx1[j] = qx2[j] = 0.f;
+    if (q != nullptr && warp < kConsumerWarps && e < G * HALF) {
+      const uint16_t* qr = q + (((size_t)sq * args.Hq) + g * G + e / HALF) * D;
+      qx1[j] = __uint_as_float((uint32_t)qr[e % HALF] << 16);
+      qx2[j] = __uint_as_float((uint32_t)qr[e % HALF + HALF] << 16);
+    }
+  }
   const Meta m = cp.meta[mh];
   const uint8_t* sepr = cp.issep + mh * NSL;
   const bool ok = !(m.n_init < 0 || m.n_init > a || m.n_sep < 0 || m.n_sep > s || m.n_pw < 0 ||
@@ -468,14 +482,16 @@ __global__ void __launch_bounds__(kThreads, 4)
       // rotated queries of the G heads at position N-1 into sQ[h][D] (fp32)
       if (ok) {
         const float2* cs_row = cp.rope + (size_t)(N - 1) * HALF;
-        for (int e = tid; e < G * HALF; e += kConsumerWarps * 32) {
-          const int hh = e / HALF, i = e % HALF;
-          const uint16_t* qr = q + (((size_t)sq * args.Hq) + g * G + hh) * D;
-          const float2 cs = cs_row[i];
-          const float x1 = __uint_as_float((uint32_t)qr[i] << 16);
-          const float x2 = __uint_as_float((uint32_t)qr[i + HALF] << 16);
-          sQ[hh * D + i] = x1 * cs.x - x2 * cs.y;
-          sQ[hh * D + i + HALF] = x2 * cs.x + x1 * cs.y;
+#pragma unroll
+        for (int j = 0; j < QPER; ++j) {
+          const int e = tid + j * kConsumerWarps * 32;
+          if (e < G * HALF) {
+            const int hh = e / HALF, i = e % HALF;
+            const float2 cs = cs_row[i];
+            const float x1 = qx1[j], x2 = qx2[j];
+            sQ[hh * D + i] = x1 * cs.x - x2 * cs.y;
+            sQ[hh * D + i + HALF] = x2 * cs.x + x1 * cs.y;
+          }
         }
       }
       consumer_sync();
@@ -690,6 +706,40 @@ __global__ void __launch_bounds__(kThreads, 4)
         }
       }
       consumer_sync();
+      if (split == 1) {
+        // the whole cache is this CTA's: the output is final.  Per thread 8
+        // consecutive dims of one head: the warps' weights once, one 16-byte
+        // store.
+        for (int e8 = tid; e8 < G * D / 8; e8 += kConsumerWarps * 32) {
+          const int hh = (8 * e8) / D, x0 = (8 * e8) % D;
+          float M = -INFINITY;
+#pragma unroll
+          for (int r = 0; r < kConsumerWarps; ++r) M = fmaxf(M, sW[(r * G + hh) * (D + 2) + D]);
+          float f[kConsumerWarps], den = 0.f;
+#pragma unroll
+          for (int r = 0; r < kConsumerWarps; ++r) {
+            const float* ws = sW + (r * G + hh) * (D + 2);
+            f[r] = ws[D] != -INFINITY ? exp2f(ws[D] - M) : 0.f;
+            den = fmaf(f[r], ws[D + 1], den);
+          }
+          const float inv = 1.f / den;
+          uint32_t pk[4];
+#pragma unroll
+          for (int j = 0; j < 8; j += 2) {
+            float n0 = 0.f, n1 = 0.f;
+#pragma unroll
+            for (int r = 0; r < kConsumerWarps; ++r) {
+              const float* ws = sW + (r * G + hh) * (D + 2) + x0 + j;
+              n0 = fmaf(f[r], ws[0], n0);
+              n1 = fmaf(f[r], ws[1], n1);
+            }
+            pk[j / 2] = pack_bf16x2(n0 * inv, n1 * inv);
+          }
+          if (att_ok)
+            *reinterpret_cast<uint4*>(out + (((size_t)sq * args.Hq) + g * G + hh) * D + x0) =
+                make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+      } else {
       for (int e = tid; e < G * D; e += kConsumerWarps * 32) {
         const int hh = e / D, x = e % D;
         float M = -INFINITY;
@@ -705,19 +755,12 @@ __global__ void __launch_bounds__(kThreads, 4)
             den = fmaf(f, ws[D + 1], den);
           }
         }
-        if (split == 1) {  // the whole cache is this CTA's: the output is final
-          if (att_ok) {
-            const __nv_bfloat16 bv = __float2bfloat16_rn(num / den);
-            out[(((size_t)sq * args.Hq) + g * G + hh) * D + x] =
-                *reinterpret_cast<const uint16_t*>(&bv);
-          }
-        } else {
-          sAcc[e] = num;
-          if (x == 0) {
-            sM[hh] = M;
-            sL[hh] = den;
-          }
+        sAcc[e] = num;
+        if (x == 0) {
+          sM[hh] = M;
+          sL[hh] = den;
         }
+      }
       }
     }
     att_ok = __syncthreads_and(att_ok || warp == kConsumerWarps);
