@@ -451,14 +451,22 @@ __global__ void __launch_bounds__(kThreads, 4)
           const int c0 = k0 + ch * CH, n = min(k1, c0 + CH) - c0;
           uint8_t* stg = dsm + L.ring + st * SS::STAGE;
           const int* sl_c = reinterpret_cast<const int*>(dsm + L.slots) + (c0 - k0);
-          for (int x = lane; x < n * CPR; x += 32) {
-            const int r = x / CPR, u = x % CPR;  // CPR is a power of two
+          // lane l copies unit l % CPR of rows l / CPR, l / CPR + 32 / CPR, ...
+          constexpr int RPI = 32 / CPR;  // rows per pass of the warp
+          const int u = lane % CPR, r0 = lane / CPR;
+          auto copy_row = [&](int r) {
             const int slot = sl_c[r];
             const uint16_t* bk = slot < 0 ? k_new + new_off : kh + (size_t)slot * D;
             const uint16_t* bv = slot < 0 ? v_new + new_off : vh + (size_t)slot * D;
             const int du = staged_unit(r, u, SS::PU);
             cp_async16(stg + du, bk + 8 * u);
             cp_async16(stg + SS::OFF_V + du, bv + 8 * u);
+          };
+          if (n == CH) {  // a full chunk: a fixed trip count the compiler unrolls
+#pragma unroll
+            for (int r = r0; r < CH; r += RPI) copy_row(r);
+          } else {
+            for (int r = r0; r < n; r += RPI) copy_row(r);
           }
           cp_async_arrive(&full_bar[st]);
         }
@@ -639,10 +647,10 @@ __global__ void __launch_bounds__(kThreads, 4)
           lrun0 *= al0;
           lrun1 *= al1;
         }
-        const float p00 = s00 == -INFINITY ? 0.f : exp2f(s00 - mrun0);
-        const float p01 = s01 == -INFINITY ? 0.f : exp2f(s01 - mrun1);
-        const float p10 = s10 == -INFINITY ? 0.f : exp2f(s10 - mrun0);
-        const float p11 = s11 == -INFINITY ? 0.f : exp2f(s11 - mrun1);
+        const float p00 = s00 == -INFINITY ? 0.f : fast_exp2(s00 - mrun0);
+        const float p01 = s01 == -INFINITY ? 0.f : fast_exp2(s01 - mrun1);
+        const float p10 = s10 == -INFINITY ? 0.f : fast_exp2(s10 - mrun0);
+        const float p11 = s11 == -INFINITY ? 0.f : fast_exp2(s11 - mrun1);
         lrun0 += p00 + p10;  // this lane's entries; summed over lanes at the end
         lrun1 += p01 + p11;
         // P^T fragments: rows of P^T(entries x heads) transposed in registers
