@@ -405,70 +405,92 @@ __global__ void __launch_bounds__(kThreads, 4)
     const int k1 = (int)(((long long)N * (rank + 1)) / split);
     const int ne = ok ? k1 - k0 : 0;
     const int n_chunks = (ne + CH - 1) / CH;
-    // where each entry of the share sits before the update
-    {
-      int* slots = reinterpret_cast<int*>(dsm + L.slots);
-      const int rS = pl.I0, rV = rS + pl.SK, rW = rV + pl.SV, rN = N - 1;
-      for (int e = k0 + tid; e < k0 + ne; e += kThreads) {
-        int slot;
-        if (e == rN) {
-          slot = -1;
-        } else if (e < rS) {
-          slot = e;
-        } else if (e < rV) {
-          int x = pl.sk0 + (e - rS);  // < 2 s
-          slot = a + (x >= s ? x - s : x);
-        } else if (e < rW) {
-          slot = surv_src[e - rV];
-        } else {
-          int x = pl.pw0 + (e - rW);  // < 2 ring
-          slot = a + s + (x >= ring ? x - ring : x);
+    // where each entry of the share sits before the update (-1: the new
+    // token, read from the caller's input)
+    const int rS = pl.I0, rV = rS + pl.SK, rW = rV + pl.SV, rN = N - 1;
+    auto slot_of = [&](int e) -> int {
+      if (e == rN) return -1;
+      if (e < rS) return e;
+      if (e < rV) {
+        const int x = pl.sk0 + (e - rS);  // < 2 s
+        return a + (x >= s ? x - s : x);
+      }
+      if (e < rW) return surv_src[e - rV];
+      const int x = pl.pw0 + (e - rW);  // < 2 ring
+      return a + s + (x >= ring ? x - ring : x);
+    };
+    int* slots = reinterpret_cast<int*>(dsm + L.slots);
+    const uint16_t* kh = cp.k + head_off;
+    const uint16_t* vh = cp.v + head_off;
+    const size_t new_off = mh * D;  // [S][Hkv][D] inputs
+    // The copy warp's copies of chunk ch, entries [c0, c0 + n): each lane
+    // copies 16-byte units of their K and V rows, from their slots in
+    // `slots`, then arrives on the stage's full barrier.
+    auto issue_chunk = [&](int ch) {
+      const int st = ch % NST;
+      const int c0 = k0 + ch * CH, n = min(k1, c0 + CH) - c0;
+      uint8_t* stg = dsm + L.ring + st * SS::STAGE;
+      const int* sl_c = slots + (c0 - k0);
+      // lane l copies unit l % CPR of rows l / CPR, l / CPR + 32 / CPR, ...
+      constexpr int RPI = 32 / CPR;  // rows per pass of the warp
+      const int u = lane % CPR, r0 = lane / CPR;
+      auto copy_row = [&](int r) {
+        const int slot = sl_c[r];
+        const uint16_t* bk = slot < 0 ? k_new + new_off : kh + (size_t)slot * D;
+        const uint16_t* bv = slot < 0 ? v_new + new_off : vh + (size_t)slot * D;
+        const int du = staged_unit(r, u, SS::PU);
+        cp_async16(stg + du, bk + 8 * u);
+        cp_async16(stg + SS::OFF_V + du, bv + 8 * u);
+      };
+      if (n == CH) {  // a full chunk: a fixed trip count the compiler unrolls
+#pragma unroll
+        for (int r = r0; r < CH; r += RPI) copy_row(r);
+      } else {
+        for (int r = r0; r < n; r += RPI) copy_row(r);
+      }
+      cp_async_arrive(&full_bar[st]);
+    };
+    if (warp == kConsumerWarps) {
+      // the copy warp sets up the ring and starts the first chunk from slots
+      // it computes itself, while the other warps list the rest
+      if (lane == 0) {
+        for (int st = 0; st < NST; ++st) {
+          mbar_init(&full_bar[st], 32);  // the copy lanes' cp.async arrivals
+          mbar_init(&empty_bar[st], kConsumerWarps);
         }
-        slots[e - k0] = slot;
+        fence_mbar_init();
+      }
+      if (lane < min(ne, CH)) slots[lane] = slot_of(k0 + lane);
+      __syncwarp();
+      if (ne > 0) issue_chunk(0);
+    } else if (ok) {
+      // rotated queries of the G heads at position N-1 into sQ[h][D] (fp32)
+      const float2* cs_row = cp.rope + (size_t)(N - 1) * HALF;
+#pragma unroll
+      for (int j = 0; j < QPER; ++j) {
+        const int e = tid + j * kConsumerWarps * 32;
+        if (e < G * HALF) {
+          const int hh = e / HALF, i = e % HALF;
+          const float2 cs = cs_row[i];
+          const float x1 = qx1[j], x2 = qx2[j];
+          sQ[hh * D + i] = x1 * cs.x - x2 * cs.y;
+          sQ[hh * D + i + HALF] = x2 * cs.x + x1 * cs.y;
+        }
       }
     }
-    if (tid == 0) {
-      for (int st = 0; st < NST; ++st) {
-        mbar_init(&full_bar[st], 32);  // the producer lanes' cp.async arrivals
-        mbar_init(&empty_bar[st], kConsumerWarps);
-      }
-      fence_mbar_init();
-    }
+    for (int e = k0 + CH + tid; e < k0 + ne; e += kThreads) slots[e - k0] = slot_of(e);
     __syncthreads();
 
     if (warp == kConsumerWarps) {
       // ------------------------------------------------------------ producer
-      // Chunk ch holds entries [c0, c0 + n): each lane copies 16-byte units
-      // of their K and V rows, from the slot an entry has before the update
-      // or from the caller's new token.
+      // chunk 0 is issued; chunk ch reuses the stage of chunk ch - NST once
+      // both consumer warps have released it
       if (ne > 0) {
-        const uint16_t* kh = cp.k + head_off;
-        const uint16_t* vh = cp.v + head_off;
-        const size_t new_off = mh * D;  // [S][Hkv][D] inputs
-        for (int ch = 0; ch < n_chunks; ++ch) {
-          const int st = ch % NST;
-          if (ch >= NST && !mbar_wait_warp(&empty_bar[st], ((ch / NST) - 1) & 1, status)) break;
-          const int c0 = k0 + ch * CH, n = min(k1, c0 + CH) - c0;
-          uint8_t* stg = dsm + L.ring + st * SS::STAGE;
-          const int* sl_c = reinterpret_cast<const int*>(dsm + L.slots) + (c0 - k0);
-          // lane l copies unit l % CPR of rows l / CPR, l / CPR + 32 / CPR, ...
-          constexpr int RPI = 32 / CPR;  // rows per pass of the warp
-          const int u = lane % CPR, r0 = lane / CPR;
-          auto copy_row = [&](int r) {
-            const int slot = sl_c[r];
-            const uint16_t* bk = slot < 0 ? k_new + new_off : kh + (size_t)slot * D;
-            const uint16_t* bv = slot < 0 ? v_new + new_off : vh + (size_t)slot * D;
-            const int du = staged_unit(r, u, SS::PU);
-            cp_async16(stg + du, bk + 8 * u);
-            cp_async16(stg + SS::OFF_V + du, bv + 8 * u);
-          };
-          if (n == CH) {  // a full chunk: a fixed trip count the compiler unrolls
-#pragma unroll
-            for (int r = r0; r < CH; r += RPI) copy_row(r);
-          } else {
-            for (int r = r0; r < n; r += RPI) copy_row(r);
-          }
-          cp_async_arrive(&full_bar[st]);
+        for (int ch = 1; ch < n_chunks; ++ch) {
+          if (ch >= NST &&
+              !mbar_wait_warp(&empty_bar[ch % NST], ((ch / NST) - 1) & 1, status))
+            break;
+          issue_chunk(ch);
         }
         // nothing this lane copies may land after the CTA is gone
         asm volatile("cp.async.wait_all;" ::: "memory");
@@ -487,22 +509,7 @@ __global__ void __launch_bounds__(kThreads, 4)
       // the pairs RoPE rotates together stay in one lane.  In the PV product
       // its m rows g, g+8 of m-tile mt are dims LD g + mt and LD g + MT + mt.
       constexpr int LD = SS::LD, NLO = SS::NLO, MT = SS::MT;
-      // rotated queries of the G heads at position N-1 into sQ[h][D] (fp32)
-      if (ok) {
-        const float2* cs_row = cp.rope + (size_t)(N - 1) * HALF;
-#pragma unroll
-        for (int j = 0; j < QPER; ++j) {
-          const int e = tid + j * kConsumerWarps * 32;
-          if (e < G * HALF) {
-            const int hh = e / HALF, i = e % HALF;
-            const float2 cs = cs_row[i];
-            const float x1 = qx1[j], x2 = qx2[j];
-            sQ[hh * D + i] = x1 * cs.x - x2 * cs.y;
-            sQ[hh * D + i + HALF] = x2 * cs.x + x1 * cs.y;
-          }
-        }
-      }
-      consumer_sync();
+      // (sQ was written before the CTA barrier above)
       const int gq = lane >> 2, tq = lane & 3;
       // Q^T fragments (B operand): b0 = q[gq][dims +0, +1], b1 = q[gq][+2, +3]
       uint32_t qf[SS::NSLAB][2];
