@@ -265,6 +265,14 @@ __device__ __forceinline__ uint32_t word_of(const uint4& u, int i) {
 __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
 }
+// The consumer warps publish the slot list to the copy warp through named
+// barrier 2: they arrive without waiting, the copy warp waits.
+__device__ __forceinline__ void slots_published() {
+  asm volatile("bar.arrive 2, %0;" ::"n"(kThreads) : "memory");
+}
+__device__ __forceinline__ void wait_slots_published() {
+  asm volatile("bar.sync 2, %0;" ::"n"(kThreads) : "memory");
+}
 
 // ---------------------------------------------------------------------------
 // The step kernel
@@ -311,6 +319,15 @@ __global__ void __launch_bounds__(kThreads, 4)
       qx2[j] = __uint_as_float((uint32_t)qr[e % HALF + HALF] << 16);
     }
   }
+  // the copy ring's barriers, initialised before any role can touch them
+  if (tid == 0) {
+    for (int st = 0; st < NST; ++st) {
+      mbar_init(&full_bar[st], 32);  // the copy lanes' cp.async arrivals
+      mbar_init(&empty_bar[st], kConsumerWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
   const Meta m = cp.meta[mh];
   const uint8_t* sepr = cp.issep + mh * NSL;
   const bool ok = !(m.n_init < 0 || m.n_init > a || m.n_sep < 0 || m.n_sep > s || m.n_pw < 0 ||
@@ -451,35 +468,33 @@ __global__ void __launch_bounds__(kThreads, 4)
       cp_async_arrive(&full_bar[st]);
     };
     if (warp == kConsumerWarps) {
-      // the copy warp sets up the ring and starts the first chunk from slots
-      // it computes itself, while the other warps list the rest
-      if (lane == 0) {
-        for (int st = 0; st < NST; ++st) {
-          mbar_init(&full_bar[st], 32);  // the copy lanes' cp.async arrivals
-          mbar_init(&empty_bar[st], kConsumerWarps);
-        }
-        fence_mbar_init();
-      }
+      // the copy warp starts the first chunk from slots it computes itself,
+      // while the consumer warps list the rest
       if (lane < min(ne, CH)) slots[lane] = slot_of(k0 + lane);
       __syncwarp();
       if (ne > 0) issue_chunk(0);
-    } else if (ok) {
-      // rotated queries of the G heads at position N-1 into sQ[h][D] (fp32)
-      const float2* cs_row = cp.rope + (size_t)(N - 1) * HALF;
+      wait_slots_published();
+    } else {
+      for (int e = k0 + CH + tid; e < k0 + ne; e += kConsumerWarps * 32)
+        slots[e - k0] = slot_of(e);
+      slots_published();
+      if (ok) {
+        // rotated queries of the G heads at position N-1 into sQ[h][D] (fp32)
+        const float2* cs_row = cp.rope + (size_t)(N - 1) * HALF;
 #pragma unroll
-      for (int j = 0; j < QPER; ++j) {
-        const int e = tid + j * kConsumerWarps * 32;
-        if (e < G * HALF) {
-          const int hh = e / HALF, i = e % HALF;
-          const float2 cs = cs_row[i];
-          const float x1 = qx1[j], x2 = qx2[j];
-          sQ[hh * D + i] = x1 * cs.x - x2 * cs.y;
-          sQ[hh * D + i + HALF] = x2 * cs.x + x1 * cs.y;
+        for (int j = 0; j < QPER; ++j) {
+          const int e = tid + j * kConsumerWarps * 32;
+          if (e < G * HALF) {
+            const int hh = e / HALF, i = e % HALF;
+            const float2 cs = cs_row[i];
+            const float x1 = qx1[j], x2 = qx2[j];
+            sQ[hh * D + i] = x1 * cs.x - x2 * cs.y;
+            sQ[hh * D + i + HALF] = x2 * cs.x + x1 * cs.y;
+          }
         }
       }
+      consumer_sync();
     }
-    for (int e = k0 + CH + tid; e < k0 + ne; e += kThreads) slots[e - k0] = slot_of(e);
-    __syncthreads();
 
     if (warp == kConsumerWarps) {
       // ------------------------------------------------------------ producer
@@ -509,7 +524,6 @@ __global__ void __launch_bounds__(kThreads, 4)
       // the pairs RoPE rotates together stay in one lane.  In the PV product
       // its m rows g, g+8 of m-tile mt are dims LD g + mt and LD g + MT + mt.
       constexpr int LD = SS::LD, NLO = SS::NLO, MT = SS::MT;
-      // (sQ was written before the CTA barrier above)
       const int gq = lane >> 2, tq = lane & 3;
       // Q^T fragments (B operand): b0 = q[gq][dims +0, +1], b1 = q[gq][+2, +3]
       uint32_t qf[SS::NSLAB][2];
