@@ -808,17 +808,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float4* sst =
             reinterpret_cast<const float4*>(smem + C::OFF_STAT + stg * 1024) + 32 * half;
-#pragma unroll 1
-        for (int cc = 0; cc < 2; ++cc) {
-          uint32_t sr[32], dr[32], pk[16], dk2[16];
-          tmem_ld32(tb + 32 * cc, sr);
-          tmem_ld32(tb + 64 + 32 * cc, dr);
-          tmem_ld_wait();
-          const uint32_t w = cc ? vm[1] : vm[0];
-          const bool full = __all_sync(0xffffffffu, w == 0xffffffffu);
+        // four chunks of 16 columns; the next chunk's S^T and dP^T loads are
+        // in flight while this one is computed (a wait covers every load
+        // issued before it)
+        uint32_t sa[16], da[16], sb[16], db[16];
+        tmem_ld16(tb, sa);
+        tmem_ld16(tb + 64, da);
+        tmem_ld_wait();
+        tmem_regs_ready16(sa);
+        tmem_regs_ready16(da);
 #pragma unroll
-          for (int x = 0; x < 32; x += 2) {
-            const float4 st2 = sst[16 * cc + x / 2];  // columns (x, x+1): (-lse, -delta)
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t* sr = (cc & 1) ? sb : sa;
+          uint32_t* dr = (cc & 1) ? db : da;
+          uint32_t* sn = (cc & 1) ? sa : sb;
+          uint32_t* dn = (cc & 1) ? da : db;
+          if (cc < 3) {
+            tmem_ld16(tb + 16 * (cc + 1), sn);
+            tmem_ld16(tb + 64 + 16 * (cc + 1), dn);
+          }
+          uint32_t pk[8], dk2[8];
+          const uint32_t w = (vm[cc >> 1] >> (16 * (cc & 1))) & 0xffffu;
+          const bool full = __all_sync(0xffffffffu, w == 0xffffu);
+#pragma unroll
+          for (int x = 0; x < 16; x += 2) {
+            const float4 st2 = sst[8 * cc + x / 2];  // columns (x, x+1): (-lse, -delta)
             float a0, a1, d0, d1;
             ffma2(a0, a1, __uint_as_float(sr[x]), __uint_as_float(sr[x + 1]), scale_log2,
                   scale_log2, st2.x, st2.z);
@@ -834,9 +848,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             dk2[x / 2] = pack_bf16x2(d0, d1);
           }
           // P^T over S^T, dS^T over dP^T: chunk cc lands on columns
-          // [16cc, 16cc+16) of each, which chunk 0's loads already read
-          tmem_st16(tb + 16 * cc, pk);
-          tmem_st16(tb + 64 + 16 * cc, dk2);
+          // [8cc, 8cc+8) of each, which earlier chunks' loads already read
+          tmem_st8(tb + 8 * cc, pk);
+          tmem_st8(tb + 64 + 8 * cc, dk2);
+          if (cc < 3) {
+            tmem_ld_wait();
+            tmem_regs_ready16(sn);
+            tmem_regs_ready16(dn);
+          }
         }
         tmem_st_wait();
         tc_fence_before();
