@@ -79,6 +79,7 @@ struct FwdCfg {
 
 constexpr int kThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-5 softmax A, 6-9 softmax B
 constexpr float kRescaleLog2 = 8.0f;
+constexpr float kRescaleBound = 256.0f;  // 2^kRescaleLog2
 
 // One work item: query tiles A = 2p and B = 2p + 1 of one (batch, q head).
 // Items are numbered longest first (pair index descending, then batch and
@@ -496,65 +497,120 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        // pass 1: the row maximum over the visible columns (S read in two
-        // halves to keep registers for the second pass)
-        float mt = -INFINITY;
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          uint32_t sr[64];
-          tmem_ld32(tS + 64 * hf, sr);
-          tmem_ld32(tS + 64 * hf + 32, sr + 32);
-          tmem_ld_wait();
-#pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            const int cc = 64 * hf + c;
-            if ((vm[cc >> 5] >> (cc & 31)) & 1u) mt = fmaxf(mt, __uint_as_float(sr[c]));
-          }
-        }
-        mt *= scale_log2;  // scale_log2 > 0 keeps the maximum where it is
-        const float m_new = fmaxf(m_used, mt);
-        const bool rescale = m_new > m_used + kRescaleLog2;
-        float alpha = 1.f;
-        if (rescale) {
-          alpha = fast_exp2(m_used - m_new);
-          m_used = m_new;
-        }
-        const float msub = (m_used == -INFINITY) ? 0.f : m_used;
-        // O rescale: S of this tile being ready means the previous P.V of
-        // this query tile has completed (the tensor pipe runs in order)
-        if (ci > 0 && __any_sync(0xffffffffu, rescale)) {
-          uint32_t ob[32];
-#pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            tmem_ld32(tO + c0, ob);
-            tmem_ld_wait();
-#pragma unroll
-            for (int q = 0; q < 32; ++q) ob[q] = __float_as_uint(__uint_as_float(ob[q]) * alpha);
-            tmem_st32(tO + c0, ob);
-          }
-        }
-        // pass 2: P = exp2(S * scale - m) as packed bf16, written over the
-        // first 64 columns of S chunk by chunk (chunk c's P lands on S
-        // columns [16c, 16c+16), all of which have been read by then)
-        float rs = 0.f;
+        // The first tile of a row (or one whose row has seen no visible
+        // column yet) takes two passes: the row maximum, then P.  A later tile
+        // takes one pass against the running maximum m_used: the lazy
+        // rescale keeps every P within 2^kRescaleLog2 while m_used stands.
+        // A chunk holding a larger P (a score more than kRescaleLog2 above
+        // m_used) ends that pass before it is written; the maximum of the
+        // chunks not yet written then sets the new m_used (the written
+        // chunks stayed below the bound, so they cannot hold it), and the
+        // written P, the row sum and O are rescaled.
+        float rs = 0.f, alpha = 1.f;
+        float msub = m_used;
+        int c0 = 0;  // first chunk of 32 columns whose P is not yet written
+        bool need_max = ci == 0 || __any_sync(0xffffffffu, m_used == -INFINITY);
+        if (!need_max) {
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t sr[32], pk[16];
-          tmem_ld32(tS + 32 * c, sr);
-          tmem_ld_wait();
-          const uint32_t w = c == 0 ? vm[0] : c == 1 ? vm[1] : c == 2 ? vm[2] : vm[3];
+          for (; c0 < 4; ++c0) {
+            uint32_t sr[32], pk[16];
+            tmem_ld32(tS + 32 * c0, sr);
+            tmem_ld_wait();
+            const uint32_t w = c0 == 0 ? vm[0] : c0 == 1 ? vm[1] : c0 == 2 ? vm[2] : vm[3];
+            const float rs0 = rs;
+            float pm = 0.f;
 #pragma unroll
-          for (int q = 0; q < 32; q += 2) {
-            float a0, a1;
-            ffma2(a0, a1, __uint_as_float(sr[q]), __uint_as_float(sr[q + 1]), scale_log2,
-                  scale_log2, -msub, -msub);
-            float p0 = fast_exp2(a0), p1 = fast_exp2(a1);
-            p0 = ((w >> q) & 1u) ? p0 : 0.f;
-            p1 = ((w >> (q + 1)) & 1u) ? p1 : 0.f;
-            rs += p0 + p1;
-            pk[q >> 1] = pack_bf16x2(p0, p1);
+            for (int q = 0; q < 32; q += 2) {
+              float a0, a1;
+              ffma2(a0, a1, __uint_as_float(sr[q]), __uint_as_float(sr[q + 1]), scale_log2,
+                    scale_log2, -msub, -msub);
+              float p0 = fast_exp2(a0), p1 = fast_exp2(a1);
+              p0 = ((w >> q) & 1u) ? p0 : 0.f;
+              p1 = ((w >> (q + 1)) & 1u) ? p1 : 0.f;
+              rs += p0 + p1;
+              pm = fmaxf(pm, fmaxf(p0, p1));
+              pk[q >> 1] = pack_bf16x2(p0, p1);
+            }
+            if (__any_sync(0xffffffffu, !(pm <= kRescaleBound))) {
+              rs = rs0;
+              need_max = true;
+              break;
+            }
+            tmem_st16(tS + 16 * c0, pk);
           }
-          tmem_st16(tS + 16 * c, pk);
+        }
+        if (need_max) {
+          // the row maximum over the visible columns of chunks c0 .. 3
+          float mt = -INFINITY;
+#pragma unroll 1
+          for (int c = c0; c < 4; ++c) {
+            uint32_t sr[32];
+            tmem_ld32(tS + 32 * c, sr);
+            tmem_ld_wait();
+            const uint32_t w = c == 0 ? vm[0] : c == 1 ? vm[1] : c == 2 ? vm[2] : vm[3];
+#pragma unroll
+            for (int q = 0; q < 32; ++q)
+              if ((w >> q) & 1u) mt = fmaxf(mt, __uint_as_float(sr[q]));
+          }
+          mt *= scale_log2;  // scale_log2 > 0 keeps the maximum where it is
+          const float m_new = fmaxf(m_used, mt);
+          const bool rescale = m_new > m_used + kRescaleLog2;
+          if (rescale) {
+            alpha = fast_exp2(m_used - m_new);
+            m_used = m_new;
+          }
+          msub = (m_used == -INFINITY) ? 0.f : m_used;
+          if (__any_sync(0xffffffffu, rescale)) {
+            // the P already written (chunks before c0) and the row sum
+#pragma unroll 1
+            for (int c = 0; c < c0; ++c) {
+              uint32_t pw[16];
+              tmem_ld16(tS + 16 * c, pw);
+              tmem_ld_wait();
+#pragma unroll
+              for (int q = 0; q < 16; ++q)
+                pw[q] = pack_bf16x2(__uint_as_float(pw[q] << 16) * alpha,
+                                    __uint_as_float(pw[q] & 0xffff0000u) * alpha);
+              tmem_st16(tS + 16 * c, pw);
+            }
+            rs *= alpha;
+            // O: S of this tile being ready means the previous P.V of this
+            // query tile has completed (the tensor pipe runs in order)
+            if (ci > 0) {
+              uint32_t ob[32];
+#pragma unroll
+              for (int o0 = 0; o0 < D; o0 += 32) {
+                tmem_ld32(tO + o0, ob);
+                tmem_ld_wait();
+#pragma unroll
+                for (int q = 0; q < 32; ++q)
+                  ob[q] = __float_as_uint(__uint_as_float(ob[q]) * alpha);
+                tmem_st32(tO + o0, ob);
+              }
+            }
+          }
+          // P = exp2(S * scale - m) as packed bf16 for chunks c0 .. 3, written
+          // over the first 64 columns of S (chunk c's P lands on S columns
+          // [16c, 16c+16), all of which have been read by then)
+#pragma unroll 1
+          for (int c = c0; c < 4; ++c) {
+            uint32_t sr[32], pk[16];
+            tmem_ld32(tS + 32 * c, sr);
+            tmem_ld_wait();
+            const uint32_t w = c == 0 ? vm[0] : c == 1 ? vm[1] : c == 2 ? vm[2] : vm[3];
+#pragma unroll
+            for (int q = 0; q < 32; q += 2) {
+              float a0, a1;
+              ffma2(a0, a1, __uint_as_float(sr[q]), __uint_as_float(sr[q + 1]), scale_log2,
+                    scale_log2, -msub, -msub);
+              float p0 = fast_exp2(a0), p1 = fast_exp2(a1);
+              p0 = ((w >> q) & 1u) ? p0 : 0.f;
+              p1 = ((w >> (q + 1)) & 1u) ? p1 : 0.f;
+              rs += p0 + p1;
+              pk[q >> 1] = pack_bf16x2(p0, p1);
+            }
+            tmem_st16(tS + 16 * c, pk);
+          }
         }
         l = l * alpha + rs;
         tmem_st_wait();

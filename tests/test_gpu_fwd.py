@@ -65,6 +65,24 @@ def test_bf16_shapes(B, Hq, Hkv, L, d, a, n, p):
     assert_close_abs(lse, rl, 1e-3, "LSE")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_bf16_late_score_jump(d):
+    """Keys far larger than any before them, in the middle of later band
+    tiles: rows whose running maximum was set by earlier tiles meet scores
+    more than 2^8 above it part-way through a tile, so the rows' maximum,
+    the probabilities already formed, the row sums and the outputs are all
+    rescaled there."""
+    L, a, n = 640, 4, 200
+    q, k, v, _, ids = synth.small_prefill(1, 2, 2, L, d, a, n, 0.05, 4242 + d, "bf16", False)
+    k = k.copy()
+    for j0, j1 in ((300, 311), (450, 456), (520, 523)):
+        k[:, :, j0:j1] *= 16.0  # a power of two: still exactly bf16
+    o, lse = gpu_forward(q, k, v, ids, a, n, "bf16")
+    ro, rl = O.attention_forward(q, k, v, ids, synth.SEP_IDS, a, n)
+    assert_close_rel(o, ro, what="O")
+    assert_close_abs(lse, rl, 1e-3 * max(1.0, float(np.max(np.abs(rl)))), "LSE")
+
+
 def test_bf16_streamingllm_reduction():
     q, k, v, _, ids = synth.small_prefill(1, 2, 2, 600, 64, 4, 50, 0.3, 3, "bf16", False)
     o, lse = gpu_forward(q, k, v, ids, 4, 50, "bf16", sep_ids=[])
