@@ -23,7 +23,9 @@
 // max (rescaling O in TMEM only when the max grows by more than 2^8, which
 // keeps every P <= 256 and the final O / l exact), write P as packed bf16
 // over the first half of S, and after the item's last tile normalise O and
-// store it with the LSE.  The next item's query tiles and first S products
+// store it with the LSE.  A row's first tile is read twice (its maximum,
+// then P); later tiles once, against the running max, with a rescale of the
+// part already written when a chunk of the tile exceeds the 2^8 bound.  The next item's query tiles and first S products
 // are issued while the current item finishes, so its epilogue overlaps them.
 // Every mbarrier wait is bounded; on expiry the kernel records
 // SEP_ERR_TIMEOUT, lets its copies and MMAs drain, frees TMEM and returns.
