@@ -499,19 +499,36 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        // The first tile of a row (or one whose row has seen no visible
-        // column yet) takes two passes: the row maximum, then P.  A later tile
-        // takes one pass against the running maximum m_used: the lazy
-        // rescale keeps every P within 2^kRescaleLog2 while m_used stands.
+        // A tile takes one pass against the running maximum m_used (for a
+        // row's first tile, the maximum of its first 32 columns; a row that
+        // has seen no visible column yet takes two passes: the row maximum,
+        // then P): the lazy rescale keeps every P within 2^kRescaleLog2 while
+        // m_used stands.
         // A chunk holding a larger P (a score more than kRescaleLog2 above
         // m_used) ends that pass before it is written; the maximum of the
         // chunks not yet written then sets the new m_used (the written
         // chunks stayed below the bound, so they cannot hold it), and the
         // written P, the row sum and O are rescaled.
         float rs = 0.f, alpha = 1.f;
-        float msub = m_used;
         int c0 = 0;  // first chunk of 32 columns whose P is not yet written
-        bool need_max = ci == 0 || __any_sync(0xffffffffu, m_used == -INFINITY);
+        bool need_max;
+        if (ci == 0) {
+          // a row's first tile: the maximum of its first 32 columns stands
+          // in for the running max (O holds nothing yet), unless a row of the
+          // warp sees none of them
+          uint32_t sr[32];
+          tmem_ld32(tS, sr);
+          tmem_ld_wait();
+          float mt0 = -INFINITY;
+#pragma unroll
+          for (int q = 0; q < 32; ++q)
+            if ((vm[0] >> q) & 1u) mt0 = fmaxf(mt0, __uint_as_float(sr[q]));
+          need_max = __any_sync(0xffffffffu, mt0 == -INFINITY);
+          if (!need_max) m_used = mt0 * scale_log2;
+        } else {
+          need_max = __any_sync(0xffffffffu, m_used == -INFINITY);
+        }
+        float msub = m_used;
         if (!need_max) {
 #pragma unroll 1
           for (; c0 < 4; ++c0) {
