@@ -65,17 +65,24 @@ def test_bf16_shapes(B, Hq, Hkv, L, d, a, n, p):
     assert_close_abs(lse, rl, 1e-3, "LSE")
 
 
-@pytest.mark.parametrize("d", [64, 128])
-def test_bf16_late_score_jump(d):
-    """Keys far larger than any before them, in the middle of later band
-    tiles: rows whose running maximum was set by earlier tiles meet scores
-    more than 2^8 above it part-way through a tile, so the rows' maximum,
-    the probabilities already formed, the row sums and the outputs are all
-    rescaled there."""
+@pytest.mark.parametrize("d,p,spans", [
+    (64, 0.05, ((300, 311), (450, 456), (520, 523))),
+    (128, 0.05, ((300, 311), (450, 456), (520, 523))),
+    # dense separators: the large keys become keep tokens, so later query
+    # tiles meet them in the second 32 columns of their first (gathered) tile
+    (64, 0.5, ((96, 112),)),
+    (128, 0.5, ((96, 112),)),
+])
+def test_bf16_late_score_jump(d, p, spans):
+    """Keys far larger than any before them, part-way through a tile: rows
+    whose running maximum was set by earlier tiles (or, in a row's first
+    tile, by its first 32 columns) meet scores more than 2^8 above it, so the
+    rows' maximum, the probabilities already formed, the row sums and the
+    outputs are all rescaled there."""
     L, a, n = 640, 4, 200
-    q, k, v, _, ids = synth.small_prefill(1, 2, 2, L, d, a, n, 0.05, 4242 + d, "bf16", False)
+    q, k, v, _, ids = synth.small_prefill(1, 2, 2, L, d, a, n, p, 4242 + d, "bf16", False)
     k = k.copy()
-    for j0, j1 in ((300, 311), (450, 456), (520, 523)):
+    for j0, j1 in spans:
         k[:, :, j0:j1] *= 16.0  # a power of two: still exactly bf16
     o, lse = gpu_forward(q, k, v, ids, a, n, "bf16")
     ro, rl = O.attention_forward(q, k, v, ids, synth.SEP_IDS, a, n)
